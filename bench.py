@@ -1,0 +1,508 @@
+"""det_gemm benchmark: one JSON line per run.
+
+A step is one forward and backward pass of the two projections of a
+4096-hidden MLP block through every det_gemm entry-point family (RL-Kernel,
+"Batch-Invariant Deterministic GEMM (det_gemm)": QKV, MLP and LM-head
+matmuls are the hot ops; "Guarantees": forward plus dA and dB):
+
+  h   = det_gemm_fwd(x[8192,4096], W_up[4096,14336])            bf16 out
+  y   = det_gemm_fwd_fp32(h, W_down[14336,4096])                  fp32 out
+  dh  = det_gemm_da(dy[8192,4096], W_down)                        Kc = 4096
+  dWd = det_gemm_db(h, dy)              -> [14336,4096]           Kc = 8192
+  dx  = det_gemm_da(dh, W_up)           -> [8192,4096]            Kc = 14336
+  dWu = det_gemm_db_transposed(x, dh)   -> [14336,4096] ([N,K])   Kc = 8192
+
+Six launches of 2*8192*4096*14336 = 962 GFLOP each. Inputs are seeded
+synthetic BF16 tensors (x ~ N(0,1), weights ~ N(0,0.02), dy ~ N(0,1e-3)).
+Every launch reads more than the 129 MB L2, so no flush is needed.
+
+--impl reference times the CPU oracle (plain C, the same arithmetic) on a
+bounded row sample of the same six products.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads as W  # noqa: E402
+
+M_TOK, D_MODEL, D_FF = 8192, 4096, 14336
+FLOP_PER_GEMM = 2 * M_TOK * D_MODEL * D_FF
+LAUNCHES = [
+    # name, kernel instance, contraction length
+    ("fwd_up", "bf16_kmn", D_MODEL),
+    ("fwd_fp32_down", "f32_kmn", D_FF),
+    ("da_down", "bf16_kk", D_MODEL),
+    ("db_down", "bf16_mnmn", M_TOK),
+    ("da_up", "bf16_kk", D_FF),
+    ("db_transposed_up", "bf16_mnmn", M_TOK),
+]
+WORKLOAD = ("mlp_fwd_bwd: x[8192,4096] W_up[4096,14336] W_down[14336,4096] dy[8192,4096]; "
+            "fwd, fwd_fp32, da x2, db, db_transposed")
+METRIC = "det_gemm BF16 TFLOP/s (fwd, dA, dB) and % of dense BF16 tensor roofline"
+L2_NOTE = "inputs larger than L2 (each launch reads >= 176 MB of operands; L2 is 129 MB); no flush"
+
+
+# ------------------------------------------------------------------ utils
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return dict(bf16_burst=float(d["bf16_tflops"]), bf16_sustained=float(d["bf16_tflops_sustained"]),
+                    hbm=float(d["hbm_gbs"]), source="measured")
+    except Exception:
+        return dict(bf16_burst=1900.0, bf16_sustained=1700.0, hbm=6800.0, source="fallback")
+
+
+def kernel_source_hash() -> str:
+    csrc = os.path.join(ROOT, "invariant_deterministic_gemm_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(f.encode() + b"\0" + fh.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_from_profiles(kernel: str):
+    """DRAM bytes per launch of `kernel` on this workload, from the committed
+    ncu summary, if it was taken on the current kernel sources."""
+    path = os.path.join(ROOT, "profiles", "det_gemm_%s_mlp.md" % kernel)
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m = re.search(r"kernel_source_sha:\s*([0-9a-f]+)", text)
+    t = re.search(r"dram_bytes_per_full_launch:\s*([0-9.eE+]+)", text)
+    if not m or not t or m.group(1) != kernel_source_hash():
+        return None
+    return float(t.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.3)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------- GPU arm
+
+def host_inputs():
+    return dict(
+        x=W.randn_bf16((M_TOK, D_MODEL), W.STD_ACT, W.seed_for(W.MLP, W.T_A)),
+        w_up=W.randn_bf16((D_MODEL, D_FF), W.STD_W, W.seed_for(W.MLP, W.T_B)),
+        w_down=W.randn_bf16((D_FF, D_MODEL), W.STD_W, W.seed_for(W.MLP, W.T_B) + 100),
+        dy=W.randn_bf16((M_TOK, D_MODEL), W.STD_DC, W.seed_for(W.MLP, W.T_DC)),
+    )
+
+
+def make_inputs(device):
+    host = host_inputs()
+    return host, {k: v.to(device) for k, v in host.items()}
+
+
+class Step:
+    """The six launches, with preallocated outputs and per-launch events."""
+
+    def __init__(self, dg, dev_in, device):
+        self.dg = dg
+        self.t = dev_in
+        e = lambda r, c, dt=torch.bfloat16: torch.empty((r, c), dtype=dt, device=device)
+        self.h = e(M_TOK, D_FF)
+        self.y = e(M_TOK, D_MODEL, torch.float32)
+        self.dh = e(M_TOK, D_FF)
+        self.dwd = e(D_FF, D_MODEL)
+        self.dx = e(M_TOK, D_MODEL)
+        self.dwu = e(D_FF, D_MODEL)
+
+    def launches(self):
+        dg, t = self.dg, self.t
+        return [
+            lambda: dg.det_gemm_fwd(t["x"], t["w_up"], out=self.h),
+            lambda: dg.det_gemm_fwd_fp32(self.h, t["w_down"], out=self.y),
+            lambda: dg.det_gemm_da(t["dy"], t["w_down"], out=self.dh),
+            lambda: dg.det_gemm_db(self.h, t["dy"], out=self.dwd),
+            lambda: dg.det_gemm_da(self.dh, t["w_up"], out=self.dx),
+            lambda: dg.det_gemm_db_transposed(t["x"], self.dh, out=self.dwu),
+        ]
+
+    def run(self, events=None):
+        for i, fn in enumerate(self.launches()):
+            if events is not None:
+                events[i][0].record()
+            fn()
+            if events is not None:
+                events[i][1].record()
+
+
+def gpu_arm(args):
+    ws, rank, local = dist_env()
+    import invariant_deterministic_gemm_gb300 as dg
+    dg.lib()   # fails loudly when the library is missing
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+
+    def barrier():
+        if ws > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    host, dev_in = make_inputs(device)
+    step = Step(dg, dev_in, device)
+    for _ in range(args.warmup):
+        step.run()
+    st = dg.det_gemm_check()
+    if st != 0:
+        raise RuntimeError("device status after warm-up: " + dg.status_string(st))
+
+    # ---- device-resident timed region
+    n_l = len(LAUNCHES)
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_l)]
+          for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    start.record()
+    for k in range(args.steps):
+        step.run(ev[k])
+    end.record()
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    barrier()
+    ms_total = start.elapsed_time(end)
+    st = dg.det_gemm_check()
+    if st != 0:
+        raise RuntimeError("device status after the timed region: " + dg.status_string(st))
+    per_launch_ms = np.array([[ev[k][i][0].elapsed_time(ev[k][i][1]) for i in range(n_l)]
+                              for k in range(args.steps)])
+    if ws > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([ms_total], device=device)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms_total = float(tt.item())
+    ms_step = ms_total / args.steps
+    flop_step = FLOP_PER_GEMM * n_l
+    value = flop_step * ws / (ms_step * 1e-3) / 1e12
+
+    # ---- end to end: host buffers in, results back to host, every step
+    pinned = {k: v.pin_memory() for k, v in host.items()}
+    outs_host = {
+        "y": torch.empty((M_TOK, D_MODEL), dtype=torch.float32).pin_memory(),
+        "dx": torch.empty((M_TOK, D_MODEL), dtype=torch.bfloat16).pin_memory(),
+        "dwd": torch.empty((D_FF, D_MODEL), dtype=torch.bfloat16).pin_memory(),
+        "dwu": torch.empty((D_FF, D_MODEL), dtype=torch.bfloat16).pin_memory(),
+    }
+    h2d = sum(v.numel() * v.element_size() for v in pinned.values())
+    d2h = sum(v.numel() * v.element_size() for v in outs_host.values())
+    e2e_steps = max(2, min(args.steps, 10))
+
+    def e2e_step():
+        for k, v in pinned.items():
+            dev_in[k].copy_(v, non_blocking=True)
+        step.run()
+        outs_host["y"].copy_(step.y, non_blocking=True)
+        outs_host["dx"].copy_(step.dx, non_blocking=True)
+        outs_host["dwd"].copy_(step.dwd, non_blocking=True)
+        outs_host["dwu"].copy_(step.dwu, non_blocking=True)
+
+    e2e_step()
+    barrier()
+    torch.cuda.synchronize()
+    s2, e2 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s2.record()
+    for _ in range(e2e_steps):
+        e2e_step()
+    e2.record()
+    torch.cuda.synchronize()
+    barrier()
+    e2e_ms = s2.elapsed_time(e2) / e2e_steps
+    if ws > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([e2e_ms], device=device)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+    st = dg.det_gemm_check()
+    if st != 0:
+        raise RuntimeError("device status after the e2e region: " + dg.status_string(st))
+
+    if rank != 0:
+        if ws > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
+
+    # ---- roofline of the dominant kernel instance
+    pk = peaks()
+    by_kernel = {}
+    for i, (name, kern, kc) in enumerate(LAUNCHES):
+        by_kernel.setdefault(kern, []).extend(per_launch_ms[:, i].tolist())
+    dom = max(by_kernel, key=lambda k: sum(by_kernel[k]))
+    dom_ms = float(np.mean(by_kernel[dom]))
+    achieved = FLOP_PER_GEMM / (dom_ms * 1e-3) / 1e12
+    peak = pk["bf16_sustained"]
+    traffic = traffic_from_profiles(dom)
+    launches = {}
+    for i, (name, kern, kc) in enumerate(LAUNCHES):
+        ms = float(np.mean(per_launch_ms[:, i]))
+        tf = FLOP_PER_GEMM / (ms * 1e-3) / 1e12
+        launches[name] = {"kernel": kern, "kc": kc, "ms": round(ms, 4), "tflops": round(tf, 1),
+                          "frac_of_peak": round(tf / peak, 4)}
+
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) activations, N(0,0.02) weights, N(0,1e-3) output gradients)",
+        "config": {"workload": WORKLOAD, "global_batch_rows": M_TOK * ws, "flop_per_step_per_gpu": flop_step,
+                   "l2": L2_NOTE, "parallelism": "independent replicas, one per GPU" if ws > 1 else "single GPU"},
+        "impl": "det_gemm_gb300",
+        "roofline": {"bound": "tensor", "kernel": "det_gemm_kernel<%s>" % dom, "achieved": round(achieved, 1),
+                     "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                     "peak_source": "%s bf16_tflops_sustained (kernel timed inside a long step)" % pk["source"],
+                     "flop_per_launch": FLOP_PER_GEMM, "traffic": traffic},
+        "launches": launches,
+        "e2e": {"value": round(flop_step * ws / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "path": "Python binding -> C-ABI, pinned host inputs copied in and results copied out every step"},
+        "gpu_launches": n_l * args.steps,
+        "clocks": clk,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(max_seconds=args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+# ------------------------------------------------------------- CPU oracle
+
+def _oracle_problems(host):
+    """The six products of the step as (X, Y) operand views for the oracle,
+    in its X[rows, Kc] @ Y[Kc, cols] form, plus their names."""
+    bits = {k: W.bits(v) for k, v in host.items()}
+    x, wu, wd, dy = bits["x"], bits["w_up"], bits["w_down"], bits["dy"]
+    # h and dh are products of the step itself; for timing the oracle any
+    # BF16 data of the right shape does: the cost does not depend on values.
+    h = W.bits(W.randn_bf16((M_TOK, D_FF), 1.0, 424242))
+    dh = W.bits(W.randn_bf16((M_TOK, D_FF), 1e-3, 424243))
+    return [
+        ("fwd_up", x, wu, False),
+        ("fwd_fp32_down", h, wd, True),
+        ("da_down", dy, wd.T, False),
+        ("db_down", h.T, dy, False),
+        ("da_up", dh, wu.T, False),
+        ("db_transposed_up", dh.T, x, False),
+    ]
+
+
+def cpu_sample(problems, rows, threads):
+    """Times the oracle on the first `rows` rows of each product. Rows are
+    independent, so the FLOP rate on a row sample is the oracle's rate on
+    the whole step."""
+    import oracle
+    t0 = time.perf_counter()
+    flops = 0
+    for _, X, Y, f32 in problems:
+        oracle.gemm(X[:rows], Y, out_fp32=f32, threads=threads)
+        flops += 2 * rows * X.shape[1] * Y.shape[1]
+    dt = time.perf_counter() - t0
+    return flops, dt
+
+
+def cpu_baseline(max_seconds=15.0):
+    """The oracle on a bounded row sample of one step, on all host cores."""
+    import oracle
+    oracle.build()
+    threads = oracle.default_threads()
+    problems = _oracle_problems(host_inputs())
+    f1, t1 = cpu_sample(problems, threads, threads)          # calibration: one row per core
+    reps = max(1, min(64, int(max_seconds / max(t1, 1e-3))))
+    rows = threads * reps
+    flops, dt = cpu_sample(problems, rows, threads)
+    return {"value": round(flops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": "first %d rows of each of the six products of one step (%.3g GFLOP in %.1f s)" % (
+                rows, flops / 1e9, dt)}
+
+
+def reference_arm(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    threads = oracle.default_threads()
+    problems = _oracle_problems(host_inputs())
+    rows = threads          # one row per core of each product per step
+    for _ in range(args.warmup):
+        cpu_sample(problems, rows, threads)
+    flops, dt = 0, 0.0
+    for _ in range(args.steps):
+        f, t = cpu_sample(problems, rows, threads)
+        flops += f
+        dt += t
+    value = flops / dt / 1e12
+    sample = "first %d rows of each of the six products per step (%.3g GFLOP per step)" % (
+        rows, flops / args.steps / 1e9)
+    line = {
+        "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic", "impl": "reference",
+        "config": {"workload": WORKLOAD, "global_batch_rows": M_TOK, "l2": L2_NOTE,
+                   "parallelism": "host cores"},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def single_arm(args):
+    """One entry point of the step on MLP-shaped operands with `rows` token
+    rows instead of 8192, run `iters` times: a small case for profilers."""
+    import invariant_deterministic_gemm_gb300 as dg
+    dg.lib()
+    dev = torch.device("cuda", 0)
+    R = args.rows
+    x = W.randn_bf16((R, D_MODEL), W.STD_ACT, W.seed_for(W.MLP, W.T_A)).to(dev)
+    w_up = W.randn_bf16((D_MODEL, D_FF), W.STD_W, W.seed_for(W.MLP, W.T_B)).to(dev)
+    w_down = W.randn_bf16((D_FF, D_MODEL), W.STD_W, W.seed_for(W.MLP, W.T_B) + 100).to(dev)
+    dy = W.randn_bf16((R, D_MODEL), W.STD_DC, W.seed_for(W.MLP, W.T_DC)).to(dev)
+    h = W.randn_bf16((R, D_FF), 1.0, 424242).to(dev)
+    dh = W.randn_bf16((R, D_FF), 1e-3, 424243).to(dev)
+    calls = {
+        "fwd_up": (lambda: dg.det_gemm_fwd(x, w_up), 2 * R * D_MODEL * D_FF),
+        "fwd_fp32_down": (lambda: dg.det_gemm_fwd_fp32(h, w_down), 2 * R * D_MODEL * D_FF),
+        "da_down": (lambda: dg.det_gemm_da(dy, w_down), 2 * R * D_MODEL * D_FF),
+        "db_down": (lambda: dg.det_gemm_db(h, dy), 2 * R * D_MODEL * D_FF),
+        "da_up": (lambda: dg.det_gemm_da(dh, w_up), 2 * R * D_MODEL * D_FF),
+        "db_transposed_up": (lambda: dg.det_gemm_db_transposed(x, dh), 2 * R * D_MODEL * D_FF),
+    }
+    fn, flop = calls[args.single]
+    times = []
+    for _ in range(args.iters):
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record()
+        fn()
+        e.record()
+        torch.cuda.synchronize()
+        times.append(s.elapsed_time(e))
+    st = dg.det_gemm_check()
+    if st != 0:
+        raise RuntimeError(dg.status_string(st))
+    best = min(times)
+    print(json.dumps({"single": args.single, "rows": R, "ms": times,
+                      "tflops_best": round(flop / (best * 1e-3) / 1e12, 1)}))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="det_gemm", choices=["det_gemm", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--single", default=None, choices=[n for n, _, _ in LAUNCHES],
+                    help="profiling aid: run only this launch, at --rows token rows")
+    ap.add_argument("--rows", type=int, default=2048)
+    ap.add_argument("--iters", type=int, default=3)
+    args = ap.parse_args()
+    if args.single:
+        single_arm(args)
+        return
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be at least 3")
+    if args.impl == "reference":
+        reference_arm(args)
+    else:
+        gpu_arm(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,181 @@
+/*
+ * det_gemm -- batch-invariant deterministic BF16 GEMM for GB300 (sm_103a).
+ *
+ * Operation (RL-Kernel, "Batch-Invariant Deterministic GEMM (det_gemm)",
+ * sections "Guarantees", "Ascend NPU backend" and "Dtypes"):
+ *
+ *   For every output element, with contraction length Kc and pairs
+ *   (x_k, y_k), the K range is cut into L = ceil(Kc / 32) leaves of 32
+ *   consecutive k (the last one may be shorter). Each leaf is summed in FP32
+ *   and rounded once to BF16 (round to nearest, ties to even). The L leaves
+ *   are merged by a fixed mid-split binary tree of BF16 adds:
+ *       T(lo, hi) = leaf[lo]                         if hi - lo == 1
+ *                 = bf16(T(lo, mid) + T(mid, hi))    otherwise, mid = (lo + hi) / 2
+ *   (integer division; for an odd range the left child holds the smaller
+ *   half). No split-K and no TF32: the bits of an output element depend only
+ *   on its own row of the left operand and its own column of the right one,
+ *   never on M, on how rows are chunked or padded, or on which CTA computed
+ *   it. When L is even, a contiguous half-K product is one child of the root,
+ *   so bf16(first_half + second_half) equals the full product bit for bit.
+ *
+ *   Within a leaf the FP32 sum is formed by the tensor core; its internal
+ *   summation order differs from a sequential loop, so a leaf can differ from
+ *   a sequential FP32 leaf by one BF16 unit when it lies next to a rounding
+ *   midpoint. The page claims batch invariance and the half-K property, not
+ *   bit parity across platforms ("Ascend NPU backend", last bullet).
+ *
+ * Conventions for every GEMM entry point below:
+ *   - All matrices are row-major with a leading dimension (ld*) counted in
+ *     elements: element (r, c) of X lives at X[r * ldx + c].
+ *   - Pointers are DEVICE pointers owned by the caller; the library never
+ *     frees or retains them after the call returns.
+ *   - M, N, K are the shapes of the forward product A[M,K] @ B[K,N] = C[M,N];
+ *     the backward entry points take the same M, N, K as their forward.
+ *   - The contraction length Kc (K for the forward entry points, N for dA,
+ *     M for dB) must be <= DET_GEMM_KC_MAX (32768, the page's "training
+ *     contract" cap on the reduction dimension).
+ *   - Base pointers must be 16-byte aligned and ld * sizeof(element) must be
+ *     a multiple of 16 bytes (the tensor-memory-access engine's rule).
+ *   - Work is enqueued on `stream` and the call returns without waiting.
+ *     Argument errors are returned synchronously before anything is
+ *     enqueued. An empty output (a zero dimension) returns DET_GEMM_OK with
+ *     nothing enqueued; Kc == 0 fills the output with +0.
+ *   - Outputs must not overlap inputs (DET_GEMM_ERR_INVALID_ARG otherwise).
+ *   - A device-side failure (a bounded wait that expired) is reported by
+ *     det_gemm_check(), not by the launching call.
+ *   - The library allocates no device memory per call.
+ */
+#ifndef DET_GEMM_H
+#define DET_GEMM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A BF16 value as its raw 16-bit pattern. */
+typedef uint16_t det_gemm_bf16;
+
+/* Same type as cudaStream_t; NULL means the legacy default stream. */
+typedef struct CUstream_st *det_gemm_stream;
+
+typedef enum {
+    DET_GEMM_OK = 0,
+    DET_GEMM_ERR_INVALID_ARG = 1,        /* null pointer, negative size, ld too small, overlap */
+    DET_GEMM_ERR_K_TOO_LARGE = 2,        /* contraction length > DET_GEMM_KC_MAX */
+    DET_GEMM_ERR_ALIGNMENT = 3,          /* base not 16-byte aligned or ld*size not a multiple of 16 */
+    DET_GEMM_ERR_UNSUPPORTED_DEVICE = 4, /* current device is not compute capability 10.3 */
+    DET_GEMM_ERR_LAUNCH = 5,             /* the CUDA launch or set-up failed */
+    DET_GEMM_ERR_TIMEOUT = 6,            /* a device-side bounded wait expired (det_gemm_check) */
+    DET_GEMM_ERR_CUDA = 7                /* another CUDA runtime error (det_gemm_check) */
+} det_gemm_status;
+
+#define DET_GEMM_KC_MAX 32768
+#define DET_GEMM_LEAF 32
+#define DET_GEMM_ABI_VERSION 1
+
+/*
+ * Forward, C[M,N] = A[M,K] @ B[K,N], BF16 out.
+ * ("Guarantees": forward C = A @ B; "Usage": a is [M,K], b is [K,N].)
+ */
+det_gemm_status det_gemm_fwd(const det_gemm_bf16 *A, const det_gemm_bf16 *B, det_gemm_bf16 *C,
+                             int64_t M, int64_t N, int64_t K,
+                             int64_t lda, int64_t ldb, int64_t ldc, det_gemm_stream stream);
+
+/*
+ * Forward with the weight stored [N,K]: C[M,N] = A[M,K] @ W[N,K]^T.
+ * ("Ascend NPU backend": the fwd_rhs_transposed entry point.)
+ */
+det_gemm_status det_gemm_fwd_rhs_transposed(const det_gemm_bf16 *A, const det_gemm_bf16 *W,
+                                            det_gemm_bf16 *C, int64_t M, int64_t N, int64_t K,
+                                            int64_t lda, int64_t ldw, int64_t ldc,
+                                            det_gemm_stream stream);
+
+/*
+ * Forward with FP32 output, C[M,N] = A[M,K] @ B[K,N]. Same leaves and the
+ * same tree, but the leaves stay FP32 and the merges are FP32 adds (round to
+ * nearest even). ("Dtypes": forward_fp32 returns FP32.)
+ */
+det_gemm_status det_gemm_fwd_fp32(const det_gemm_bf16 *A, const det_gemm_bf16 *B, float *C,
+                                  int64_t M, int64_t N, int64_t K,
+                                  int64_t lda, int64_t ldb, int64_t ldc, det_gemm_stream stream);
+
+/*
+ * FP32-output forward with the weight stored [N,K]: C[M,N] = A @ W^T.
+ * Not among the page's names; it is the fwd_fp32 product with the
+ * fwd_rhs_transposed operand layout, for an LM head whose weight is [N,K].
+ */
+det_gemm_status det_gemm_fwd_fp32_rhs_transposed(const det_gemm_bf16 *A, const det_gemm_bf16 *W,
+                                                 float *C, int64_t M, int64_t N, int64_t K,
+                                                 int64_t lda, int64_t ldw, int64_t ldc,
+                                                 det_gemm_stream stream);
+
+/*
+ * Input gradient, dA[M,K] = dC[M,N] @ B[K,N]^T (contraction over N).
+ * ("Guarantees": backward dA = dC.B^T; "Ascend NPU backend": backward reuses
+ * the forward product on transposed operands.)
+ */
+det_gemm_status det_gemm_da(const det_gemm_bf16 *dC, const det_gemm_bf16 *B, det_gemm_bf16 *dA,
+                            int64_t M, int64_t N, int64_t K,
+                            int64_t lddc, int64_t ldb, int64_t ldda, det_gemm_stream stream);
+
+/*
+ * Weight gradient, dB[K,N] = A[M,K]^T @ dC[M,N] (contraction over M).
+ * ("Guarantees": backward dB = A^T.dC.)
+ */
+det_gemm_status det_gemm_db(const det_gemm_bf16 *A, const det_gemm_bf16 *dC, det_gemm_bf16 *dB,
+                            int64_t M, int64_t N, int64_t K,
+                            int64_t lda, int64_t lddc, int64_t lddb, det_gemm_stream stream);
+
+/*
+ * Weight gradient written in the canonical weight layout [N,K]:
+ * dBt[N,K] = (A^T @ dC)^T = dC[M,N]^T @ A[M,K] (contraction over M).
+ * ("Ascend NPU backend": db_transposed stores the weight gradient born
+ * contiguous in [N,K].) Bit for bit the transpose of det_gemm_db.
+ */
+det_gemm_status det_gemm_db_transposed(const det_gemm_bf16 *A, const det_gemm_bf16 *dC,
+                                       det_gemm_bf16 *dBt, int64_t M, int64_t N, int64_t K,
+                                       int64_t lda, int64_t lddc, int64_t lddbt,
+                                       det_gemm_stream stream);
+
+/*
+ * Waits for `stream`, then reports and clears the device status word of the
+ * current device: DET_GEMM_OK, DET_GEMM_ERR_TIMEOUT when a kernel gave up a
+ * bounded wait since the last check, or DET_GEMM_ERR_CUDA when the stream
+ * itself reports a CUDA error.
+ */
+det_gemm_status det_gemm_check(det_gemm_stream stream);
+
+/* Static, human-readable name of a status code. Never NULL. */
+const char *det_gemm_status_string(det_gemm_status status);
+
+/* DET_GEMM_ABI_VERSION of the loaded library. */
+int det_gemm_abi_version(void);
+
+/*
+ * Host-only helper, no GPU needed: the per-leaf merge schedule the kernels
+ * apply for a contraction of `num_leaves` leaves (1..1024). out[l] describes
+ * what follows leaf l in an in-order walk of the mid-split tree: bits 0..9
+ * are the pending-partial slots merged into the running value, lowest slot
+ * first (slot s holds the left child of a node of height s + 1); bits 12..15
+ * are the slot the result is parked in, or 15 when it is the root.
+ * `out` is caller-owned host memory of num_leaves entries.
+ * DET_GEMM_ERR_INVALID_ARG for a bad count or a NULL out.
+ */
+det_gemm_status det_gemm_tree_schedule(int64_t num_leaves, uint16_t *out);
+
+/*
+ * Test hook: while `enable` is nonzero, every GEMM launch makes its MMA warp
+ * wait on a barrier that nothing signals, with a short bound (about 50 ms).
+ * The wait expires, the kernel abandons its work, releases its tensor
+ * memory and returns, and det_gemm_check() reports DET_GEMM_ERR_TIMEOUT; the
+ * CUDA context stays usable. Outputs of such launches are undefined.
+ */
+det_gemm_status det_gemm_debug_force_timeout(int enable);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DET_GEMM_H */

@@ -1,0 +1,261 @@
+"""Python binding of the det_gemm C-ABI (libdet_gemm.so), for GB300 / sm_103a.
+
+Argument marshalling only: every entry point takes PyTorch CUDA BF16
+tensors, checks their layout, allocates the output with PyTorch when none is
+given, and calls the C function of the same name on the current CUDA stream.
+All arithmetic happens in the library's kernels. There is no fallback: if the
+library is missing or the device is not sm_103, the call raises.
+
+Operations (RL-Kernel, "Batch-Invariant Deterministic GEMM (det_gemm)",
+sections "Guarantees", "Ascend NPU backend", "Dtypes"):
+  det_gemm_fwd(A[M,K], B[K,N])                 -> C[M,N] bf16
+  det_gemm_fwd_rhs_transposed(A[M,K], W[N,K])  -> C[M,N] bf16
+  det_gemm_fwd_fp32(A[M,K], B[K,N])            -> C[M,N] fp32
+  det_gemm_fwd_fp32_rhs_transposed(A, W[N,K])  -> C[M,N] fp32
+  det_gemm_da(dC[M,N], B[K,N])                 -> dA[M,K] = dC B^T
+  det_gemm_db(A[M,K], dC[M,N])                 -> dB[K,N] = A^T dC
+  det_gemm_db_transposed(A[M,K], dC[M,N])      -> dB^T[N,K]
+Matrices are row-major with a leading dimension (``t.stride(0)``) and unit
+column stride; row-slices of bigger tensors are accepted as they are.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libdet_gemm.so")
+
+OK = 0
+STATUS_NAMES = {
+    0: "DET_GEMM_OK",
+    1: "DET_GEMM_ERR_INVALID_ARG",
+    2: "DET_GEMM_ERR_K_TOO_LARGE",
+    3: "DET_GEMM_ERR_ALIGNMENT",
+    4: "DET_GEMM_ERR_UNSUPPORTED_DEVICE",
+    5: "DET_GEMM_ERR_LAUNCH",
+    6: "DET_GEMM_ERR_TIMEOUT",
+    7: "DET_GEMM_ERR_CUDA",
+}
+KC_MAX = 32768
+
+_lib = None
+_lock = threading.Lock()
+
+_GEMM_NAMES = (
+    "det_gemm_fwd", "det_gemm_fwd_rhs_transposed", "det_gemm_fwd_fp32",
+    "det_gemm_fwd_fp32_rhs_transposed", "det_gemm_da", "det_gemm_db",
+    "det_gemm_db_transposed",
+)
+
+
+class DetGemmError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = int(status)
+        super().__init__("%s: %s" % (where, status_string(status)))
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded C library (raises if it was not built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise ImportError("libdet_gemm.so is not built (%s); run __graft_entry__.build() "
+                              "or python -m invariant_deterministic_gemm_gb300._build" % LIB_PATH)
+        L = ctypes.CDLL(LIB_PATH)
+        p, i64 = ctypes.c_void_p, ctypes.c_int64
+        for name in _GEMM_NAMES:
+            fn = getattr(L, name)
+            fn.argtypes = [p, p, p, i64, i64, i64, i64, i64, i64, p]
+            fn.restype = ctypes.c_int
+        L.det_gemm_check.argtypes = [p]
+        L.det_gemm_check.restype = ctypes.c_int
+        L.det_gemm_status_string.argtypes = [ctypes.c_int]
+        L.det_gemm_status_string.restype = ctypes.c_char_p
+        L.det_gemm_abi_version.argtypes = []
+        L.det_gemm_abi_version.restype = ctypes.c_int
+        L.det_gemm_tree_schedule.argtypes = [i64, p]
+        L.det_gemm_tree_schedule.restype = ctypes.c_int
+        L.det_gemm_debug_force_timeout.argtypes = [ctypes.c_int]
+        L.det_gemm_debug_force_timeout.restype = ctypes.c_int
+        _lib = L
+        return L
+
+
+def status_string(status: int) -> str:
+    return lib().det_gemm_status_string(int(status)).decode()
+
+
+def _stream_handle(stream) -> int:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return int(s.cuda_stream)
+
+
+def _mat(t: torch.Tensor, name: str, dtype=torch.bfloat16):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch.Tensor" % name)
+    if t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if t.dim() != 2:
+        raise ValueError("%s must be 2-D, got shape %s" % (name, tuple(t.shape)))
+    if t.device.type != "cuda":
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if t.shape[1] > 1 and t.stride(1) != 1:
+        raise ValueError("%s must be row-major with unit column stride" % name)
+    if t.shape[0] > 1:
+        ld = t.stride(0)
+    else:
+        # One row: the leading dimension is never used to address anything,
+        # so any value that meets the library's 16-byte pitch rule will do.
+        ld = max(t.shape[1], t.stride(0))
+        per16 = 16 // t.element_size()
+        ld = (ld + per16 - 1) // per16 * per16
+    return t.data_ptr(), int(ld)
+
+
+def _out(out, rows, cols, dtype, like: torch.Tensor):
+    if out is None:
+        # Pad the row pitch to 16 bytes (the library's rule) and hand back
+        # the [rows, cols] view.
+        per16 = 16 // torch.empty((), dtype=dtype).element_size()
+        ld = max(per16, (cols + per16 - 1) // per16 * per16)
+        return torch.empty((rows, ld), dtype=dtype, device=like.device)[:, :cols]
+    if tuple(out.shape) != (rows, cols):
+        raise ValueError("out must have shape %s, got %s" % ((rows, cols), tuple(out.shape)))
+    return out
+
+
+def _call(name: str, x_ptr, y_ptr, out_ptr, M, N, K, ldx, ldy, ldo, stream):
+    st = getattr(lib(), name)(x_ptr, y_ptr, out_ptr, M, N, K, ldx, ldy, ldo, _stream_handle(stream))
+    if st != OK:
+        raise DetGemmError(st, name)
+
+
+def det_gemm_fwd(A: torch.Tensor, B: torch.Tensor, out: torch.Tensor | None = None, stream=None):
+    """C[M,N] = A[M,K] @ B[K,N] (BF16 out)."""
+    M, K = A.shape
+    K2, N = B.shape
+    if K2 != K:
+        raise ValueError("inner dimensions differ: %d vs %d" % (K, K2))
+    a, lda = _mat(A, "A")
+    b, ldb = _mat(B, "B")
+    C = _out(out, M, N, torch.bfloat16, A)
+    c, ldc = _mat(C, "out")
+    _call("det_gemm_fwd", a, b, c, M, N, K, lda, ldb, ldc, stream)
+    return C
+
+
+def det_gemm_fwd_rhs_transposed(A: torch.Tensor, W: torch.Tensor, out=None, stream=None):
+    """C[M,N] = A[M,K] @ W[N,K]^T (BF16 out)."""
+    M, K = A.shape
+    N, K2 = W.shape
+    if K2 != K:
+        raise ValueError("inner dimensions differ: %d vs %d" % (K, K2))
+    a, lda = _mat(A, "A")
+    w, ldw = _mat(W, "W")
+    C = _out(out, M, N, torch.bfloat16, A)
+    c, ldc = _mat(C, "out")
+    _call("det_gemm_fwd_rhs_transposed", a, w, c, M, N, K, lda, ldw, ldc, stream)
+    return C
+
+
+def det_gemm_fwd_fp32(A: torch.Tensor, B: torch.Tensor, out=None, stream=None):
+    """C[M,N] = A[M,K] @ B[K,N] with FP32 leaves, FP32 tree, FP32 out."""
+    M, K = A.shape
+    K2, N = B.shape
+    if K2 != K:
+        raise ValueError("inner dimensions differ: %d vs %d" % (K, K2))
+    a, lda = _mat(A, "A")
+    b, ldb = _mat(B, "B")
+    C = _out(out, M, N, torch.float32, A)
+    c, ldc = _mat(C, "out", torch.float32)
+    _call("det_gemm_fwd_fp32", a, b, c, M, N, K, lda, ldb, ldc, stream)
+    return C
+
+
+def det_gemm_fwd_fp32_rhs_transposed(A: torch.Tensor, W: torch.Tensor, out=None, stream=None):
+    """C[M,N] = A[M,K] @ W[N,K]^T with FP32 leaves, FP32 tree, FP32 out."""
+    M, K = A.shape
+    N, K2 = W.shape
+    if K2 != K:
+        raise ValueError("inner dimensions differ: %d vs %d" % (K, K2))
+    a, lda = _mat(A, "A")
+    w, ldw = _mat(W, "W")
+    C = _out(out, M, N, torch.float32, A)
+    c, ldc = _mat(C, "out", torch.float32)
+    _call("det_gemm_fwd_fp32_rhs_transposed", a, w, c, M, N, K, lda, ldw, ldc, stream)
+    return C
+
+
+def det_gemm_da(dC: torch.Tensor, B: torch.Tensor, out=None, stream=None):
+    """dA[M,K] = dC[M,N] @ B[K,N]^T."""
+    M, N = dC.shape
+    K, N2 = B.shape
+    if N2 != N:
+        raise ValueError("dC and B disagree on N: %d vs %d" % (N, N2))
+    g, ldg = _mat(dC, "dC")
+    b, ldb = _mat(B, "B")
+    dA = _out(out, M, K, torch.bfloat16, dC)
+    d, ldd = _mat(dA, "out")
+    _call("det_gemm_da", g, b, d, M, N, K, ldg, ldb, ldd, stream)
+    return dA
+
+
+def det_gemm_db(A: torch.Tensor, dC: torch.Tensor, out=None, stream=None):
+    """dB[K,N] = A[M,K]^T @ dC[M,N]."""
+    M, K = A.shape
+    M2, N = dC.shape
+    if M2 != M:
+        raise ValueError("A and dC disagree on M: %d vs %d" % (M, M2))
+    a, lda = _mat(A, "A")
+    g, ldg = _mat(dC, "dC")
+    dB = _out(out, K, N, torch.bfloat16, A)
+    d, ldd = _mat(dB, "out")
+    _call("det_gemm_db", a, g, d, M, N, K, lda, ldg, ldd, stream)
+    return dB
+
+
+def det_gemm_db_transposed(A: torch.Tensor, dC: torch.Tensor, out=None, stream=None):
+    """dB^T[N,K] = dC[M,N]^T @ A[M,K] (the weight gradient in [N,K] layout)."""
+    M, K = A.shape
+    M2, N = dC.shape
+    if M2 != M:
+        raise ValueError("A and dC disagree on M: %d vs %d" % (M, M2))
+    a, lda = _mat(A, "A")
+    g, ldg = _mat(dC, "dC")
+    dBt = _out(out, N, K, torch.bfloat16, A)
+    d, ldd = _mat(dBt, "out")
+    _call("det_gemm_db_transposed", a, g, d, M, N, K, lda, ldg, ldd, stream)
+    return dBt
+
+
+def det_gemm_check(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device status code."""
+    return int(lib().det_gemm_check(_stream_handle(stream)))
+
+
+def det_gemm_tree_schedule(num_leaves: int) -> list[int]:
+    """Host-only: the per-leaf merge schedule the kernels apply (see det_gemm.h)."""
+    buf = (ctypes.c_uint16 * max(1, num_leaves))()
+    st = lib().det_gemm_tree_schedule(int(num_leaves), buf)
+    if st != OK:
+        raise DetGemmError(st, "det_gemm_tree_schedule")
+    return list(buf)[:num_leaves]
+
+
+def det_gemm_debug_force_timeout(enable: bool) -> None:
+    """Test hook: make every later launch time out on purpose (see det_gemm.h)."""
+    lib().det_gemm_debug_force_timeout(1 if enable else 0)
+
+
+__all__ = [
+    "det_gemm_fwd", "det_gemm_fwd_rhs_transposed", "det_gemm_fwd_fp32",
+    "det_gemm_fwd_fp32_rhs_transposed", "det_gemm_da", "det_gemm_db",
+    "det_gemm_db_transposed", "det_gemm_check", "det_gemm_tree_schedule",
+    "det_gemm_debug_force_timeout", "DetGemmError", "lib", "status_string",
+]

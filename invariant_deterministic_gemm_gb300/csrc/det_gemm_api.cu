@@ -1,0 +1,424 @@
+// det_gemm C-ABI: argument checks, the leaf-merge schedule, TMA descriptors
+// and kernel launches. The operation each entry point computes is stated in
+// include/det_gemm.h (RL-Kernel, "Batch-Invariant Deterministic GEMM
+// (det_gemm)", sections "Guarantees", "Ascend NPU backend" and "Dtypes").
+#include "det_gemm.h"
+#include "det_gemm_internal.h"
+
+#include <cudaTypedefs.h>
+
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+namespace detg {
+
+// Device status word: [0] = first error code seen since the last check.
+// One instance per device context; host code reaches it through
+// cudaGetSymbolAddress (the host-side symbol is not a device address).
+__device__ int g_status[4];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr unsigned long long kForcedTimeoutNs = 50ull * 1000 * 1000;
+
+struct DeviceState {
+    bool init = false;
+    det_gemm_status init_status = DET_GEMM_OK;
+    int sm_count = 0;
+    int *status_ptr = nullptr;
+    bool prepared[kVariantCount] = {};
+    det_gemm_status prepare_status[kVariantCount] = {};
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+int g_force_timeout = 0;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+uint16_t *g_sched_cache[kMaxLeaves + 1] = {};
+
+VariantOps variant_ops(Variant v)
+{
+    switch (v) {
+    case kBf16KMN: return ops_bf16_kmn();
+    case kBf16KK: return ops_bf16_kk();
+    case kBf16MNMN: return ops_bf16_mnmn();
+    case kF32KMN: return ops_f32_kmn();
+    case kF32KK: return ops_f32_kk();
+    default: return VariantOps{};
+    }
+}
+
+unsigned long long timeout_ns()
+{
+    if (g_force_timeout) return kForcedTimeoutNs;
+    const char *s = std::getenv("DET_GEMM_TIMEOUT_MS");
+    long long ms = s ? std::atoll(s) : 1000;
+    if (ms < 1) ms = 1;
+    return static_cast<unsigned long long>(ms) * 1000ull * 1000ull;
+}
+
+// smallest h with 2^h >= n, for n >= 1
+int ceil_log2(int64_t n)
+{
+    int h = 0;
+    while ((int64_t{1} << h) < n) ++h;
+    return h;
+}
+
+// The per-leaf schedule of the mid-split tree (format in det_gemm.h). The
+// walk descends from the root [0, L) to leaf l, splitting [lo, hi) at
+// mid = (lo + hi) / 2. A node over n leaves has height ceil(log2 n); the
+// left child of a node of height h waits in slot h - 1. After leaf l is
+// finished the running value climbs while it is a right child, merging the
+// waiting left sibling at each such node, and is parked at the first node
+// where it is a left child (or is the root).
+void build_schedule(int64_t L, uint16_t *out)
+{
+    for (int64_t l = 0; l < L; ++l) {
+        int64_t lo = 0, hi = L;
+        int depth = 0;
+        int slot_at[32];
+        bool right_at[32];
+        while (hi - lo > 1) {
+            const int64_t mid = (lo + hi) >> 1;
+            slot_at[depth] = ceil_log2(hi - lo) - 1;
+            right_at[depth] = (l >= mid);
+            ++depth;
+            if (l >= mid) lo = mid;
+            else hi = mid;
+        }
+        uint32_t mask = 0;
+        uint32_t store = kSlotRoot;
+        for (int d = depth - 1; d >= 0; --d) {
+            if (right_at[d]) {
+                mask |= 1u << slot_at[d];
+            } else {
+                store = static_cast<uint32_t>(slot_at[d]);
+                break;
+            }
+        }
+        out[l] = static_cast<uint16_t>(mask | (store << 12));
+    }
+}
+
+const uint16_t *schedule_for(int64_t L)
+{
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_sched_cache[L]) {
+        uint16_t *s = static_cast<uint16_t *>(std::malloc(sizeof(uint16_t) * L));
+        if (!s) return nullptr;
+        build_schedule(L, s);
+        g_sched_cache[L] = s;
+    }
+    return g_sched_cache[L];
+}
+
+// ---------------------------------------------------------- validation
+
+struct Mat {
+    const void *ptr;
+    int64_t rows, cols, ld;
+    int esize;
+};
+
+det_gemm_status check_mat(const Mat &m)
+{
+    if (m.rows <= 0 || m.cols <= 0) return DET_GEMM_OK;   // empty: never touched
+    if (m.ptr == nullptr) return DET_GEMM_ERR_INVALID_ARG;
+    if (m.ld < m.cols) return DET_GEMM_ERR_INVALID_ARG;
+    if (m.ld > (int64_t{1} << 36)) return DET_GEMM_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(m.ptr) % 16 != 0) return DET_GEMM_ERR_ALIGNMENT;
+    if ((m.ld * m.esize) % 16 != 0) return DET_GEMM_ERR_ALIGNMENT;
+    return DET_GEMM_OK;
+}
+
+bool overlaps(const Mat &a, const Mat &b)
+{
+    if (a.rows <= 0 || a.cols <= 0 || b.rows <= 0 || b.cols <= 0) return false;
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a.ptr);
+    const uintptr_t a1 = a0 + static_cast<uintptr_t>(((a.rows - 1) * a.ld + a.cols) * a.esize);
+    const uintptr_t b0 = reinterpret_cast<uintptr_t>(b.ptr);
+    const uintptr_t b1 = b0 + static_cast<uintptr_t>(((b.rows - 1) * b.ld + b.cols) * b.esize);
+    return a0 < b1 && b0 < a1;
+}
+
+// ------------------------------------------------------------- devices
+
+det_gemm_status device_state(DeviceState **out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return DET_GEMM_ERR_UNSUPPORTED_DEVICE;
+    }
+    if (dev < 0 || dev >= kMaxDevices) return DET_GEMM_ERR_UNSUPPORTED_DEVICE;
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceState &st = g_dev[dev];
+    if (!st.init) {
+        st.init = true;
+        int major = 0, minor = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&st.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            cudaGetLastError();
+            st.init_status = DET_GEMM_ERR_UNSUPPORTED_DEVICE;
+        } else if (major != 10 || minor != 3) {
+            st.init_status = DET_GEMM_ERR_UNSUPPORTED_DEVICE;
+        } else if (cudaGetSymbolAddress(reinterpret_cast<void **>(&st.status_ptr), g_status) != cudaSuccess) {
+            cudaGetLastError();
+            st.init_status = DET_GEMM_ERR_LAUNCH;
+        } else {
+            if (!g_encode) {
+                cudaDriverEntryPointQueryResult q;
+                void *fn = nullptr;
+                if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                                     &q) != cudaSuccess ||
+                    q != cudaDriverEntryPointSuccess || fn == nullptr) {
+                    cudaGetLastError();
+                    st.init_status = DET_GEMM_ERR_LAUNCH;
+                } else {
+                    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+                }
+            }
+        }
+    }
+    if (st.init_status != DET_GEMM_OK) return st.init_status;
+    *out = &st;
+    return DET_GEMM_OK;
+}
+
+det_gemm_status prepare_variant(DeviceState *st, Variant v)
+{
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!st->prepared[v]) {
+        st->prepared[v] = true;
+        int regs = 0;
+        VariantOps ops = variant_ops(v);
+        if (!ops.prepare || ops.prepare(&regs) != cudaSuccess) {
+            cudaGetLastError();
+            st->prepare_status[v] = DET_GEMM_ERR_LAUNCH;
+        } else if (regs * kThreads < kProdRegs * 128 + kEpiRegs * 256) {
+            // setmaxnreg redistributes the registers the CTA was launched
+            // with; a smaller launch allocation could never satisfy the
+            // epilogue's request.
+            st->prepare_status[v] = DET_GEMM_ERR_LAUNCH;
+        }
+    }
+    return st->prepare_status[v];
+}
+
+bool encode(CUtensorMap *m, const void *ptr, uint64_t inner, uint64_t outer, uint64_t ld_elems,
+            uint32_t box_inner, uint32_t box_outer)
+{
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {ld_elems * 2};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box,
+                          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// One GEMM: out[rows, cols] = sum over kc of Aop[row, k] * Bop[k, col].
+// Aop is `a` stored either K-major ([rows, kc] row-major) or MN-major
+// ([kc, rows] row-major); Bop is `b` stored K-major ([cols, kc]) or MN-major
+// ([kc, cols]).
+det_gemm_status run(Variant v, Mat a, bool a_kmajor, Mat b, bool b_kmajor, Mat out, int64_t rows, int64_t cols,
+                    int64_t kc, cudaStream_t stream)
+{
+    if (rows < 0 || cols < 0 || kc < 0) return DET_GEMM_ERR_INVALID_ARG;
+    if (rows > (int64_t{1} << 31) - 256 || cols > (int64_t{1} << 31) - 256) return DET_GEMM_ERR_INVALID_ARG;
+    if (rows == 0 || cols == 0) return DET_GEMM_OK;
+    if (kc > kKcMax) return DET_GEMM_ERR_K_TOO_LARGE;
+    det_gemm_status s = check_mat(out);
+    if (s != DET_GEMM_OK) return s;
+    if (kc > 0) {
+        if ((s = check_mat(a)) != DET_GEMM_OK) return s;
+        if ((s = check_mat(b)) != DET_GEMM_OK) return s;
+        if (overlaps(out, a) || overlaps(out, b)) return DET_GEMM_ERR_INVALID_ARG;
+    }
+    DeviceState *st = nullptr;
+    if ((s = device_state(&st)) != DET_GEMM_OK) return s;
+
+    if (kc == 0) {
+        // Empty contraction: every element is the empty sum, +0.
+        cudaError_t e = cudaMemset2DAsync(const_cast<void *>(out.ptr), static_cast<size_t>(out.ld * out.esize), 0,
+                                          static_cast<size_t>(cols * out.esize), static_cast<size_t>(rows), stream);
+        return e == cudaSuccess ? DET_GEMM_OK : (cudaGetLastError(), DET_GEMM_ERR_LAUNCH);
+    }
+    if ((s = prepare_variant(st, v)) != DET_GEMM_OK) return s;
+    VariantOps ops = variant_ops(v);
+
+    const int64_t L = (kc + kLeaf - 1) / kLeaf;
+    const uint16_t *sched = schedule_for(L);
+    if (!sched) return DET_GEMM_ERR_LAUNCH;
+
+    Params p;
+    std::memset(&p, 0, sizeof(p));
+    bool ok;
+    if (a_kmajor) ok = encode(&p.tmap_a, a.ptr, kc, rows, a.ld, 64, kBM);
+    else ok = encode(&p.tmap_a, a.ptr, rows, kc, a.ld, 64, 64);
+    if (ok) {
+        if (b_kmajor) ok = encode(&p.tmap_b, b.ptr, kc, cols, b.ld, 64, ops.bn);
+        else ok = encode(&p.tmap_b, b.ptr, cols, kc, b.ld, 64, 64);
+    }
+    if (!ok) return DET_GEMM_ERR_LAUNCH;
+    p.out = const_cast<void *>(out.ptr);
+    p.ldo = out.ld;
+    p.status = st->status_ptr;
+    p.timeout_ns = timeout_ns();
+    p.rows = static_cast<int>(rows);
+    p.cols = static_cast<int>(cols);
+    p.kc = static_cast<int>(kc);
+    p.num_leaves = static_cast<int>(L);
+    p.m_tiles = static_cast<int>((rows + kBM - 1) / kBM);
+    p.n_tiles = static_cast<int>((cols + ops.bn - 1) / ops.bn);
+    p.force_timeout = g_force_timeout;
+    std::memcpy(p.sched, sched, sizeof(uint16_t) * L);
+
+    const int64_t tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
+    if (tiles > (int64_t{1} << 31) - 1) return DET_GEMM_ERR_INVALID_ARG;
+    const int grid = static_cast<int>(tiles < st->sm_count ? tiles : st->sm_count);
+    if (ops.launch(p, grid, stream) != cudaSuccess) {
+        cudaGetLastError();
+        return DET_GEMM_ERR_LAUNCH;
+    }
+    return DET_GEMM_OK;
+}
+
+Mat bf16(const void *p, int64_t r, int64_t c, int64_t ld) { return Mat{p, r, c, ld, 2}; }
+Mat f32(const void *p, int64_t r, int64_t c, int64_t ld) { return Mat{p, r, c, ld, 4}; }
+
+}  // namespace
+}  // namespace detg
+
+using namespace detg;
+
+extern "C" {
+
+det_gemm_status det_gemm_fwd(const det_gemm_bf16 *A, const det_gemm_bf16 *B, det_gemm_bf16 *C, int64_t M,
+                             int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldc, det_gemm_stream stream)
+{
+    if (M < 0 || N < 0 || K < 0) return DET_GEMM_ERR_INVALID_ARG;
+    return run(kBf16KMN, bf16(A, M, K, lda), true, bf16(B, K, N, ldb), false, bf16(C, M, N, ldc), M, N, K,
+               reinterpret_cast<cudaStream_t>(stream));
+}
+
+det_gemm_status det_gemm_fwd_rhs_transposed(const det_gemm_bf16 *A, const det_gemm_bf16 *W, det_gemm_bf16 *C,
+                                            int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldw,
+                                            int64_t ldc, det_gemm_stream stream)
+{
+    if (M < 0 || N < 0 || K < 0) return DET_GEMM_ERR_INVALID_ARG;
+    return run(kBf16KK, bf16(A, M, K, lda), true, bf16(W, N, K, ldw), true, bf16(C, M, N, ldc), M, N, K,
+               reinterpret_cast<cudaStream_t>(stream));
+}
+
+det_gemm_status det_gemm_fwd_fp32(const det_gemm_bf16 *A, const det_gemm_bf16 *B, float *C, int64_t M, int64_t N,
+                                  int64_t K, int64_t lda, int64_t ldb, int64_t ldc, det_gemm_stream stream)
+{
+    if (M < 0 || N < 0 || K < 0) return DET_GEMM_ERR_INVALID_ARG;
+    return run(kF32KMN, bf16(A, M, K, lda), true, bf16(B, K, N, ldb), false, f32(C, M, N, ldc), M, N, K,
+               reinterpret_cast<cudaStream_t>(stream));
+}
+
+det_gemm_status det_gemm_fwd_fp32_rhs_transposed(const det_gemm_bf16 *A, const det_gemm_bf16 *W, float *C,
+                                                 int64_t M, int64_t N, int64_t K, int64_t lda, int64_t ldw,
+                                                 int64_t ldc, det_gemm_stream stream)
+{
+    if (M < 0 || N < 0 || K < 0) return DET_GEMM_ERR_INVALID_ARG;
+    return run(kF32KK, bf16(A, M, K, lda), true, bf16(W, N, K, ldw), true, f32(C, M, N, ldc), M, N, K,
+               reinterpret_cast<cudaStream_t>(stream));
+}
+
+det_gemm_status det_gemm_da(const det_gemm_bf16 *dC, const det_gemm_bf16 *B, det_gemm_bf16 *dA, int64_t M,
+                            int64_t N, int64_t K, int64_t lddc, int64_t ldb, int64_t ldda, det_gemm_stream stream)
+{
+    // dA[m, k] = sum_n dC[m, n] * B[k, n]: rows M, columns K, contraction N.
+    // dC is [M, N] with n contiguous (K-major); B is [K, N] with n contiguous
+    // (K-major for the columns k).
+    if (M < 0 || N < 0 || K < 0) return DET_GEMM_ERR_INVALID_ARG;
+    return run(kBf16KK, bf16(dC, M, N, lddc), true, bf16(B, K, N, ldb), true, bf16(dA, M, K, ldda), M, K, N,
+               reinterpret_cast<cudaStream_t>(stream));
+}
+
+det_gemm_status det_gemm_db(const det_gemm_bf16 *A, const det_gemm_bf16 *dC, det_gemm_bf16 *dB, int64_t M,
+                            int64_t N, int64_t K, int64_t lda, int64_t lddc, int64_t lddb, det_gemm_stream stream)
+{
+    // dB[k, n] = sum_m A[m, k] * dC[m, n]: rows K, columns N, contraction M.
+    // A is [M, K] with k contiguous (MN-major for rows k); dC is [M, N] with n
+    // contiguous (MN-major for columns n).
+    if (M < 0 || N < 0 || K < 0) return DET_GEMM_ERR_INVALID_ARG;
+    return run(kBf16MNMN, bf16(A, M, K, lda), false, bf16(dC, M, N, lddc), false, bf16(dB, K, N, lddb), K, N, M,
+               reinterpret_cast<cudaStream_t>(stream));
+}
+
+det_gemm_status det_gemm_db_transposed(const det_gemm_bf16 *A, const det_gemm_bf16 *dC, det_gemm_bf16 *dBt,
+                                       int64_t M, int64_t N, int64_t K, int64_t lda, int64_t lddc, int64_t lddbt,
+                                       det_gemm_stream stream)
+{
+    // dBt[n, k] = sum_m dC[m, n] * A[m, k]: rows N, columns K, contraction M.
+    if (M < 0 || N < 0 || K < 0) return DET_GEMM_ERR_INVALID_ARG;
+    return run(kBf16MNMN, bf16(dC, M, N, lddc), false, bf16(A, M, K, lda), false, bf16(dBt, N, K, lddbt), N, K, M,
+               reinterpret_cast<cudaStream_t>(stream));
+}
+
+det_gemm_status det_gemm_check(det_gemm_stream stream)
+{
+    DeviceState *st = nullptr;
+    det_gemm_status s = device_state(&st);
+    if (s != DET_GEMM_OK) return s;
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) {
+        cudaGetLastError();
+        return DET_GEMM_ERR_CUDA;
+    }
+    int code = 0;
+    if (cudaMemcpyFromSymbol(&code, g_status, sizeof(int)) != cudaSuccess) {
+        cudaGetLastError();
+        return DET_GEMM_ERR_CUDA;
+    }
+    if (code != 0) {
+        const int zero = 0;
+        if (cudaMemcpyToSymbol(g_status, &zero, sizeof(int)) != cudaSuccess) {
+            cudaGetLastError();
+            return DET_GEMM_ERR_CUDA;
+        }
+    }
+    return code == 0 ? DET_GEMM_OK : static_cast<det_gemm_status>(code);
+}
+
+const char *det_gemm_status_string(det_gemm_status status)
+{
+    switch (status) {
+    case DET_GEMM_OK: return "DET_GEMM_OK";
+    case DET_GEMM_ERR_INVALID_ARG: return "DET_GEMM_ERR_INVALID_ARG: null pointer, bad size or leading dimension, or overlapping output";
+    case DET_GEMM_ERR_K_TOO_LARGE: return "DET_GEMM_ERR_K_TOO_LARGE: contraction length above 32768";
+    case DET_GEMM_ERR_ALIGNMENT: return "DET_GEMM_ERR_ALIGNMENT: pointer not 16-byte aligned or row pitch not a multiple of 16 bytes";
+    case DET_GEMM_ERR_UNSUPPORTED_DEVICE: return "DET_GEMM_ERR_UNSUPPORTED_DEVICE: needs a compute capability 10.3 GPU";
+    case DET_GEMM_ERR_LAUNCH: return "DET_GEMM_ERR_LAUNCH: kernel set-up or launch failed";
+    case DET_GEMM_ERR_TIMEOUT: return "DET_GEMM_ERR_TIMEOUT: a device-side bounded wait expired";
+    case DET_GEMM_ERR_CUDA: return "DET_GEMM_ERR_CUDA: CUDA runtime error on the stream";
+    default: return "DET_GEMM: unknown status";
+    }
+}
+
+int det_gemm_abi_version(void) { return DET_GEMM_ABI_VERSION; }
+
+det_gemm_status det_gemm_tree_schedule(int64_t num_leaves, uint16_t *out)
+{
+    if (out == nullptr || num_leaves < 1 || num_leaves > kMaxLeaves) return DET_GEMM_ERR_INVALID_ARG;
+    build_schedule(num_leaves, out);
+    return DET_GEMM_OK;
+}
+
+det_gemm_status det_gemm_debug_force_timeout(int enable)
+{
+    std::lock_guard<std::mutex> lk(g_mu);
+    g_force_timeout = enable ? 1 : 0;
+    return DET_GEMM_OK;
+}
+
+}  // extern "C"

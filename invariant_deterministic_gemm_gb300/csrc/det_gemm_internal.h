@@ -1,0 +1,66 @@
+// Internal declarations shared by the det_gemm host code and kernel
+// translation units. Not part of the public C-ABI (include/det_gemm.h).
+#pragma once
+
+#include <cstdint>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace detg {
+
+constexpr int kLeaf = 32;                 // contraction elements per leaf
+constexpr int kKcMax = 32768;             // cap on the contraction length
+constexpr int kMaxLeaves = kKcMax / kLeaf;
+constexpr int kSlotRoot = 15;             // schedule "store" value for the root
+constexpr int kMaxSlots = 10;             // ceil(log2(kMaxLeaves)) pending partials
+constexpr int kBM = 128;                  // output rows per tile (one TMEM lane per row)
+constexpr int kBK = 64;                   // contraction elements per shared-memory stage (two leaves)
+constexpr int kThreads = 384;             // 8 epilogue warps + producer warpgroup
+constexpr int kEpiWarps = 8;
+constexpr int kEpiRegs = 224;             // registers per epilogue thread after setmaxnreg
+constexpr int kProdRegs = 56;             // registers per producer-warpgroup thread
+
+// Operand major-ness as seen by the MMA: K-major = contraction contiguous.
+enum Major { kKMajor = 0, kMNMajor = 1 };
+
+// Kernel variants: (A operand major, B operand major, output type).
+enum Variant {
+    kBf16KMN = 0,   // fwd: A[M,K] K-major, B[K,N] N-major
+    kBf16KK,        // fwd_rhs_transposed, da: both K-major
+    kBf16MNMN,      // db, db_transposed: both MN-major
+    kF32KMN,        // fwd_fp32
+    kF32KK,         // fwd_fp32 with a [N,K] weight
+    kVariantCount
+};
+
+// Everything a launch needs; passed by value as a __grid_constant__ param.
+struct Params {
+    CUtensorMap tmap_a;           // "A operand": output rows x contraction
+    CUtensorMap tmap_b;           // "B operand": contraction x output columns
+    void *out;                    // row-major output, rows x cols
+    long long ldo;                // output leading dimension, elements
+    int *status;                  // device status word (first int = code)
+    unsigned long long timeout_ns;
+    int rows, cols, kc, num_leaves;
+    int m_tiles, n_tiles;
+    int force_timeout;
+    int pad_;
+    uint16_t sched[kMaxLeaves];   // per-leaf merge schedule (see det_gemm_tree_schedule)
+};
+
+struct VariantOps {
+    // Sets the kernel's shared-memory attribute; reports registers per thread.
+    cudaError_t (*prepare)(int *num_regs);
+    cudaError_t (*launch)(const Params &p, int grid, cudaStream_t stream);
+    int bn;                       // output columns per tile
+    int smem_bytes;
+};
+
+VariantOps ops_bf16_kmn();
+VariantOps ops_bf16_kk();
+VariantOps ops_bf16_mnmn();
+VariantOps ops_f32_kmn();
+VariantOps ops_f32_kk();
+
+}  // namespace detg

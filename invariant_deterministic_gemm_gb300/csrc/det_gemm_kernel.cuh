@@ -1,0 +1,921 @@
+// det_gemm kernel for sm_103a: TMA -> shared memory -> tcgen05 MMA into TMEM,
+// one 32-wide K leaf per accumulator, leaf rounding and the fixed mid-split
+// merge tree applied by the epilogue warps.
+//
+// Arithmetic (RL-Kernel, "Batch-Invariant Deterministic GEMM (det_gemm)",
+// sections "Guarantees" and "Ascend NPU backend"): FP32 accumulation inside
+// 32-element leaves, each leaf rounded once to BF16 (RNE), leaves merged by
+// BF16 adds in a fixed mid-split tree; FP32 leaves and FP32 adds for the
+// fp32-output variant ("Dtypes"). Every output element is produced end to
+// end by one CTA in a fixed leaf order; which CTA, and the order in which
+// tiles are visited, change timing only ("Ascend NPU backend", batch-
+// invariance bullet). One tile shape per variant, whatever M is: choosing a
+// kernel by problem shape is what breaks batch invariance (section "Why").
+//
+// CTA layout (384 threads, one CTA per SM, persistent over output tiles):
+//   warps 0-7  epilogue: warp w reads TMEM lanes 32*(w%4).. (rows) and the
+//              column half w/4 of the tile; each thread owns one row and
+//              BN/2 columns, and keeps the tree's pending partials for them.
+//   warp 8     TMA producer (one lane).
+//   warp 9     TMEM allocator and MMA issuer (one lane).
+//   warps 10-11 idle (they complete the producer warpgroup for setmaxnreg).
+//
+// Per tile: the producer streams 64-wide K stages (two leaves) of the A and B
+// operand tiles into a ring of swizzled shared-memory buffers. For leaf l the
+// MMA lane issues two K=16 MMAs into accumulator buffer l % NACC (the first
+// one overwrites, so each leaf starts from zero) and commits to that
+// buffer's "full" barrier. The epilogue loads the leaf, frees the buffer at
+// once (so the MMA can run NACC-1 leaves ahead), rounds it (bf16 variant)
+// and merges it into its pending partials following the per-leaf schedule,
+// and writes the root after the last leaf.
+//
+// Pending partials ("slots"): slot s holds the finished left child of a tree
+// node of height s + 1, so at most ceil(log2 L) <= 10 are live, and slot s
+// is written at most once per 2^(s+1) leaves. Slot 0 and the running value
+// share two register arrays that swap roles (parking a leaf in slot 0 is a
+// relabelling, not a copy); slots 1-2 are registers; the next ones are TMEM
+// columns past the accumulators, then shared memory; slot 9 (more than 512
+// leaves) is parked in the thread's own output elements, where the root
+// will later be written.
+//
+// Every mbarrier wait is bounded (Params::timeout_ns of %globaltimer). On
+// expiry the waiter records DET_GEMM_ERR_TIMEOUT in the status word and sets
+// a CTA-wide abort flag; every role then leaves its loop, outstanding TMA
+// loads and MMAs are drained with bounded waits, TMEM is released and the
+// CTA exits.
+#pragma once
+
+#include "det_gemm_internal.h"
+
+namespace detg {
+
+constexpr int kStatusTimeout = 6;   // DET_GEMM_ERR_TIMEOUT
+
+// ------------------------------------------------------------------ config
+
+template <bool F32>
+struct Cfg {
+    static constexpr int BN = F32 ? 64 : 128;           // output columns per tile
+    static constexpr int NACC = F32 ? 4 : 3;            // TMEM accumulator buffers
+    static constexpr int STAGES = F32 ? 6 : 3;          // shared-memory ring depth
+    static constexpr int A_STAGE = kBM * kBK * 2;       // bytes of one A stage
+    static constexpr int B_STAGE = BN * kBK * 2;        // bytes of one B stage
+    static constexpr int STAGE_TX = A_STAGE + B_STAGE;  // TMA bytes per stage
+    static constexpr int COLS = BN / 2;                 // output columns per epilogue thread
+    static constexpr int WORDS = 32;                    // 32-bit words per slot per thread
+    static constexpr int TMEM_COLS = 512;
+    static constexpr int TMEM_SLOT_BASE = NACC * BN;    // after the accumulators
+    static constexpr int TMEM_FIRST = 3;                // slots 0-2 live in registers
+    static constexpr int TMEM_SLOTS = (TMEM_COLS - TMEM_SLOT_BASE) / 64;
+    static constexpr int SMEM_FIRST = TMEM_FIRST + TMEM_SLOTS;
+    static constexpr int OUT_SLOT = kMaxSlots - 1;
+    static constexpr int SMEM_SLOTS = OUT_SLOT - SMEM_FIRST;
+    static constexpr int SMEM_SLOT_BYTES = kEpiWarps * 32 * WORDS * 4;
+
+    static constexpr int OFF_A = 0;
+    static constexpr int OFF_B = OFF_A + STAGES * A_STAGE;
+    static constexpr int OFF_SLOTS = OFF_B + STAGES * B_STAGE;
+    static constexpr int OFF_BAR = OFF_SLOTS + SMEM_SLOTS * SMEM_SLOT_BYTES;
+    // barriers: full[STAGES], empty[STAGES], acc_full[NACC], acc_empty[NACC], never, drain
+    static constexpr int NUM_BARS = 2 * STAGES + 2 * NACC + 2;
+    static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
+    static constexpr int BYTES = OFF_MISC + 16;
+    static constexpr int SMEM_BYTES = BYTES + 1024;     // slack to align the base to 1024 B
+
+    static_assert(SMEM_SLOTS >= 0, "slot storage");
+    static_assert(SMEM_BYTES <= 232448, "shared memory");
+    static_assert(A_STAGE % 1024 == 0 && B_STAGE % 1024 == 0, "swizzle atoms");
+    static_assert(F32 ? (COLS == WORDS) : (COLS == 2 * WORDS), "packing");
+};
+
+// ----------------------------------------------------------- PTX helpers
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ unsigned long long global_ns()
+{
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// try_wait with a suspend-time hint: a waiting thread sleeps until the
+// phase completes or the hint expires instead of spinning, so it does not
+// take issue slots from the warps sharing its scheduler.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait for the phase with the given parity. Returns false when the
+// CTA is aborting (another waiter gave up) or when this wait exceeds the
+// launch's time bound, in which case it records the timeout and starts the
+// abort. `honor_abort` = false is used by the drain waits of the teardown.
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                             int *status, unsigned long long timeout_ns, bool honor_abort)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = global_ns();
+    for (;;) {
+        if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+        if (honor_abort && *abort_flag) return false;
+        if (global_ns() - t0 > timeout_ns) {
+            *abort_flag = 1;
+            atomicExch(status, kStatusTimeout);
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, uint32_t bar, int x,
+                                            int y)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmap_prefetch(const CUtensorMap *map)
+{
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// UMMA shared-memory descriptor, 128-byte swizzle, sm_100 family version 1.
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo)
+{
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+    d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+    d |= static_cast<uint64_t>(1) << 46;   // descriptor version for tcgen05
+    d |= static_cast<uint64_t>(2) << 61;   // SWIZZLE_128B
+    return d;
+}
+
+// Instruction descriptor, kind::f16: BF16 x BF16 -> FP32, M x N, dense.
+__host__ __device__ constexpr uint32_t idesc_bf16(int m, int n, int a_major, int b_major)
+{
+    return (1u << 4)                                   // D format: F32
+           | (1u << 7)                                 // A format: BF16
+           | (1u << 10)                                // B format: BF16
+           | (static_cast<uint32_t>(a_major) << 15)    // A: 0 K-major, 1 MN-major
+           | (static_cast<uint32_t>(b_major) << 16)    // B: 0 K-major, 1 MN-major
+           | (static_cast<uint32_t>(n >> 3) << 17)
+           | (static_cast<uint32_t>(m >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                         uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, "
+        "%20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+          "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+          "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+
+__device__ __forceinline__ void reg_fence16(uint32_t (&r)[16])
+{
+    asm volatile(""
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                   "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                   "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]));
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32])
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, "
+        "%20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+        "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
+        "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
+        "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// Ties the registers written by tcgen05.ld to a point after tcgen05.wait::ld,
+// so no use of them can be scheduled before the wait.
+__device__ __forceinline__ void reg_fence(uint32_t (&r)[32])
+{
+    asm volatile(""
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                   "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                   "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]),
+                   "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]),
+                   "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]),
+                   "+r"(r[30]), "+r"(r[31]));
+}
+
+// Two FP32 values -> packed BF16 pair, each rounded to nearest even.
+// The low half holds `lo` (the lower column), as memory order wants.
+__device__ __forceinline__ uint32_t cvt_bf16x2(uint32_t lo, uint32_t hi)
+{
+    uint32_t d;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(__uint_as_float(hi)), "f"(__uint_as_float(lo)));
+    return d;
+}
+
+// One tree node: left + right, rounded once (BF16 pair, or one FP32 value).
+template <bool F32>
+__device__ __forceinline__ uint32_t merge(uint32_t left, uint32_t right)
+{
+    if constexpr (F32) {
+        return __float_as_uint(__fadd_rn(__uint_as_float(left), __uint_as_float(right)));
+    } else {
+        uint32_t d;
+        asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(left), "r"(right));
+        return d;
+    }
+}
+
+// ------------------------------------------------------------- schedule
+
+// Tile t of the persistent walk -> (m tile, n tile). Tiles are grouped 8
+// m-tiles at a time so that CTAs running together share operand panels in
+// L2. Only timing depends on this order.
+__device__ __forceinline__ void tile_coords(int t, int m_tiles, int n_tiles, int &mt, int &nt)
+{
+    constexpr int G = 8;
+    const int group = G * n_tiles;
+    const int g = t / group;
+    const int first = g * G;
+    const int gm = min(G, m_tiles - first);
+    const int r = t - g * group;
+    mt = first + r % gm;
+    nt = r / gm;
+}
+
+// ------------------------------------------------------------- epilogue
+
+template <bool F32>
+__device__ __forceinline__ void merge_all(uint32_t (&v)[32], const uint32_t (&s)[32])
+{
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = merge<F32>(s[i], v[i]);
+}
+
+// What one epilogue thread needs to reach its storage.
+struct EpiCtx {
+    uint32_t tmem_slot;   // TMEM address of this thread's first TMEM slot
+    uint32_t smem_slot;   // shared-memory address of this thread's first slot
+    int lane;
+    int row, col;         // first output element owned by this thread
+};
+
+// Shared-memory slot chunk c (16 bytes) of this thread: chunks are XOR-
+// swizzled by lane so that the warp's row-wise accesses spread over banks.
+__device__ __forceinline__ uint32_t smem_chunk(uint32_t base, int lane, int c)
+{
+    return base + static_cast<uint32_t>((c ^ (lane & 7)) * 16);
+}
+
+// Byte b (0..127) of this thread's first shared-memory slot, in the
+// swizzled layout of smem_chunk.
+__device__ __forceinline__ uint32_t smem_byte(const EpiCtx &c, int b)
+{
+    return c.smem_slot + static_cast<uint32_t>((((b >> 4) ^ (c.lane & 7)) << 4) + (b & 15));
+}
+
+// Writes this thread's 32 words (64 BF16 or 32 FP32 columns) to the output,
+// clipped to the matrix: used for the root and to park the root's left
+// child. A row the matrix clips goes element by element through this
+// thread's first shared-memory slot, which is always free here (the root's
+// children are formed only after every lower slot has been merged away).
+template <bool F32>
+__device__ __forceinline__ void store_out(const uint32_t (&v)[32], const Params &p, const EpiCtx &c)
+{
+    using C = Cfg<F32>;
+    constexpr int ES = F32 ? 4 : 2;
+    if (c.row >= p.rows) return;
+    const int ncols = p.cols - c.col;
+    if (ncols <= 0) return;
+    uint8_t *dst = static_cast<uint8_t *>(p.out) + (static_cast<long long>(c.row) * p.ldo + c.col) * ES;
+    if (ncols >= C::COLS) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(dst + 16 * k), "r"(v[4 * k]),
+                         "r"(v[4 * k + 1]), "r"(v[4 * k + 2]), "r"(v[4 * k + 3])
+                         : "memory");
+        return;
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(smem_chunk(c.smem_slot, c.lane, k)),
+                     "r"(v[4 * k]), "r"(v[4 * k + 1]), "r"(v[4 * k + 2]), "r"(v[4 * k + 3])
+                     : "memory");
+#pragma unroll 1
+    for (int j = 0; j < ncols; ++j) {
+        if constexpr (F32) {
+            uint32_t w;
+            asm volatile("ld.shared.b32 %0, [%1];" : "=r"(w) : "r"(smem_byte(c, 4 * j)) : "memory");
+            asm volatile("st.global.b32 [%0], %1;" ::"l"(dst + 4 * j), "r"(w) : "memory");
+        } else {
+            uint16_t w;
+            asm volatile("ld.shared.u16 %0, [%1];" : "=h"(w) : "r"(smem_byte(c, 2 * j)) : "memory");
+            asm volatile("st.global.u16 [%0], %1;" ::"l"(dst + 2 * j), "h"(w) : "memory");
+        }
+    }
+}
+
+// Reads back half H (words 16H .. 16H+15) of what store_out parked, with
+// the same clipping (words outside the matrix read as zero; they are never
+// written out).
+template <bool F32, int H>
+__device__ __forceinline__ void load_out_half(uint32_t (&v)[16], const Params &p, const EpiCtx &c)
+{
+    using C = Cfg<F32>;
+    constexpr int ES = F32 ? 4 : 2;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = 0;
+    if (c.row >= p.rows) return;
+    const int ncols = p.cols - c.col;
+    if (ncols <= 0) return;
+    const uint8_t *src =
+        static_cast<const uint8_t *>(p.out) + (static_cast<long long>(c.row) * p.ldo + c.col) * ES;
+    if (ncols >= C::COLS) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            asm volatile("ld.global.v4.b32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(v[4 * k]), "=r"(v[4 * k + 1]), "=r"(v[4 * k + 2]), "=r"(v[4 * k + 3])
+                         : "l"(src + 64 * H + 16 * k)
+                         : "memory");
+        return;
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+        asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(smem_chunk(c.smem_slot, c.lane, 4 * H + k)),
+                     "r"(0u)
+                     : "memory");
+    const int j0 = H * (C::COLS / 2);
+    const int j1 = min(ncols, (H + 1) * (C::COLS / 2));
+#pragma unroll 1
+    for (int j = j0; j < j1; ++j) {
+        if constexpr (F32) {
+            uint32_t w;
+            asm volatile("ld.global.b32 %0, [%1];" : "=r"(w) : "l"(src + 4 * j) : "memory");
+            asm volatile("st.shared.b32 [%0], %1;" ::"r"(smem_byte(c, 4 * j)), "r"(w) : "memory");
+        } else {
+            uint16_t w;
+            asm volatile("ld.global.u16 %0, [%1];" : "=h"(w) : "l"(src + 2 * j) : "memory");
+            asm volatile("st.shared.u16 [%0], %1;" ::"r"(smem_byte(c, 2 * j)), "h"(w) : "memory");
+        }
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(v[4 * k]), "=r"(v[4 * k + 1]), "=r"(v[4 * k + 2]), "=r"(v[4 * k + 3])
+                     : "r"(smem_chunk(c.smem_slot, c.lane, 4 * H + k))
+                     : "memory");
+}
+
+// Half H (words 16H .. 16H+15) of deep slot s (TMEM, shared memory or the
+// parked output) -> t. Deep slots are read in halves to keep the
+// epilogue's register peak low.
+template <bool F32, int H>
+__device__ __forceinline__ void load_slot_half(int s, uint32_t (&t)[16], const EpiCtx &c, const Params &p)
+{
+    using C = Cfg<F32>;
+    if (s < C::SMEM_FIRST) {
+        tmem_ld16(c.tmem_slot + static_cast<uint32_t>((s - C::TMEM_FIRST) * 64 + 16 * H), t);
+        tmem_wait_ld();
+        reg_fence16(t);
+    } else if (s < C::OUT_SLOT) {
+        const uint32_t base = c.smem_slot + static_cast<uint32_t>((s - C::SMEM_FIRST) * C::SMEM_SLOT_BYTES);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(t[4 * k]), "=r"(t[4 * k + 1]), "=r"(t[4 * k + 2]), "=r"(t[4 * k + 3])
+                         : "r"(smem_chunk(base, c.lane, 4 * H + k))
+                         : "memory");
+        }
+    } else {
+        load_out_half<F32, H>(t, p, c);
+    }
+}
+
+// v -> deep slot s held in TMEM or shared memory.
+template <bool F32>
+__device__ __forceinline__ void store_slot(int s, const uint32_t (&v)[32], const EpiCtx &c)
+{
+    using C = Cfg<F32>;
+    if (s < C::SMEM_FIRST) {
+        tmem_st32(c.tmem_slot + static_cast<uint32_t>((s - C::TMEM_FIRST) * 64), v);
+        tmem_wait_st();
+    } else {
+        const uint32_t base = c.smem_slot + static_cast<uint32_t>((s - C::SMEM_FIRST) * C::SMEM_SLOT_BYTES);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(smem_chunk(base, c.lane, k)),
+                         "r"(v[4 * k]), "r"(v[4 * k + 1]), "r"(v[4 * k + 2]), "r"(v[4 * k + 3])
+                         : "memory");
+        }
+    }
+}
+
+// Issues the TMEM load of one accumulator (this thread's row, its BN/2
+// columns) into the staging registers; tcgen05.wait::ld completes it.
+template <bool F32>
+__device__ __forceinline__ void stage_load(uint32_t acc_taddr, uint32_t (&stg)[64])
+{
+    uint32_t(&lo)[32] = *reinterpret_cast<uint32_t(*)[32]>(&stg[0]);
+    tmem_ld32(acc_taddr, lo);
+    if constexpr (!F32) {
+        uint32_t(&hi)[32] = *reinterpret_cast<uint32_t(*)[32]>(&stg[32]);
+        tmem_ld32(acc_taddr + 32, hi);
+    }
+}
+
+template <bool F32>
+__device__ __forceinline__ void stage_wait(uint32_t (&stg)[64])
+{
+    uint32_t(&lo)[32] = *reinterpret_cast<uint32_t(*)[32]>(&stg[0]);
+    tmem_wait_ld();
+    reg_fence(lo);
+    if constexpr (!F32) {
+        uint32_t(&hi)[32] = *reinterpret_cast<uint32_t(*)[32]>(&stg[32]);
+        reg_fence(hi);
+    }
+}
+
+// The staged leaf -> F: rounded once to BF16 (RNE), two columns per word,
+// for the bf16 variant; as is for the fp32 variant.
+template <bool F32>
+__device__ __forceinline__ void stage_convert(const uint32_t (&stg)[64], uint32_t (&F)[32])
+{
+    if constexpr (F32) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) F[i] = stg[i];
+    } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) F[i] = cvt_bf16x2(stg[2 * i], stg[2 * i + 1]);
+    }
+}
+
+// ----------------------------------------------------------------- kernel
+
+// Shared-memory and TMEM addresses of one CTA.
+template <bool F32>
+struct Smem {
+    uint32_t sA, sB, sSlots, bar0, tmem;
+    volatile int *abort_flag;
+    __device__ uint32_t full(int s) const { return bar0 + 8u * s; }
+    __device__ uint32_t empty(int s) const { return bar0 + 8u * (Cfg<F32>::STAGES + s); }
+    __device__ uint32_t accf(int b) const { return bar0 + 8u * (2 * Cfg<F32>::STAGES + b); }
+    __device__ uint32_t acce(int b) const { return bar0 + 8u * (2 * Cfg<F32>::STAGES + Cfg<F32>::NACC + b); }
+    __device__ uint32_t never() const { return bar0 + 8u * (2 * Cfg<F32>::STAGES + 2 * Cfg<F32>::NACC); }
+    __device__ uint32_t drain() const { return never() + 8u; }
+};
+
+// TMA producer (one lane): streams the A and B K-stages of every tile.
+template <int A_MAJOR, int B_MAJOR, bool F32>
+__device__ __forceinline__ void producer_role(const Params &p, const Smem<F32> &S)
+{
+    using C = Cfg<F32>;
+    const int num_tiles = p.m_tiles * p.n_tiles;
+    const int num_kstages = (p.num_leaves + 1) / 2;
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t issued = 0;          // bit s: stage s has had a load issued
+    uint32_t issued_parity = 0;   // bit s: parity of that stage's last load
+    bool ok = true;
+    for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+        int mt, nt;
+        tile_coords(t, p.m_tiles, p.n_tiles, mt, nt);
+        const int m0 = mt * kBM, n0 = nt * C::BN;
+        for (int ks = 0; ks < num_kstages; ++ks) {
+            if (!wait_bounded(S.empty(stage), phase ^ 1u, S.abort_flag, p.status, p.timeout_ns, true)) {
+                ok = false;
+                break;
+            }
+            const uint32_t fb = S.full(stage);
+            mbar_arrive_expect_tx(fb, C::STAGE_TX);
+            const uint32_t a_dst = S.sA + stage * C::A_STAGE;
+            const uint32_t b_dst = S.sB + stage * C::B_STAGE;
+            const int k0 = ks * kBK;
+            if constexpr (A_MAJOR == kKMajor) {
+                tma_load_2d(a_dst, &p.tmap_a, fb, k0, m0);
+            } else {
+                tma_load_2d(a_dst, &p.tmap_a, fb, m0, k0);
+                tma_load_2d(a_dst + 8192, &p.tmap_a, fb, m0 + 64, k0);
+            }
+            if constexpr (B_MAJOR == kKMajor) {
+                tma_load_2d(b_dst, &p.tmap_b, fb, k0, n0);
+            } else {
+#pragma unroll
+                for (int b = 0; b < C::BN / 64; ++b) tma_load_2d(b_dst + 8192 * b, &p.tmap_b, fb, n0 + 64 * b, k0);
+            }
+            issued |= 1u << stage;
+            issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
+            if (++stage == C::STAGES) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+    }
+    if (!ok) {
+        // Abandoned: let every load already issued land before the CTA and
+        // its shared memory go away.
+        for (int s = 0; s < C::STAGES; ++s)
+            if ((issued >> s) & 1u)
+                wait_bounded(S.full(s), (issued_parity >> s) & 1u, S.abort_flag, p.status, p.timeout_ns, false);
+    }
+}
+
+// MMA issuer (one lane): two K=16 MMAs per leaf into a fresh accumulator.
+template <int A_MAJOR, int B_MAJOR, bool F32>
+__device__ __forceinline__ void mma_role(const Params &p, const Smem<F32> &S)
+{
+    using C = Cfg<F32>;
+    constexpr uint32_t IDESC = idesc_bf16(kBM, C::BN, A_MAJOR, B_MAJOR);
+    // Byte offset of K step k (16 contraction elements) inside a stage:
+    // K-major rows hold the stage's 64 contraction elements (128 B), so a
+    // step is 32 B along the row; MN-major tiles hold one 128 B row per
+    // contraction index, so a step is 16 rows = 2048 B. Descriptors address
+    // in 16-byte units, so offsets are added to the start-address field.
+    constexpr uint32_t A_KSTEP = ((A_MAJOR == kKMajor) ? 32u : 2048u) >> 4;
+    constexpr uint32_t B_KSTEP = ((B_MAJOR == kKMajor) ? 32u : 2048u) >> 4;
+    constexpr uint32_t A_LBO = (A_MAJOR == kKMajor) ? 16u : 8192u;
+    constexpr uint32_t B_LBO = (B_MAJOR == kKMajor) ? 16u : 8192u;
+    const uint64_t a_desc0 = sdesc(S.sA, A_LBO, 1024u);
+    const uint64_t b_desc0 = sdesc(S.sB, B_LBO, 1024u);
+    const int num_tiles = p.m_tiles * p.n_tiles;
+    const int L = p.num_leaves;
+    int stage = 0;
+    uint32_t phase = 0;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    bool issued_any = false;
+    if (p.force_timeout) {
+        // Test hook: a wait that nothing will end.
+        ok = wait_bounded(S.never(), 0, S.abort_flag, p.status, p.timeout_ns, true);
+    }
+    for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+        for (int l = 0; l < L; l += 2) {
+            if (!wait_bounded(S.full(stage), phase, S.abort_flag, p.status, p.timeout_ns, true)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint64_t a_st = a_desc0 + static_cast<uint64_t>(stage * (C::A_STAGE >> 4));
+            const uint64_t b_st = b_desc0 + static_cast<uint64_t>(stage * (C::B_STAGE >> 4));
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                if (l + j >= L) break;
+                if (!wait_bounded(S.acce(acc), acc_phase ^ 1u, S.abort_flag, p.status, p.timeout_ns, true)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d = S.tmem + static_cast<uint32_t>(acc * C::BN);
+                mma_bf16(d, a_st + (2 * j) * A_KSTEP, b_st + (2 * j) * B_KSTEP, IDESC, 0u);   // fresh leaf
+                mma_bf16(d, a_st + (2 * j + 1) * A_KSTEP, b_st + (2 * j + 1) * B_KSTEP, IDESC, 1u);
+                issued_any = true;
+                mma_commit(S.accf(acc));
+                if (++acc == C::NACC) {
+                    acc = 0;
+                    acc_phase ^= 1u;
+                }
+            }
+            if (!ok) break;
+            mma_commit(S.empty(stage));
+            if (++stage == C::STAGES) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+    }
+    if (!ok && issued_any) {
+        // Abandoned: wait for the MMAs in flight before TMEM is released.
+        mma_commit(S.drain());
+        wait_bounded(S.drain(), 0, S.abort_flag, p.status, p.timeout_ns, false);
+    }
+}
+
+// Epilogue warp: leaf rounding and the merge tree for one row and BN/2
+// columns of every tile.
+//
+// The tree is walked in units. In a mid-split tree every leaf's parent has
+// two or three leaves below it, so each leaf is either one of a sibling
+// pair, merged at once, or the single left child of a three-leaf node,
+// which is parked in slot 1 (height 2). In the per-leaf schedule a pair's
+// first leaf is the one parked in slot 0, and the second leaf's entry holds
+// the pair's merges and park. Pending partials: slots 1-2 in registers,
+// then TMEM, shared memory, and for slot 9 the thread's own output.
+template <bool F32>
+__device__ __forceinline__ void epilogue_role(const Params &p, const Smem<F32> &S, int warp, int lane)
+{
+    using C = Cfg<F32>;
+    const int q = warp & 3;               // TMEM lane quadrant (rows 32q .. 32q+31)
+    const int h = warp >> 2;              // column half of the tile
+    const uint32_t lane_bits = static_cast<uint32_t>(q * 32) << 16;
+    const uint32_t acc0 = S.tmem + lane_bits + static_cast<uint32_t>(h * C::COLS);
+    EpiCtx c;
+    c.tmem_slot = S.tmem + lane_bits + static_cast<uint32_t>(C::TMEM_SLOT_BASE + h * 32);
+    c.smem_slot = S.sSlots + static_cast<uint32_t>(warp * 32 + lane) * 128u;
+    c.lane = lane;
+    const int num_tiles = p.m_tiles * p.n_tiles;
+    const int L = p.num_leaves;
+
+    uint32_t X[32], Y[32], S1[32], S2[32], stg[64];
+    int acc = 0;                          // accumulator of the next leaf
+    uint32_t acc_phase = 0;
+    auto release = [&](int a) {
+        // The MMA may now overwrite accumulator a with the leaf NACC ahead.
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(S.acce(a));
+    };
+    auto bump = [&]() {
+        if (++acc == C::NACC) {
+            acc = 0;
+            acc_phase ^= 1u;
+        }
+    };
+    auto acc_addr = [&](int a) { return acc0 + static_cast<uint32_t>(a * C::BN); };
+
+    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+        int mt, nt;
+        tile_coords(t, p.m_tiles, p.n_tiles, mt, nt);
+        c.row = mt * kBM + q * 32 + lane;
+        c.col = nt * C::BN + h * C::COLS;
+        for (int l = 0; l < L;) {
+            const uint32_t e = p.sched[l];
+            if ((e >> 12) == 0) {
+                // ---- a sibling pair (l, l + 1); the MMA commits are
+                // cumulative, so the second leaf's barrier covers both.
+                const uint32_t e2 = p.sched[l + 1];
+                const int a0 = acc;
+                bump();
+                const int a1 = acc;
+                const uint32_t ph1 = acc_phase;
+                bump();
+                const bool got = wait_bounded(S.accf(a1), ph1, S.abort_flag, p.status, p.timeout_ns, true);
+                if (!__all_sync(0xFFFFFFFFu, got)) return;
+                tc_fence_after();
+                stage_load<F32>(acc_addr(a0), stg);
+                stage_wait<F32>(stg);
+                release(a0);
+                stage_convert<F32>(stg, X);
+                stage_load<F32>(acc_addr(a1), stg);
+                stage_wait<F32>(stg);
+                release(a1);
+                stage_convert<F32>(stg, Y);
+                const uint32_t mask = e2 & 0x3FEu;   // slots above 0 (bit 0 is the pair itself)
+                const int st = static_cast<int>(e2 >> 12);
+                if (mask == 0 && st == 1) {
+                    // the pair is a left child of height 2: park it
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) S1[i] = merge<F32>(X[i], Y[i]);
+                } else if (mask == 2u && st == 2) {
+                    // right child of height 2, whose parent is a left child
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) X[i] = merge<F32>(X[i], Y[i]);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) S2[i] = merge<F32>(S1[i], X[i]);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) X[i] = merge<F32>(X[i], Y[i]);
+                    if (mask & 2u) merge_all<F32>(X, S1);
+                    if (mask & 4u) merge_all<F32>(X, S2);
+                    if (mask >> C::TMEM_FIRST) {
+#pragma unroll 1
+                        for (int s = C::TMEM_FIRST; s < kMaxSlots; ++s) {
+                            if (!((mask >> s) & 1u)) continue;
+                            uint32_t tt[16];
+                            load_slot_half<F32, 0>(s, tt, c, p);
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) X[i] = merge<F32>(tt[i], X[i]);
+                            load_slot_half<F32, 1>(s, tt, c, p);
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) X[16 + i] = merge<F32>(tt[i], X[16 + i]);
+                        }
+                    }
+                    if (st == 1) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) S1[i] = X[i];
+                    } else if (st == 2) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) S2[i] = X[i];
+                    } else if (st == kSlotRoot || st == C::OUT_SLOT) {
+                        store_out<F32>(X, p, c);
+                    } else {
+                        store_slot<F32>(st, X, c);
+                    }
+                }
+                l += 2;
+            } else {
+                // ---- a single leaf: the left child of a three-leaf node
+                // (parked in slot 1), or the whole tree when L == 1.
+                const bool got = wait_bounded(S.accf(acc), acc_phase, S.abort_flag, p.status, p.timeout_ns, true);
+                if (!__all_sync(0xFFFFFFFFu, got)) return;
+                tc_fence_after();
+                const int a0 = acc;
+                bump();
+                stage_load<F32>(acc_addr(a0), stg);
+                stage_wait<F32>(stg);
+                release(a0);
+                if ((e >> 12) == kSlotRoot) {
+                    stage_convert<F32>(stg, X);
+                    store_out<F32>(X, p, c);
+                } else {
+                    stage_convert<F32>(stg, S1);
+                }
+                l += 1;
+            }
+        }
+    }
+}
+
+template <int A_MAJOR, int B_MAJOR, bool F32>
+__global__ void __launch_bounds__(kThreads, 1) det_gemm_kernel(const __grid_constant__ Params p)
+{
+    using C = Cfg<F32>;
+    extern __shared__ uint8_t smem_raw[];
+    // 128-byte swizzle atoms need 1024-byte aligned buffers.
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t *smem = smem_raw + (base - raw);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    Smem<F32> S;
+    S.sA = base + C::OFF_A;
+    S.sB = base + C::OFF_B;
+    S.sSlots = base + C::OFF_SLOTS;
+    S.bar0 = base + C::OFF_BAR;
+    uint32_t *tmem_base_smem = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
+    S.abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
+
+    // ---- set-up: barriers, TMEM allocation
+    if (threadIdx.x == 0) {
+        *S.abort_flag = 0;
+        for (int s = 0; s < C::STAGES; ++s) {
+            mbar_init(S.full(s), 1);
+            mbar_init(S.empty(s), 1);
+        }
+        for (int b = 0; b < C::NACC; ++b) {
+            mbar_init(S.accf(b), 1);
+            mbar_init(S.acce(b), kEpiWarps);
+        }
+        mbar_init(S.never(), 1);
+        mbar_init(S.drain(), 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 8 && lane == 0) {
+        tmap_prefetch(&p.tmap_a);
+        tmap_prefetch(&p.tmap_b);
+    }
+    if (warp == 9) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(tmem_base_smem)),
+                     "r"(C::TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    S.tmem = *tmem_base_smem;
+
+    // Register split: the producer warpgroup gives up registers and the two
+    // epilogue warpgroups take them (kProdRegs*128 + kEpiRegs*256 equals the
+    // 168 x 384 registers the CTA is launched with). Each role's code sits
+    // inside its own branch so that the compiler allocates it under the
+    // matching limit.
+    if (warp >= kEpiWarps) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kProdRegs));
+        if (warp == 8 && lane == 0) producer_role<A_MAJOR, B_MAJOR, F32>(p, S);
+        else if (warp == 9 && lane == 0) mma_role<A_MAJOR, B_MAJOR, F32>(p, S);
+    } else {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kEpiRegs));
+        epilogue_role<F32>(p, S, warp, lane);
+    }
+
+    // ---- teardown
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 9) {
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(S.tmem), "r"(C::TMEM_COLS)
+                     : "memory");
+    }
+}
+
+// --------------------------------------------------------- host launcher
+
+template <int A_MAJOR, int B_MAJOR, bool F32>
+struct Launcher {
+    static cudaError_t prepare(int *num_regs)
+    {
+        auto fn = det_gemm_kernel<A_MAJOR, B_MAJOR, F32>;
+        cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             Cfg<F32>::SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        cudaFuncAttributes at;
+        e = cudaFuncGetAttributes(&at, fn);
+        if (e != cudaSuccess) return e;
+        *num_regs = at.numRegs;
+        return cudaSuccess;
+    }
+    static cudaError_t launch(const Params &p, int grid, cudaStream_t stream)
+    {
+        det_gemm_kernel<A_MAJOR, B_MAJOR, F32><<<grid, kThreads, Cfg<F32>::SMEM_BYTES, stream>>>(p);
+        return cudaGetLastError();
+    }
+    static VariantOps ops()
+    {
+        VariantOps o;
+        o.prepare = &prepare;
+        o.launch = &launch;
+        o.bn = Cfg<F32>::BN;
+        o.smem_bytes = Cfg<F32>::SMEM_BYTES;
+        return o;
+    }
+};
+
+}  // namespace detg

@@ -1,0 +1,152 @@
+"""Host-side checks of the C-ABI library: it loads, exports what the header
+declares, rejects bad arguments before touching a GPU, and its per-leaf merge
+schedule replays the mid-split tree exactly. No GPU needed."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "det_gemm.h")
+
+
+@pytest.fixture(scope="module")
+def dg():
+    from invariant_deterministic_gemm_gb300 import _build
+    _build.build()
+    import invariant_deterministic_gemm_gb300 as m
+    m.lib()
+    return m
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(det_gemm_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_page_surface():
+    names = declared_functions()
+    for n in ("det_gemm_fwd", "det_gemm_fwd_rhs_transposed", "det_gemm_fwd_fp32", "det_gemm_da",
+              "det_gemm_db", "det_gemm_db_transposed", "det_gemm_check", "det_gemm_status_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(dg):
+    L = dg.lib()
+    for n in declared_functions():
+        assert hasattr(L, n), n
+
+
+def test_status_strings_and_version(dg):
+    L = dg.lib()
+    assert L.det_gemm_abi_version() == 1
+    for code in range(8):
+        s = dg.status_string(code)
+        assert s.startswith(dg.STATUS_NAMES[code])
+    assert "unknown" in dg.status_string(99)
+
+
+P = 0x10000   # a 16-byte aligned fake device address; never dereferenced here
+
+
+def call(dg, name, x, y, o, M, N, K, ldx, ldy, ldo):
+    return getattr(dg.lib(), name)(x, y, o, M, N, K, ldx, ldy, ldo, None)
+
+
+@pytest.mark.parametrize("name", ["det_gemm_fwd", "det_gemm_fwd_rhs_transposed", "det_gemm_fwd_fp32",
+                                  "det_gemm_fwd_fp32_rhs_transposed"])
+def test_forward_argument_errors_are_returned_before_any_launch(dg, name):
+    ok_ld = 4096
+    assert call(dg, name, P, P * 8, P * 64, 4, 8, 32769, 32776, 32776, ok_ld) == 2   # K too large
+    assert call(dg, name, P, P * 8, P * 64, -1, 8, 8, 8, 8, 8) == 1                  # negative size
+    assert call(dg, name, 0, P * 8, P * 64, 4, 8, 8, 8, 8, 8) == 1                   # null input
+    assert call(dg, name, P, P * 8, 0, 4, 8, 8, 8, 8, 8) == 1                        # null output
+    assert call(dg, name, P + 2, P * 8, P * 64, 4, 8, 8, 8, 8, 8) == 3               # misaligned base
+    assert call(dg, name, P, P * 8, P * 64, 4, 8, 12, 12, 16, 16) == 3               # lda*2 not /16
+    assert call(dg, name, P, P * 8, P * 64, 4, 8, 16, 8, 16, 16) == 1                # lda < K
+    assert call(dg, name, P, P, P, 4, 8, 8, 8, 8, 8) == 1                            # output overlaps
+    # empty outputs are fine and enqueue nothing
+    assert call(dg, name, 0, 0, 0, 0, 8, 8, 8, 8, 8) == 0
+    assert call(dg, name, 0, 0, 0, 4, 0, 8, 8, 8, 8) == 0
+
+
+def test_backward_argument_errors(dg):
+    # dA: contraction over N
+    assert call(dg, "det_gemm_da", P, P * 8, P * 64, 4, 32769, 8, 32776, 32776, 8) == 2
+    # dB: contraction over M
+    assert call(dg, "det_gemm_db", P, P * 8, P * 64, 32769, 8, 8, 8, 8, 8) == 2
+    assert call(dg, "det_gemm_db_transposed", P, P * 8, P * 64, 32769, 8, 8, 8, 8, 8) == 2
+    # M = 40000 is fine for the forward (rows) but not for dB (contraction)
+    assert call(dg, "det_gemm_db", P, P * 8, 0, 40000, 8, 8, 8, 8, 8) == 2
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU answer")
+def test_valid_arguments_without_a_gpu_report_unsupported_device(dg):
+    assert call(dg, "det_gemm_fwd", P, P * 8, P * 64, 4, 8, 8, 8, 8, 8) == 4
+
+
+# ---------------------------------------------------------- tree schedule
+
+def mid_split_tree(lo, hi):
+    """The tree as nested tuples, written from the definition."""
+    if hi - lo == 1:
+        return lo
+    mid = (lo + hi) // 2
+    return (mid_split_tree(lo, mid), mid_split_tree(mid, hi))
+
+
+def replay(sched):
+    """Run the per-leaf schedule on symbolic leaves, the way the kernel does:
+    merge the running value with the pending slots named in the mask (lowest
+    first; the pending value is the left operand), then park it in a slot or
+    emit it as the root. Checks that every slot is written before it is read
+    and never overwritten while pending."""
+    slots = {}
+    root = None
+    for leaf, e in enumerate(sched):
+        mask, store = e & 0x3FF, e >> 12
+        assert (e >> 10) & 3 == 0
+        v = leaf
+        for s in range(10):
+            if mask >> s & 1:
+                assert s in slots, ("read of an empty slot", leaf, s)
+                v = (slots.pop(s), v)
+        if store == 15:
+            assert root is None
+            root = v
+        else:
+            assert store < 10 and store not in slots, ("overwrite", leaf, store)
+            assert all(store > s for s in range(10) if mask >> s & 1)
+            slots[store] = v
+    assert not slots, "partials left over"
+    return root
+
+
+def test_schedule_replays_the_mid_split_tree_for_every_leaf_count(dg):
+    for L in range(1, 1025):
+        sched = dg.det_gemm_tree_schedule(L)
+        assert len(sched) == L
+        assert replay(sched) == mid_split_tree(0, L), L
+
+
+def test_schedule_slot_depth_fits_ten_slots(dg):
+    for L in (512, 513, 1000, 1024):
+        sched = dg.det_gemm_tree_schedule(L)
+        used = set()
+        for e in sched:
+            m, s = e & 0x3FF, e >> 12
+            used |= {b for b in range(10) if m >> b & 1}
+            if s != 15:
+                used.add(s)
+        assert max(used) == (L - 1).bit_length() - 1
+
+
+def test_schedule_rejects_bad_counts(dg):
+    L = dg.lib()
+    buf = (ctypes.c_uint16 * 2)()
+    assert L.det_gemm_tree_schedule(0, buf) == 1
+    assert L.det_gemm_tree_schedule(1025, buf) == 1
+    assert L.det_gemm_tree_schedule(4, None) == 1
