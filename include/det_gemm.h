@@ -43,7 +43,12 @@
  *   - Outputs must not overlap inputs (DET_GEMM_ERR_INVALID_ARG otherwise).
  *   - A device-side failure (a bounded wait that expired) is reported by
  *     det_gemm_check(), not by the launching call.
- *   - The library allocates no device memory per call.
+ *   - The library allocates no device memory per call. It keeps one small
+ *     device scratch buffer per (device, stream) it has launched on (one CTA
+ *     per SM x 96 KiB: the tree's most rarely touched pending partials), created
+ *     on the first launch on that stream and reused by every later one, so
+ *     launches on different streams never share it. det_gemm_shutdown()
+ *     releases them.
  */
 #ifndef DET_GEMM_H
 #define DET_GEMM_H
@@ -164,6 +169,26 @@ int det_gemm_abi_version(void);
  * DET_GEMM_ERR_INVALID_ARG for a bad count or a NULL out.
  */
 det_gemm_status det_gemm_tree_schedule(int64_t num_leaves, uint16_t *out);
+
+/*
+ * Host-only helper, no GPU needed: the block schedule the kernels walk. The
+ * tree is cut into its maximal subtrees of at most four leaves (for a tree
+ * of more than four leaves these have 2, 3 or 4 leaves), in leaf order;
+ * out[b] describes block b: bits 10..11 hold (leaves in the block - 1);
+ * bits 0..9 the pending-partial slots its value is merged with, lowest
+ * first; bits 12..15 the slot its result is parked in, or 15 for the root.
+ * It is the per-leaf entry of the block's last leaf (det_gemm_tree_schedule)
+ * with the merges inside the block removed. `out` needs num_leaves entries;
+ * *num_blocks receives the count.
+ */
+det_gemm_status det_gemm_block_schedule(int64_t num_leaves, uint16_t *out, int64_t *num_blocks);
+
+/*
+ * Frees the per-stream scratch buffers and forgets them; the next launch on
+ * a stream allocates again. Call only when no det_gemm work is in flight
+ * (it waits for the devices it frees on).
+ */
+det_gemm_status det_gemm_shutdown(void);
 
 /*
  * Test hook: while `enable` is nonzero, every GEMM launch makes its MMA warp

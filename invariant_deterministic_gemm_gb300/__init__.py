@@ -81,6 +81,10 @@ def lib() -> ctypes.CDLL:
         L.det_gemm_abi_version.restype = ctypes.c_int
         L.det_gemm_tree_schedule.argtypes = [i64, p]
         L.det_gemm_tree_schedule.restype = ctypes.c_int
+        L.det_gemm_block_schedule.argtypes = [i64, p, p]
+        L.det_gemm_block_schedule.restype = ctypes.c_int
+        L.det_gemm_shutdown.argtypes = []
+        L.det_gemm_shutdown.restype = ctypes.c_int
         L.det_gemm_debug_force_timeout.argtypes = [ctypes.c_int]
         L.det_gemm_debug_force_timeout.restype = ctypes.c_int
         _lib = L
@@ -248,6 +252,21 @@ def det_gemm_tree_schedule(num_leaves: int) -> list[int]:
     return list(buf)[:num_leaves]
 
 
+def det_gemm_block_schedule(num_leaves: int) -> list[int]:
+    """Host-only: the block schedule the kernels walk (see det_gemm.h)."""
+    buf = (ctypes.c_uint16 * max(1, num_leaves))()
+    nb = ctypes.c_int64(0)
+    st = lib().det_gemm_block_schedule(int(num_leaves), buf, ctypes.byref(nb))
+    if st != OK:
+        raise DetGemmError(st, "det_gemm_block_schedule")
+    return list(buf)[:nb.value]
+
+
+def det_gemm_shutdown() -> None:
+    """Free the library's cached per-stream scratch (see det_gemm.h)."""
+    lib().det_gemm_shutdown()
+
+
 def det_gemm_debug_force_timeout(enable: bool) -> None:
     """Test hook: make every later launch time out on purpose (see det_gemm.h)."""
     lib().det_gemm_debug_force_timeout(1 if enable else 0)
@@ -256,6 +275,6 @@ def det_gemm_debug_force_timeout(enable: bool) -> None:
 __all__ = [
     "det_gemm_fwd", "det_gemm_fwd_rhs_transposed", "det_gemm_fwd_fp32",
     "det_gemm_fwd_fp32_rhs_transposed", "det_gemm_da", "det_gemm_db",
-    "det_gemm_db_transposed", "det_gemm_check", "det_gemm_tree_schedule",
-    "det_gemm_debug_force_timeout", "DetGemmError", "lib", "status_string",
+    "det_gemm_db_transposed", "det_gemm_check", "det_gemm_tree_schedule", "det_gemm_block_schedule",
+    "det_gemm_debug_force_timeout", "det_gemm_shutdown", "DetGemmError", "lib", "status_string",
 ]

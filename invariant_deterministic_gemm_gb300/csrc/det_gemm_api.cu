@@ -35,9 +35,22 @@ struct DeviceState {
 
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
+
+// Deep-slot scratch, one buffer per (device, stream) so that launches on
+// different streams never share one; allocated on first use, reused by
+// every later launch on that stream, freed by det_gemm_shutdown().
+struct ScratchEntry {
+    int device;
+    cudaStream_t stream;
+    void *ptr;
+    size_t bytes;
+};
+constexpr int kMaxScratch = 64;
+ScratchEntry g_scratch[kMaxScratch];
+int g_scratch_count = 0;
+int g_scratch_next_evict = 0;
 int g_force_timeout = 0;
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
-uint16_t *g_sched_cache[kMaxLeaves + 1] = {};
 
 VariantOps variant_ops(Variant v)
 {
@@ -104,16 +117,51 @@ void build_schedule(int64_t L, uint16_t *out)
     }
 }
 
-const uint16_t *schedule_for(int64_t L)
+// The block schedule (format in det_gemm.h): the tree cut into its maximal
+// subtrees of at most four leaves, in leaf order. A block's leaves are
+// merged among themselves in registers; its entry says which pending
+// partials to merge its value with and where to park the result, which is
+// the per-leaf entry of its last leaf without the merges inside the block.
+void add_blocks(const uint16_t *leaf_sched, int64_t lo, int64_t hi, uint16_t *out, int64_t *nb)
+{
+    const int64_t n = hi - lo;
+    if (n > 4) {
+        const int64_t mid = (lo + hi) >> 1;
+        add_blocks(leaf_sched, lo, mid, out, nb);
+        add_blocks(leaf_sched, mid, hi, out, nb);
+        return;
+    }
+    const uint32_t e = leaf_sched[hi - 1];
+    const int h = ceil_log2(n);                  // the block's height
+    const uint32_t up = (e & 0x3FFu) & ~((1u << h) - 1u);
+    out[(*nb)++] = static_cast<uint16_t>(up | (static_cast<uint32_t>(n - 1) << 10) | (e & 0xF000u));
+}
+
+void build_blocks(int64_t L, uint16_t *out, int64_t *nb)
+{
+    uint16_t leaf_sched[kMaxLeaves];
+    build_schedule(L, leaf_sched);
+    *nb = 0;
+    add_blocks(leaf_sched, 0, L, out, nb);
+}
+
+struct BlockSchedule {
+    uint16_t *entries;
+    int64_t count;
+};
+BlockSchedule g_block_cache[kMaxLeaves + 1] = {};
+
+const BlockSchedule *blocks_for(int64_t L)
 {
     std::lock_guard<std::mutex> lk(g_mu);
-    if (!g_sched_cache[L]) {
+    if (!g_block_cache[L].entries) {
         uint16_t *s = static_cast<uint16_t *>(std::malloc(sizeof(uint16_t) * L));
         if (!s) return nullptr;
-        build_schedule(L, s);
-        g_sched_cache[L] = s;
+        int64_t nb = 0;
+        build_blocks(L, s, &nb);
+        g_block_cache[L] = BlockSchedule{s, nb};
     }
-    return g_sched_cache[L];
+    return &g_block_cache[L];
 }
 
 // ---------------------------------------------------------- validation
@@ -210,6 +258,45 @@ det_gemm_status prepare_variant(DeviceState *st, Variant v)
     return st->prepare_status[v];
 }
 
+// Scratch of at least `bytes` for launches on `stream` of the current device.
+void *scratch_for(int device, cudaStream_t stream, size_t bytes)
+{
+    std::lock_guard<std::mutex> lk(g_mu);
+    for (int i = 0; i < g_scratch_count; ++i) {
+        ScratchEntry &e = g_scratch[i];
+        if (e.device == device && e.stream == stream) {
+            if (e.bytes >= bytes) return e.ptr;
+            // Grow: cudaFree waits for the device, so no launch still uses it.
+            cudaFree(e.ptr);
+            e.ptr = nullptr;
+            if (cudaMalloc(&e.ptr, bytes) != cudaSuccess) {
+                cudaGetLastError();
+                e.ptr = nullptr;
+                e.bytes = 0;
+                return nullptr;
+            }
+            e.bytes = bytes;
+            return e.ptr;
+        }
+    }
+    int slot;
+    if (g_scratch_count < kMaxScratch) {
+        slot = g_scratch_count++;
+    } else {
+        slot = g_scratch_next_evict;
+        g_scratch_next_evict = (g_scratch_next_evict + 1) % kMaxScratch;
+        cudaFree(g_scratch[slot].ptr);   // waits for the device first
+    }
+    void *ptr = nullptr;
+    if (cudaMalloc(&ptr, bytes) != cudaSuccess) {
+        cudaGetLastError();
+        g_scratch[slot] = ScratchEntry{device, stream, nullptr, 0};
+        return nullptr;
+    }
+    g_scratch[slot] = ScratchEntry{device, stream, ptr, bytes};
+    return ptr;
+}
+
 bool encode(CUtensorMap *m, const void *ptr, uint64_t inner, uint64_t outer, uint64_t ld_elems,
             uint32_t box_inner, uint32_t box_outer)
 {
@@ -254,8 +341,8 @@ det_gemm_status run(Variant v, Mat a, bool a_kmajor, Mat b, bool b_kmajor, Mat o
     VariantOps ops = variant_ops(v);
 
     const int64_t L = (kc + kLeaf - 1) / kLeaf;
-    const uint16_t *sched = schedule_for(L);
-    if (!sched) return DET_GEMM_ERR_LAUNCH;
+    const BlockSchedule *blocks = blocks_for(L);
+    if (!blocks) return DET_GEMM_ERR_LAUNCH;
 
     Params p;
     std::memset(&p, 0, sizeof(p));
@@ -269,6 +356,14 @@ det_gemm_status run(Variant v, Mat a, bool a_kmajor, Mat b, bool b_kmajor, Mat o
     if (!ok) return DET_GEMM_ERR_LAUNCH;
     p.out = const_cast<void *>(out.ptr);
     p.ldo = out.ld;
+    {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        // Sized for the largest variant and a grid of one CTA per SM, so
+        // every launch on this stream can reuse it.
+        p.scratch = scratch_for(dev, stream, static_cast<size_t>(st->sm_count) * kMaxScratchCtaBytes);
+        if (!p.scratch) return DET_GEMM_ERR_LAUNCH;
+    }
     p.status = st->status_ptr;
     p.timeout_ns = timeout_ns();
     p.rows = static_cast<int>(rows);
@@ -278,7 +373,8 @@ det_gemm_status run(Variant v, Mat a, bool a_kmajor, Mat b, bool b_kmajor, Mat o
     p.m_tiles = static_cast<int>((rows + kBM - 1) / kBM);
     p.n_tiles = static_cast<int>((cols + ops.bn - 1) / ops.bn);
     p.force_timeout = g_force_timeout;
-    std::memcpy(p.sched, sched, sizeof(uint16_t) * L);
+    p.num_blocks = static_cast<int>(blocks->count);
+    std::memcpy(p.blocks, blocks->entries, sizeof(uint16_t) * blocks->count);
 
     const int64_t tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
     if (tiles > (int64_t{1} << 31) - 1) return DET_GEMM_ERR_INVALID_ARG;
@@ -411,6 +507,33 @@ det_gemm_status det_gemm_tree_schedule(int64_t num_leaves, uint16_t *out)
 {
     if (out == nullptr || num_leaves < 1 || num_leaves > kMaxLeaves) return DET_GEMM_ERR_INVALID_ARG;
     build_schedule(num_leaves, out);
+    return DET_GEMM_OK;
+}
+
+det_gemm_status det_gemm_block_schedule(int64_t num_leaves, uint16_t *out, int64_t *num_blocks)
+{
+    if (out == nullptr || num_blocks == nullptr || num_leaves < 1 || num_leaves > kMaxLeaves)
+        return DET_GEMM_ERR_INVALID_ARG;
+    build_blocks(num_leaves, out, num_blocks);
+    return DET_GEMM_OK;
+}
+
+det_gemm_status det_gemm_shutdown(void)
+{
+    std::lock_guard<std::mutex> lk(g_mu);
+    for (int i = 0; i < g_scratch_count; ++i) {
+        if (g_scratch[i].ptr) {
+            int cur = 0;
+            cudaGetDevice(&cur);
+            cudaSetDevice(g_scratch[i].device);
+            cudaFree(g_scratch[i].ptr);
+            cudaSetDevice(cur);
+        }
+        g_scratch[i] = ScratchEntry{0, nullptr, nullptr, 0};
+    }
+    g_scratch_count = 0;
+    g_scratch_next_evict = 0;
+    cudaGetLastError();
     return DET_GEMM_OK;
 }
 

@@ -40,13 +40,14 @@ struct Params {
     CUtensorMap tmap_b;           // "B operand": contraction x output columns
     void *out;                    // row-major output, rows x cols
     long long ldo;                // output leading dimension, elements
+    void *scratch;                // deep-slot scratch: grid x VariantOps::scratch_cta_bytes
     int *status;                  // device status word (first int = code)
     unsigned long long timeout_ns;
     int rows, cols, kc, num_leaves;
     int m_tiles, n_tiles;
     int force_timeout;
-    int pad_;
-    uint16_t sched[kMaxLeaves];   // per-leaf merge schedule (see det_gemm_tree_schedule)
+    int num_blocks;
+    uint16_t blocks[kMaxLeaves];  // block schedule (see det_gemm_block_schedule)
 };
 
 struct VariantOps {
@@ -55,7 +56,11 @@ struct VariantOps {
     cudaError_t (*launch)(const Params &p, int grid, cudaStream_t stream);
     int bn;                       // output columns per tile
     int smem_bytes;
+    int scratch_cta_bytes;        // global scratch each CTA needs for its deep slots
 };
+
+// Largest scratch_cta_bytes over all variants (bf16: 3 slots x 32 KiB).
+constexpr int kMaxScratchCtaBytes = 3 * 256 * 128;
 
 VariantOps ops_bf16_kmn();
 VariantOps ops_bf16_kk();

@@ -31,12 +31,12 @@
 //
 // Pending partials ("slots"): slot s holds the finished left child of a tree
 // node of height s + 1, so at most ceil(log2 L) <= 10 are live, and slot s
-// is written at most once per 2^(s+1) leaves. Slot 0 and the running value
-// share two register arrays that swap roles (parking a leaf in slot 0 is a
-// relabelling, not a copy); slots 1-2 are registers; the next ones are TMEM
-// columns past the accumulators, then shared memory; slot 9 (more than 512
-// leaves) is parked in the thread's own output elements, where the root
-// will later be written.
+// is written at most once per 2^(s+1) leaves. The epilogue evaluates the
+// tree's maximal subtrees of at most four leaves ("blocks", height <= 2)
+// entirely in registers, so only slots 2 and up ever hold a value: the
+// next slots are TMEM columns past the accumulators, then shared memory,
+// and the last three (touched at most once per 256 leaves) a per-CTA
+// global-memory scratch line of 128 bytes per thread.
 //
 // Every mbarrier wait is bounded (Params::timeout_ns of %globaltimer). On
 // expiry the waiter records DET_GEMM_ERR_TIMEOUT in the status word and sets
@@ -57,7 +57,7 @@ template <bool F32>
 struct Cfg {
     static constexpr int BN = F32 ? 64 : 128;           // output columns per tile
     static constexpr int NACC = F32 ? 4 : 3;            // TMEM accumulator buffers
-    static constexpr int STAGES = F32 ? 6 : 3;          // shared-memory ring depth
+    static constexpr int STAGES = F32 ? 6 : 4;          // shared-memory ring depth
     static constexpr int A_STAGE = kBM * kBK * 2;       // bytes of one A stage
     static constexpr int B_STAGE = BN * kBK * 2;        // bytes of one B stage
     static constexpr int STAGE_TX = A_STAGE + B_STAGE;  // TMA bytes per stage
@@ -65,24 +65,27 @@ struct Cfg {
     static constexpr int WORDS = 32;                    // 32-bit words per slot per thread
     static constexpr int TMEM_COLS = 512;
     static constexpr int TMEM_SLOT_BASE = NACC * BN;    // after the accumulators
-    static constexpr int TMEM_FIRST = 3;                // slots 0-2 live in registers
+    static constexpr int TMEM_FIRST = 2;                // slots 0-1 never leave a block's registers
     static constexpr int TMEM_SLOTS = (TMEM_COLS - TMEM_SLOT_BASE) / 64;
     static constexpr int SMEM_FIRST = TMEM_FIRST + TMEM_SLOTS;
-    static constexpr int OUT_SLOT = kMaxSlots - 1;
-    static constexpr int SMEM_SLOTS = OUT_SLOT - SMEM_FIRST;
-    static constexpr int SMEM_SLOT_BYTES = kEpiWarps * 32 * WORDS * 4;
+    static constexpr int SMEM_SLOTS = F32 ? 2 : 3;
+    static constexpr int GLOBAL_FIRST = SMEM_FIRST + SMEM_SLOTS;
+    static constexpr int GLOBAL_SLOTS = kMaxSlots - GLOBAL_FIRST;
+    static constexpr int SLOT_BYTES = kEpiWarps * 32 * WORDS * 4;   // one slot for the whole CTA
+    static constexpr int SCRATCH_CTA_BYTES = GLOBAL_SLOTS * SLOT_BYTES;
 
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + STAGES * A_STAGE;
     static constexpr int OFF_SLOTS = OFF_B + STAGES * B_STAGE;
-    static constexpr int OFF_BAR = OFF_SLOTS + SMEM_SLOTS * SMEM_SLOT_BYTES;
+    static constexpr int OFF_BAR = OFF_SLOTS + SMEM_SLOTS * SLOT_BYTES;
     // barriers: full[STAGES], empty[STAGES], acc_full[NACC], acc_empty[NACC], never, drain
     static constexpr int NUM_BARS = 2 * STAGES + 2 * NACC + 2;
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
     static constexpr int BYTES = OFF_MISC + 16;
     static constexpr int SMEM_BYTES = BYTES + 1024;     // slack to align the base to 1024 B
 
-    static_assert(SMEM_SLOTS >= 0, "slot storage");
+    static_assert(GLOBAL_SLOTS >= 1, "slot storage");
+    static_assert(SCRATCH_CTA_BYTES <= kMaxScratchCtaBytes, "scratch");
     static_assert(SMEM_BYTES <= 232448, "shared memory");
     static_assert(A_STAGE % 1024 == 0 && B_STAGE % 1024 == 0, "swizzle atoms");
     static_assert(F32 ? (COLS == WORDS) : (COLS == 2 * WORDS), "packing");
@@ -340,30 +343,23 @@ __device__ __forceinline__ void merge_all(uint32_t (&v)[32], const uint32_t (&s)
 // What one epilogue thread needs to reach its storage.
 struct EpiCtx {
     uint32_t tmem_slot;   // TMEM address of this thread's first TMEM slot
-    uint32_t smem_slot;   // shared-memory address of this thread's first slot
+    uint32_t smem_slot;   // shared-memory address of this thread's line in the first shared slot
+    uint8_t *scratch;     // this thread's 128-byte line in the first global slot
     int lane;
     int row, col;         // first output element owned by this thread
 };
 
-// Shared-memory slot chunk c (16 bytes) of this thread: chunks are XOR-
-// swizzled by lane so that the warp's row-wise accesses spread over banks.
-__device__ __forceinline__ uint32_t smem_chunk(uint32_t base, int lane, int c)
+// 16-byte chunk k of a thread's 128-byte shared-memory line: chunks are
+// XOR-swizzled by lane so that a warp's row-wise accesses spread over banks.
+__device__ __forceinline__ uint32_t smem_chunk(uint32_t line, int lane, int k)
 {
-    return base + static_cast<uint32_t>((c ^ (lane & 7)) * 16);
+    return line + static_cast<uint32_t>((k ^ (lane & 7)) * 16);
 }
 
-// Byte b (0..127) of this thread's first shared-memory slot, in the
-// swizzled layout of smem_chunk.
-__device__ __forceinline__ uint32_t smem_byte(const EpiCtx &c, int b)
-{
-    return c.smem_slot + static_cast<uint32_t>((((b >> 4) ^ (c.lane & 7)) << 4) + (b & 15));
-}
-
-// Writes this thread's 32 words (64 BF16 or 32 FP32 columns) to the output,
-// clipped to the matrix: used for the root and to park the root's left
-// child. A row the matrix clips goes element by element through this
-// thread's first shared-memory slot, which is always free here (the root's
-// children are formed only after every lower slot has been merged away).
+// Writes this thread's 32 words (64 BF16 or 32 FP32 columns) of the root
+// to the output, clipped to the matrix. A row the matrix clips goes element
+// by element through the thread's scratch line, which is free once the
+// root is formed (every pending partial has been merged into it).
 template <bool F32>
 __device__ __forceinline__ void store_out(const uint32_t (&v)[32], const Params &p, const EpiCtx &c)
 {
@@ -372,111 +368,58 @@ __device__ __forceinline__ void store_out(const uint32_t (&v)[32], const Params 
     if (c.row >= p.rows) return;
     const int ncols = p.cols - c.col;
     if (ncols <= 0) return;
+    const bool full = ncols >= C::COLS;
     uint8_t *dst = static_cast<uint8_t *>(p.out) + (static_cast<long long>(c.row) * p.ldo + c.col) * ES;
-    if (ncols >= C::COLS) {
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-            asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(dst + 16 * k), "r"(v[4 * k]),
-                         "r"(v[4 * k + 1]), "r"(v[4 * k + 2]), "r"(v[4 * k + 3])
-                         : "memory");
-        return;
-    }
+    uint8_t *vec = full ? dst : c.scratch;
 #pragma unroll
     for (int k = 0; k < 8; ++k)
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(smem_chunk(c.smem_slot, c.lane, k)),
-                     "r"(v[4 * k]), "r"(v[4 * k + 1]), "r"(v[4 * k + 2]), "r"(v[4 * k + 3])
+        asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(vec + 16 * k), "r"(v[4 * k]),
+                     "r"(v[4 * k + 1]), "r"(v[4 * k + 2]), "r"(v[4 * k + 3])
                      : "memory");
+    if (full) return;
 #pragma unroll 1
     for (int j = 0; j < ncols; ++j) {
         if constexpr (F32) {
             uint32_t w;
-            asm volatile("ld.shared.b32 %0, [%1];" : "=r"(w) : "r"(smem_byte(c, 4 * j)) : "memory");
+            asm volatile("ld.global.b32 %0, [%1];" : "=r"(w) : "l"(c.scratch + 4 * j) : "memory");
             asm volatile("st.global.b32 [%0], %1;" ::"l"(dst + 4 * j), "r"(w) : "memory");
         } else {
             uint16_t w;
-            asm volatile("ld.shared.u16 %0, [%1];" : "=h"(w) : "r"(smem_byte(c, 2 * j)) : "memory");
+            asm volatile("ld.global.u16 %0, [%1];" : "=h"(w) : "l"(c.scratch + 2 * j) : "memory");
             asm volatile("st.global.u16 [%0], %1;" ::"l"(dst + 2 * j), "h"(w) : "memory");
         }
     }
 }
 
-// Reads back half H (words 16H .. 16H+15) of what store_out parked, with
-// the same clipping (words outside the matrix read as zero; they are never
-// written out).
-template <bool F32, int H>
-__device__ __forceinline__ void load_out_half(uint32_t (&v)[16], const Params &p, const EpiCtx &c)
-{
-    using C = Cfg<F32>;
-    constexpr int ES = F32 ? 4 : 2;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = 0;
-    if (c.row >= p.rows) return;
-    const int ncols = p.cols - c.col;
-    if (ncols <= 0) return;
-    const uint8_t *src =
-        static_cast<const uint8_t *>(p.out) + (static_cast<long long>(c.row) * p.ldo + c.col) * ES;
-    if (ncols >= C::COLS) {
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-            asm volatile("ld.global.v4.b32 {%0, %1, %2, %3}, [%4];"
-                         : "=r"(v[4 * k]), "=r"(v[4 * k + 1]), "=r"(v[4 * k + 2]), "=r"(v[4 * k + 3])
-                         : "l"(src + 64 * H + 16 * k)
-                         : "memory");
-        return;
-    }
-#pragma unroll
-    for (int k = 0; k < 4; ++k)
-        asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(smem_chunk(c.smem_slot, c.lane, 4 * H + k)),
-                     "r"(0u)
-                     : "memory");
-    const int j0 = H * (C::COLS / 2);
-    const int j1 = min(ncols, (H + 1) * (C::COLS / 2));
-#pragma unroll 1
-    for (int j = j0; j < j1; ++j) {
-        if constexpr (F32) {
-            uint32_t w;
-            asm volatile("ld.global.b32 %0, [%1];" : "=r"(w) : "l"(src + 4 * j) : "memory");
-            asm volatile("st.shared.b32 [%0], %1;" ::"r"(smem_byte(c, 4 * j)), "r"(w) : "memory");
-        } else {
-            uint16_t w;
-            asm volatile("ld.global.u16 %0, [%1];" : "=h"(w) : "l"(src + 2 * j) : "memory");
-            asm volatile("st.shared.u16 [%0], %1;" ::"r"(smem_byte(c, 2 * j)), "h"(w) : "memory");
-        }
-    }
-#pragma unroll
-    for (int k = 0; k < 4; ++k)
-        asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                     : "=r"(v[4 * k]), "=r"(v[4 * k + 1]), "=r"(v[4 * k + 2]), "=r"(v[4 * k + 3])
-                     : "r"(smem_chunk(c.smem_slot, c.lane, 4 * H + k))
-                     : "memory");
-}
-
-// Half H (words 16H .. 16H+15) of deep slot s (TMEM, shared memory or the
-// parked output) -> t. Deep slots are read in halves to keep the
-// epilogue's register peak low.
-template <bool F32, int H>
-__device__ __forceinline__ void load_slot_half(int s, uint32_t (&t)[16], const EpiCtx &c, const Params &p)
+// Slot s >= 2 (TMEM, shared memory or global scratch) -> t.
+template <bool F32>
+__device__ __forceinline__ void load_slot(int s, uint32_t (&t)[32], const EpiCtx &c)
 {
     using C = Cfg<F32>;
     if (s < C::SMEM_FIRST) {
-        tmem_ld16(c.tmem_slot + static_cast<uint32_t>((s - C::TMEM_FIRST) * 64 + 16 * H), t);
+        tmem_ld32(c.tmem_slot + static_cast<uint32_t>((s - C::TMEM_FIRST) * 64), t);
         tmem_wait_ld();
-        reg_fence16(t);
-    } else if (s < C::OUT_SLOT) {
-        const uint32_t base = c.smem_slot + static_cast<uint32_t>((s - C::SMEM_FIRST) * C::SMEM_SLOT_BYTES);
+        reg_fence(t);
+    } else if (s < C::GLOBAL_FIRST) {
+        const uint32_t line = c.smem_slot + static_cast<uint32_t>((s - C::SMEM_FIRST) * C::SLOT_BYTES);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
+        for (int k = 0; k < 8; ++k)
             asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
                          : "=r"(t[4 * k]), "=r"(t[4 * k + 1]), "=r"(t[4 * k + 2]), "=r"(t[4 * k + 3])
-                         : "r"(smem_chunk(base, c.lane, 4 * H + k))
+                         : "r"(smem_chunk(line, c.lane, k))
                          : "memory");
-        }
     } else {
-        load_out_half<F32, H>(t, p, c);
+        const uint8_t *src = c.scratch + (s - C::GLOBAL_FIRST) * C::SLOT_BYTES;
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            asm volatile("ld.global.v4.b32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(t[4 * k]), "=r"(t[4 * k + 1]), "=r"(t[4 * k + 2]), "=r"(t[4 * k + 3])
+                         : "l"(src + 16 * k)
+                         : "memory");
     }
 }
 
-// v -> deep slot s held in TMEM or shared memory.
+// v -> slot s >= 2 (TMEM, shared memory or global scratch).
 template <bool F32>
 __device__ __forceinline__ void store_slot(int s, const uint32_t (&v)[32], const EpiCtx &c)
 {
@@ -484,14 +427,20 @@ __device__ __forceinline__ void store_slot(int s, const uint32_t (&v)[32], const
     if (s < C::SMEM_FIRST) {
         tmem_st32(c.tmem_slot + static_cast<uint32_t>((s - C::TMEM_FIRST) * 64), v);
         tmem_wait_st();
-    } else {
-        const uint32_t base = c.smem_slot + static_cast<uint32_t>((s - C::SMEM_FIRST) * C::SMEM_SLOT_BYTES);
+    } else if (s < C::GLOBAL_FIRST) {
+        const uint32_t line = c.smem_slot + static_cast<uint32_t>((s - C::SMEM_FIRST) * C::SLOT_BYTES);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(smem_chunk(base, c.lane, k)),
+        for (int k = 0; k < 8; ++k)
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(smem_chunk(line, c.lane, k)),
                          "r"(v[4 * k]), "r"(v[4 * k + 1]), "r"(v[4 * k + 2]), "r"(v[4 * k + 3])
                          : "memory");
-        }
+    } else {
+        uint8_t *dst = c.scratch + (s - C::GLOBAL_FIRST) * C::SLOT_BYTES;
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(dst + 16 * k), "r"(v[4 * k]),
+                         "r"(v[4 * k + 1]), "r"(v[4 * k + 2]), "r"(v[4 * k + 3])
+                         : "memory");
     }
 }
 
@@ -678,13 +627,12 @@ __device__ __forceinline__ void mma_role(const Params &p, const Smem<F32> &S)
 // Epilogue warp: leaf rounding and the merge tree for one row and BN/2
 // columns of every tile.
 //
-// The tree is walked in units. In a mid-split tree every leaf's parent has
-// two or three leaves below it, so each leaf is either one of a sibling
-// pair, merged at once, or the single left child of a three-leaf node,
-// which is parked in slot 1 (height 2). In the per-leaf schedule a pair's
-// first leaf is the one parked in slot 0, and the second leaf's entry holds
-// the pair's merges and park. Pending partials: slots 1-2 in registers,
-// then TMEM, shared memory, and for slot 9 the thread's own output.
+// The tree is walked block by block (det_gemm_block_schedule): a block's
+// two to four leaves are rounded and merged in registers in straight-line
+// code, then the block's value is merged with the pending partials its
+// entry names and parked (one TMEM or scratch access) or written out as the
+// root. The code stays small so that the loop, rare branches included,
+// lives in the instruction cache.
 template <bool F32>
 __device__ __forceinline__ void epilogue_role(const Params &p, const Smem<F32> &S, int warp, int lane)
 {
@@ -696,116 +644,75 @@ __device__ __forceinline__ void epilogue_role(const Params &p, const Smem<F32> &
     EpiCtx c;
     c.tmem_slot = S.tmem + lane_bits + static_cast<uint32_t>(C::TMEM_SLOT_BASE + h * 32);
     c.smem_slot = S.sSlots + static_cast<uint32_t>(warp * 32 + lane) * 128u;
+    c.scratch = static_cast<uint8_t *>(p.scratch) + static_cast<long long>(blockIdx.x) * C::SCRATCH_CTA_BYTES +
+                (warp * 32 + lane) * 128;
     c.lane = lane;
     const int num_tiles = p.m_tiles * p.n_tiles;
-    const int L = p.num_leaves;
+    const int NB = p.num_blocks;
 
-    uint32_t X[32], Y[32], S1[32], S2[32], stg[64];
+    uint32_t A[32], B[32], Cc[32], stg[64];
     int acc = 0;                          // accumulator of the next leaf
     uint32_t acc_phase = 0;
-    auto release = [&](int a) {
-        // The MMA may now overwrite accumulator a with the leaf NACC ahead.
+    bool ok = true;
+    // Waits for the next leaf's accumulator, loads it, hands it back to the
+    // MMA (which may then fill it with the leaf NACC ahead) and rounds the
+    // leaf into dst.
+    auto take = [&](uint32_t(&dst)[32]) {
+        const bool got = wait_bounded(S.accf(acc), acc_phase, S.abort_flag, p.status, p.timeout_ns, true);
+        if (!__all_sync(0xFFFFFFFFu, got)) {
+            ok = false;
+            return;
+        }
+        tc_fence_after();
+        stage_load<F32>(acc0 + static_cast<uint32_t>(acc * C::BN), stg);
+        stage_wait<F32>(stg);
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(S.acce(a));
-    };
-    auto bump = [&]() {
+        if (lane == 0) mbar_arrive(S.acce(acc));
         if (++acc == C::NACC) {
             acc = 0;
             acc_phase ^= 1u;
         }
+        stage_convert<F32>(stg, dst);
     };
-    auto acc_addr = [&](int a) { return acc0 + static_cast<uint32_t>(a * C::BN); };
+    auto add = [](uint32_t(&left)[32], const uint32_t(&right)[32]) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) left[i] = merge<F32>(left[i], right[i]);
+    };
 
-    for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+    for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
         int mt, nt;
         tile_coords(t, p.m_tiles, p.n_tiles, mt, nt);
         c.row = mt * kBM + q * 32 + lane;
         c.col = nt * C::BN + h * C::COLS;
-        for (int l = 0; l < L;) {
-            const uint32_t e = p.sched[l];
-            if ((e >> 12) == 0) {
-                // ---- a sibling pair (l, l + 1); the MMA commits are
-                // cumulative, so the second leaf's barrier covers both.
-                const uint32_t e2 = p.sched[l + 1];
-                const int a0 = acc;
-                bump();
-                const int a1 = acc;
-                const uint32_t ph1 = acc_phase;
-                bump();
-                const bool got = wait_bounded(S.accf(a1), ph1, S.abort_flag, p.status, p.timeout_ns, true);
-                if (!__all_sync(0xFFFFFFFFu, got)) return;
-                tc_fence_after();
-                stage_load<F32>(acc_addr(a0), stg);
-                stage_wait<F32>(stg);
-                release(a0);
-                stage_convert<F32>(stg, X);
-                stage_load<F32>(acc_addr(a1), stg);
-                stage_wait<F32>(stg);
-                release(a1);
-                stage_convert<F32>(stg, Y);
-                const uint32_t mask = e2 & 0x3FEu;   // slots above 0 (bit 0 is the pair itself)
-                const int st = static_cast<int>(e2 >> 12);
-                if (mask == 0 && st == 1) {
-                    // the pair is a left child of height 2: park it
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) S1[i] = merge<F32>(X[i], Y[i]);
-                } else if (mask == 2u && st == 2) {
-                    // right child of height 2, whose parent is a left child
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) X[i] = merge<F32>(X[i], Y[i]);
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) S2[i] = merge<F32>(S1[i], X[i]);
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) X[i] = merge<F32>(X[i], Y[i]);
-                    if (mask & 2u) merge_all<F32>(X, S1);
-                    if (mask & 4u) merge_all<F32>(X, S2);
-                    if (mask >> C::TMEM_FIRST) {
-#pragma unroll 1
-                        for (int s = C::TMEM_FIRST; s < kMaxSlots; ++s) {
-                            if (!((mask >> s) & 1u)) continue;
-                            uint32_t tt[16];
-                            load_slot_half<F32, 0>(s, tt, c, p);
-#pragma unroll
-                            for (int i = 0; i < 16; ++i) X[i] = merge<F32>(tt[i], X[i]);
-                            load_slot_half<F32, 1>(s, tt, c, p);
-#pragma unroll
-                            for (int i = 0; i < 16; ++i) X[16 + i] = merge<F32>(tt[i], X[16 + i]);
-                        }
-                    }
-                    if (st == 1) {
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) S1[i] = X[i];
-                    } else if (st == 2) {
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) S2[i] = X[i];
-                    } else if (st == kSlotRoot || st == C::OUT_SLOT) {
-                        store_out<F32>(X, p, c);
-                    } else {
-                        store_slot<F32>(st, X, c);
-                    }
-                }
-                l += 2;
-            } else {
-                // ---- a single leaf: the left child of a three-leaf node
-                // (parked in slot 1), or the whole tree when L == 1.
-                const bool got = wait_bounded(S.accf(acc), acc_phase, S.abort_flag, p.status, p.timeout_ns, true);
-                if (!__all_sync(0xFFFFFFFFu, got)) return;
-                tc_fence_after();
-                const int a0 = acc;
-                bump();
-                stage_load<F32>(acc_addr(a0), stg);
-                stage_wait<F32>(stg);
-                release(a0);
-                if ((e >> 12) == kSlotRoot) {
-                    stage_convert<F32>(stg, X);
-                    store_out<F32>(X, p, c);
-                } else {
-                    stage_convert<F32>(stg, S1);
-                }
-                l += 1;
+        for (int b = 0; b < NB; ++b) {
+            const uint32_t e = p.blocks[b];
+            const int n = static_cast<int>((e >> 10) & 3u) + 1;   // leaves in the block
+            // n = 1: A = l0          n = 2: A = l0 + l1
+            // n = 3: A = l0 + (l1 + l2)     n = 4: A = (l0 + l1) + (l2 + l3)
+            take(A);
+            if (n >= 2) take(B);
+            if (n == 4) {
+                add(A, B);
+                take(B);
             }
+            if (n >= 3) {
+                take(Cc);
+                add(B, Cc);
+            }
+            if (!ok) return;
+            if (n >= 2) add(A, B);
+            // merge with the pending left siblings above the block, lowest first
+#pragma unroll 1
+            for (uint32_t m = (e & 0x3FFu) >> C::TMEM_FIRST, s = C::TMEM_FIRST; m != 0; m >>= 1, ++s) {
+                if (!(m & 1u)) continue;
+                load_slot<F32>(static_cast<int>(s), B, c);   // B is free once the block is merged
+#pragma unroll
+                for (int i = 0; i < 32; ++i) A[i] = merge<F32>(B[i], A[i]);
+            }
+            const int st = static_cast<int>(e >> 12);
+            if (st == kSlotRoot) store_out<F32>(A, p, c);
+            else store_slot<F32>(st, A, c);
         }
     }
 }
@@ -914,6 +821,7 @@ struct Launcher {
         o.launch = &launch;
         o.bn = Cfg<F32>::BN;
         o.smem_bytes = Cfg<F32>::SMEM_BYTES;
+        o.scratch_cta_bytes = Cfg<F32>::SCRATCH_CTA_BYTES;
         return o;
     }
 };

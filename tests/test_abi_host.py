@@ -150,3 +150,46 @@ def test_schedule_rejects_bad_counts(dg):
     assert L.det_gemm_tree_schedule(0, buf) == 1
     assert L.det_gemm_tree_schedule(1025, buf) == 1
     assert L.det_gemm_tree_schedule(4, None) == 1
+
+
+def block_shape(leaves):
+    """The mid-split tree of a block's leaves (nested tuples)."""
+    n = len(leaves)
+    if n == 1:
+        return leaves[0]
+    mid = n // 2
+    return (block_shape(leaves[:mid]), block_shape(leaves[mid:]))
+
+
+def replay_blocks(blocks, L):
+    """Run the block schedule on symbolic leaves the way the kernel does."""
+    slots = {}
+    root = None
+    nxt = 0
+    for e in blocks:
+        n = ((e >> 10) & 3) + 1
+        mask, store = e & 0x3FF, e >> 12
+        v = block_shape(list(range(nxt, nxt + n)))
+        nxt += n
+        assert mask & 3 == 0, "blocks never merge with slots 0-1"
+        for s in range(10):
+            if mask >> s & 1:
+                assert s in slots, ("read of an empty slot", s)
+                v = (slots.pop(s), v)
+        if store == 15:
+            assert root is None
+            root = v
+        else:
+            assert 2 <= store < 10 and store not in slots
+            slots[store] = v
+    assert nxt == L and not slots
+    return root
+
+
+def test_block_schedule_replays_the_mid_split_tree_for_every_leaf_count(dg):
+    for L in range(1, 1025):
+        blocks = dg.det_gemm_block_schedule(L)
+        sizes = [((e >> 10) & 3) + 1 for e in blocks]
+        if L > 4:
+            assert set(sizes) <= {2, 3, 4}, L
+        assert replay_blocks(blocks, L) == mid_split_tree(0, L), L
