@@ -159,6 +159,13 @@ const char *det_gemm_status_string(det_gemm_status status);
 int det_gemm_abi_version(void);
 
 /*
+ * The calling thread's record of the CUDA error behind its last
+ * DET_GEMM_ERR_LAUNCH (name and message), or "" if none was recorded.
+ * Static per-thread storage; never NULL.
+ */
+const char *det_gemm_last_error_detail(void);
+
+/*
  * Host-only helper, no GPU needed: the per-leaf merge schedule the kernels
  * apply for a contraction of `num_leaves` leaves (1..1024). out[l] describes
  * what follows leaf l in an in-order walk of the mid-split tree: bits 0..9

@@ -55,7 +55,12 @@ _GEMM_NAMES = (
 class DetGemmError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = int(status)
-        super().__init__("%s: %s" % (where, status_string(status)))
+        msg = "%s: %s" % (where, status_string(status))
+        if self.status == 5:
+            detail = lib().det_gemm_last_error_detail().decode()
+            if detail:
+                msg += " [" + detail + "]"
+        super().__init__(msg)
 
 
 def lib() -> ctypes.CDLL:
@@ -77,6 +82,8 @@ def lib() -> ctypes.CDLL:
         L.det_gemm_check.restype = ctypes.c_int
         L.det_gemm_status_string.argtypes = [ctypes.c_int]
         L.det_gemm_status_string.restype = ctypes.c_char_p
+        L.det_gemm_last_error_detail.argtypes = []
+        L.det_gemm_last_error_detail.restype = ctypes.c_char_p
         L.det_gemm_abi_version.argtypes = []
         L.det_gemm_abi_version.restype = ctypes.c_int
         L.det_gemm_tree_schedule.argtypes = [i64, p]

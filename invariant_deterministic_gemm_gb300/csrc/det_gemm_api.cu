@@ -9,6 +9,7 @@
 
 #include <cstdint>
 #include <cstdlib>
+#include <cstdio>
 #include <cstring>
 #include <mutex>
 
@@ -50,6 +51,15 @@ ScratchEntry g_scratch[kMaxScratch];
 int g_scratch_count = 0;
 int g_scratch_next_evict = 0;
 int g_force_timeout = 0;
+thread_local char g_detail[256] = "";
+
+// Records the CUDA error behind a DET_GEMM_ERR_LAUNCH / _CUDA status.
+det_gemm_status fail_cuda(det_gemm_status st, cudaError_t e, const char *where)
+{
+    std::snprintf(g_detail, sizeof g_detail, "%s: %s (%s)", where, cudaGetErrorName(e), cudaGetErrorString(e));
+    cudaGetLastError();
+    return st;
+}
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 VariantOps variant_ops(Variant v)
@@ -245,13 +255,15 @@ det_gemm_status prepare_variant(DeviceState *st, Variant v)
         st->prepared[v] = true;
         int regs = 0;
         VariantOps ops = variant_ops(v);
-        if (!ops.prepare || ops.prepare(&regs) != cudaSuccess) {
-            cudaGetLastError();
-            st->prepare_status[v] = DET_GEMM_ERR_LAUNCH;
-        } else if (regs * kThreads < kProdRegs * 128 + kEpiRegs * 256) {
-            // setmaxnreg redistributes the registers the CTA was launched
-            // with; a smaller launch allocation could never satisfy the
-            // epilogue's request.
+        cudaError_t e = ops.prepare ? ops.prepare(&regs) : cudaErrorInvalidDeviceFunction;
+        if (e != cudaSuccess) {
+            st->prepare_status[v] = fail_cuda(DET_GEMM_ERR_LAUNCH, e, "kernel attributes");
+        } else if (regs != kLaunchRegs) {
+            // setmaxnreg redistributes exactly the registers the CTA is
+            // launched with; any other launch allocation would make the
+            // epilogue's request unsatisfiable or waste registers.
+            std::snprintf(g_detail, sizeof g_detail, "kernel compiled for %d registers per thread, expected %d",
+                          regs, kLaunchRegs);
             st->prepare_status[v] = DET_GEMM_ERR_LAUNCH;
         }
     }
@@ -379,10 +391,8 @@ det_gemm_status run(Variant v, Mat a, bool a_kmajor, Mat b, bool b_kmajor, Mat o
     const int64_t tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
     if (tiles > (int64_t{1} << 31) - 1) return DET_GEMM_ERR_INVALID_ARG;
     const int grid = static_cast<int>(tiles < st->sm_count ? tiles : st->sm_count);
-    if (ops.launch(p, grid, stream) != cudaSuccess) {
-        cudaGetLastError();
-        return DET_GEMM_ERR_LAUNCH;
-    }
+    const cudaError_t le = ops.launch(p, grid, stream);
+    if (le != cudaSuccess) return fail_cuda(DET_GEMM_ERR_LAUNCH, le, "kernel launch");
     return DET_GEMM_OK;
 }
 
@@ -502,6 +512,8 @@ const char *det_gemm_status_string(det_gemm_status status)
 }
 
 int det_gemm_abi_version(void) { return DET_GEMM_ABI_VERSION; }
+
+const char *det_gemm_last_error_detail(void) { return g_detail; }
 
 det_gemm_status det_gemm_tree_schedule(int64_t num_leaves, uint16_t *out)
 {

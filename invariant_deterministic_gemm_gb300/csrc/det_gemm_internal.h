@@ -16,10 +16,13 @@ constexpr int kSlotRoot = 15;             // schedule "store" value for the root
 constexpr int kMaxSlots = 10;             // ceil(log2(kMaxLeaves)) pending partials
 constexpr int kBM = 128;                  // output rows per tile (one TMEM lane per row)
 constexpr int kBK = 64;                   // contraction elements per shared-memory stage (two leaves)
-constexpr int kThreads = 384;             // 8 epilogue warps + producer warpgroup
-constexpr int kEpiWarps = 8;
-constexpr int kEpiRegs = 224;             // registers per epilogue thread after setmaxnreg
-constexpr int kProdRegs = 56;             // registers per producer-warpgroup thread
+constexpr int kEpiWarps = 16;             // four per scheduler, one TMEM lane quadrant each
+constexpr int kProducerWarp = 16;         // TMA producer
+constexpr int kMmaWarp = 17;              // TMEM allocator and MMA issuer
+constexpr int kThreads = 32 * (kEpiWarps + 4);   // warps 18-19 complete the producer warpgroup
+constexpr int kLaunchRegs = 96;           // registers per thread at launch (65536 / 640, rounded down to 8)
+constexpr int kProdRegs = 40;             // producer warpgroup after setmaxnreg
+constexpr int kEpiRegs = 104;             // epilogue warpgroups after setmaxnreg
 
 // Operand major-ness as seen by the MMA: K-major = contraction contiguous.
 enum Major { kKMajor = 0, kMNMajor = 1 };
@@ -60,7 +63,7 @@ struct VariantOps {
 };
 
 // Largest scratch_cta_bytes over all variants (bf16: 3 slots x 32 KiB).
-constexpr int kMaxScratchCtaBytes = 3 * 256 * 128;
+constexpr int kMaxScratchCtaBytes = 3 * 32768;
 
 VariantOps ops_bf16_kmn();
 VariantOps ops_bf16_kk();

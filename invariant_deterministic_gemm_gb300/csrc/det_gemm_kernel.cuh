@@ -12,13 +12,14 @@
 // invariance bullet). One tile shape per variant, whatever M is: choosing a
 // kernel by problem shape is what breaks batch invariance (section "Why").
 //
-// CTA layout (384 threads, one CTA per SM, persistent over output tiles):
-//   warps 0-7  epilogue: warp w reads TMEM lanes 32*(w%4).. (rows) and the
-//              column half w/4 of the tile; each thread owns one row and
-//              BN/2 columns, and keeps the tree's pending partials for them.
-//   warp 8     TMA producer (one lane).
-//   warp 9     TMEM allocator and MMA issuer (one lane).
-//   warps 10-11 idle (they complete the producer warpgroup for setmaxnreg).
+// CTA layout (640 threads, one CTA per SM, persistent over output tiles):
+//   warps 0-15 epilogue: warp w reads TMEM lanes 32*(w%4).. (rows) and the
+//              column quarter w/4 of the tile; each thread owns one row and
+//              BN/4 columns, and keeps the tree's pending partials for them.
+//              Four epilogue warps per scheduler hide each other's waits.
+//   warp 16    TMA producer (one lane).
+//   warp 17    TMEM allocator and MMA issuer (one lane).
+//   warps 18-19 idle (they complete the producer warpgroup for setmaxnreg).
 //
 // Per tile: the producer streams 64-wide K stages (two leaves) of the A and B
 // operand tiles into a ring of swizzled shared-memory buffers. For leaf l the
@@ -26,7 +27,7 @@
 // one overwrites, so each leaf starts from zero) and commits to that
 // buffer's "full" barrier. The epilogue loads the leaf, frees the buffer at
 // once (so the MMA can run NACC-1 leaves ahead), rounds it (bf16 variant)
-// and merges it into its pending partials following the per-leaf schedule,
+// and merges it into its pending partials following the block schedule,
 // and writes the root after the last leaf.
 //
 // Pending partials ("slots"): slot s holds the finished left child of a tree
@@ -61,8 +62,8 @@ struct Cfg {
     static constexpr int A_STAGE = kBM * kBK * 2;       // bytes of one A stage
     static constexpr int B_STAGE = BN * kBK * 2;        // bytes of one B stage
     static constexpr int STAGE_TX = A_STAGE + B_STAGE;  // TMA bytes per stage
-    static constexpr int COLS = BN / 2;                 // output columns per epilogue thread
-    static constexpr int WORDS = 32;                    // 32-bit words per slot per thread
+    static constexpr int COLS = BN / 4;                 // output columns per epilogue thread
+    static constexpr int WORDS = F32 ? COLS : COLS / 2; // 32-bit words per value per thread (16)
     static constexpr int TMEM_COLS = 512;
     static constexpr int TMEM_SLOT_BASE = NACC * BN;    // after the accumulators
     static constexpr int TMEM_FIRST = 2;                // slots 0-1 never leave a block's registers
@@ -71,7 +72,8 @@ struct Cfg {
     static constexpr int SMEM_SLOTS = F32 ? 2 : 3;
     static constexpr int GLOBAL_FIRST = SMEM_FIRST + SMEM_SLOTS;
     static constexpr int GLOBAL_SLOTS = kMaxSlots - GLOBAL_FIRST;
-    static constexpr int SLOT_BYTES = kEpiWarps * 32 * WORDS * 4;   // one slot for the whole CTA
+    static constexpr int LINE = WORDS * 4;              // bytes of one value of one thread (64)
+    static constexpr int SLOT_BYTES = kEpiWarps * 32 * LINE;   // one slot for the whole CTA
     static constexpr int SCRATCH_CTA_BYTES = GLOBAL_SLOTS * SLOT_BYTES;
 
     static constexpr int OFF_A = 0;
@@ -88,7 +90,7 @@ struct Cfg {
     static_assert(SCRATCH_CTA_BYTES <= kMaxScratchCtaBytes, "scratch");
     static_assert(SMEM_BYTES <= 232448, "shared memory");
     static_assert(A_STAGE % 1024 == 0 && B_STAGE % 1024 == 0, "swizzle atoms");
-    static_assert(F32 ? (COLS == WORDS) : (COLS == 2 * WORDS), "packing");
+    static_assert(WORDS == 16, "epilogue values are 16 words per thread");
 };
 
 // ----------------------------------------------------------- PTX helpers
@@ -254,6 +256,16 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16])
         : "r"(taddr));
 }
 
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16])
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+}
+
 __device__ __forceinline__ void reg_fence16(uint32_t (&r)[16])
 {
     asm volatile(""
@@ -333,35 +345,33 @@ __device__ __forceinline__ void tile_coords(int t, int m_tiles, int n_tiles, int
 
 // ------------------------------------------------------------- epilogue
 
-template <bool F32>
-__device__ __forceinline__ void merge_all(uint32_t (&v)[32], const uint32_t (&s)[32])
-{
-#pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = merge<F32>(s[i], v[i]);
-}
+// Every epilogue value (a rounded leaf, a partial, the root) is 16 words per
+// thread: 32 BF16 columns packed in pairs, or 16 FP32 columns.
+using Val = uint32_t[16];
 
 // What one epilogue thread needs to reach its storage.
 struct EpiCtx {
     uint32_t tmem_slot;   // TMEM address of this thread's first TMEM slot
     uint32_t smem_slot;   // shared-memory address of this thread's line in the first shared slot
-    uint8_t *scratch;     // this thread's 128-byte line in the first global slot
+    uint8_t *scratch;     // this thread's 64-byte line in the first global slot
     int lane;
     int row, col;         // first output element owned by this thread
 };
 
-// 16-byte chunk k of a thread's 128-byte shared-memory line: chunks are
-// XOR-swizzled by lane so that a warp's row-wise accesses spread over banks.
+// 16-byte chunk k (0..3) of a thread's 64-byte shared-memory line. Lines of
+// consecutive lanes are 64 bytes apart; swizzling the chunk by lane/2 puts
+// the eight lanes of a quarter-warp access on eight distinct bank groups.
 __device__ __forceinline__ uint32_t smem_chunk(uint32_t line, int lane, int k)
 {
-    return line + static_cast<uint32_t>((k ^ (lane & 7)) * 16);
+    return line + static_cast<uint32_t>((k ^ ((lane >> 1) & 3)) * 16);
 }
 
-// Writes this thread's 32 words (64 BF16 or 32 FP32 columns) of the root
-// to the output, clipped to the matrix. A row the matrix clips goes element
-// by element through the thread's scratch line, which is free once the
-// root is formed (every pending partial has been merged into it).
+// Writes this thread's value of the root to the output, clipped to the
+// matrix. A row the matrix clips goes element by element through the
+// thread's scratch line, which is free once the root is formed (every
+// pending partial has been merged into it).
 template <bool F32>
-__device__ __forceinline__ void store_out(const uint32_t (&v)[32], const Params &p, const EpiCtx &c)
+__device__ __forceinline__ void store_out(const Val &v, const Params &p, const EpiCtx &c)
 {
     using C = Cfg<F32>;
     constexpr int ES = F32 ? 4 : 2;
@@ -372,7 +382,7 @@ __device__ __forceinline__ void store_out(const uint32_t (&v)[32], const Params 
     uint8_t *dst = static_cast<uint8_t *>(p.out) + (static_cast<long long>(c.row) * p.ldo + c.col) * ES;
     uint8_t *vec = full ? dst : c.scratch;
 #pragma unroll
-    for (int k = 0; k < 8; ++k)
+    for (int k = 0; k < 4; ++k)
         asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(vec + 16 * k), "r"(v[4 * k]),
                      "r"(v[4 * k + 1]), "r"(v[4 * k + 2]), "r"(v[4 * k + 3])
                      : "memory");
@@ -393,17 +403,17 @@ __device__ __forceinline__ void store_out(const uint32_t (&v)[32], const Params 
 
 // Slot s >= 2 (TMEM, shared memory or global scratch) -> t.
 template <bool F32>
-__device__ __forceinline__ void load_slot(int s, uint32_t (&t)[32], const EpiCtx &c)
+__device__ __forceinline__ void load_slot(int s, Val &t, const EpiCtx &c)
 {
     using C = Cfg<F32>;
     if (s < C::SMEM_FIRST) {
-        tmem_ld32(c.tmem_slot + static_cast<uint32_t>((s - C::TMEM_FIRST) * 64), t);
+        tmem_ld16(c.tmem_slot + static_cast<uint32_t>((s - C::TMEM_FIRST) * 64), t);
         tmem_wait_ld();
-        reg_fence(t);
+        reg_fence16(t);
     } else if (s < C::GLOBAL_FIRST) {
         const uint32_t line = c.smem_slot + static_cast<uint32_t>((s - C::SMEM_FIRST) * C::SLOT_BYTES);
 #pragma unroll
-        for (int k = 0; k < 8; ++k)
+        for (int k = 0; k < 4; ++k)
             asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
                          : "=r"(t[4 * k]), "=r"(t[4 * k + 1]), "=r"(t[4 * k + 2]), "=r"(t[4 * k + 3])
                          : "r"(smem_chunk(line, c.lane, k))
@@ -411,7 +421,7 @@ __device__ __forceinline__ void load_slot(int s, uint32_t (&t)[32], const EpiCtx
     } else {
         const uint8_t *src = c.scratch + (s - C::GLOBAL_FIRST) * C::SLOT_BYTES;
 #pragma unroll
-        for (int k = 0; k < 8; ++k)
+        for (int k = 0; k < 4; ++k)
             asm volatile("ld.global.v4.b32 {%0, %1, %2, %3}, [%4];"
                          : "=r"(t[4 * k]), "=r"(t[4 * k + 1]), "=r"(t[4 * k + 2]), "=r"(t[4 * k + 3])
                          : "l"(src + 16 * k)
@@ -421,65 +431,57 @@ __device__ __forceinline__ void load_slot(int s, uint32_t (&t)[32], const EpiCtx
 
 // v -> slot s >= 2 (TMEM, shared memory or global scratch).
 template <bool F32>
-__device__ __forceinline__ void store_slot(int s, const uint32_t (&v)[32], const EpiCtx &c)
+__device__ __forceinline__ void store_slot(int s, const Val &v, const EpiCtx &c)
 {
     using C = Cfg<F32>;
     if (s < C::SMEM_FIRST) {
-        tmem_st32(c.tmem_slot + static_cast<uint32_t>((s - C::TMEM_FIRST) * 64), v);
+        tmem_st16(c.tmem_slot + static_cast<uint32_t>((s - C::TMEM_FIRST) * 64), v);
         tmem_wait_st();
     } else if (s < C::GLOBAL_FIRST) {
         const uint32_t line = c.smem_slot + static_cast<uint32_t>((s - C::SMEM_FIRST) * C::SLOT_BYTES);
 #pragma unroll
-        for (int k = 0; k < 8; ++k)
+        for (int k = 0; k < 4; ++k)
             asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(smem_chunk(line, c.lane, k)),
                          "r"(v[4 * k]), "r"(v[4 * k + 1]), "r"(v[4 * k + 2]), "r"(v[4 * k + 3])
                          : "memory");
     } else {
         uint8_t *dst = c.scratch + (s - C::GLOBAL_FIRST) * C::SLOT_BYTES;
 #pragma unroll
-        for (int k = 0; k < 8; ++k)
+        for (int k = 0; k < 4; ++k)
             asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(dst + 16 * k), "r"(v[4 * k]),
                          "r"(v[4 * k + 1]), "r"(v[4 * k + 2]), "r"(v[4 * k + 3])
                          : "memory");
     }
 }
 
-// Issues the TMEM load of one accumulator (this thread's row, its BN/2
-// columns) into the staging registers; tcgen05.wait::ld completes it.
+// Loads this thread's BN/4 accumulator columns (32 FP32 for the bf16
+// variant, 16 for the fp32 one) into the staging registers and waits.
 template <bool F32>
-__device__ __forceinline__ void stage_load(uint32_t acc_taddr, uint32_t (&stg)[64])
+__device__ __forceinline__ void stage_load(uint32_t acc_taddr, uint32_t (&stg)[32])
 {
-    uint32_t(&lo)[32] = *reinterpret_cast<uint32_t(*)[32]>(&stg[0]);
-    tmem_ld32(acc_taddr, lo);
-    if constexpr (!F32) {
-        uint32_t(&hi)[32] = *reinterpret_cast<uint32_t(*)[32]>(&stg[32]);
-        tmem_ld32(acc_taddr + 32, hi);
-    }
-}
-
-template <bool F32>
-__device__ __forceinline__ void stage_wait(uint32_t (&stg)[64])
-{
-    uint32_t(&lo)[32] = *reinterpret_cast<uint32_t(*)[32]>(&stg[0]);
-    tmem_wait_ld();
-    reg_fence(lo);
-    if constexpr (!F32) {
-        uint32_t(&hi)[32] = *reinterpret_cast<uint32_t(*)[32]>(&stg[32]);
-        reg_fence(hi);
+    if constexpr (F32) {
+        uint32_t(&lo)[16] = *reinterpret_cast<uint32_t(*)[16]>(&stg[0]);
+        tmem_ld16(acc_taddr, lo);
+        tmem_wait_ld();
+        reg_fence16(lo);
+    } else {
+        tmem_ld32(acc_taddr, stg);
+        tmem_wait_ld();
+        reg_fence(stg);
     }
 }
 
 // The staged leaf -> F: rounded once to BF16 (RNE), two columns per word,
 // for the bf16 variant; as is for the fp32 variant.
 template <bool F32>
-__device__ __forceinline__ void stage_convert(const uint32_t (&stg)[64], uint32_t (&F)[32])
+__device__ __forceinline__ void stage_convert(const uint32_t (&stg)[32], Val &F)
 {
     if constexpr (F32) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) F[i] = stg[i];
+        for (int i = 0; i < 16; ++i) F[i] = stg[i];
     } else {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) F[i] = cvt_bf16x2(stg[2 * i], stg[2 * i + 1]);
+        for (int i = 0; i < 16; ++i) F[i] = cvt_bf16x2(stg[2 * i], stg[2 * i + 1]);
     }
 }
 
@@ -638,26 +640,27 @@ __device__ __forceinline__ void epilogue_role(const Params &p, const Smem<F32> &
 {
     using C = Cfg<F32>;
     const int q = warp & 3;               // TMEM lane quadrant (rows 32q .. 32q+31)
-    const int h = warp >> 2;              // column half of the tile
+    const int cq = warp >> 2;             // column quarter of the tile
     const uint32_t lane_bits = static_cast<uint32_t>(q * 32) << 16;
-    const uint32_t acc0 = S.tmem + lane_bits + static_cast<uint32_t>(h * C::COLS);
+    const uint32_t acc0 = S.tmem + lane_bits + static_cast<uint32_t>(cq * C::COLS);
     EpiCtx c;
-    c.tmem_slot = S.tmem + lane_bits + static_cast<uint32_t>(C::TMEM_SLOT_BASE + h * 32);
-    c.smem_slot = S.sSlots + static_cast<uint32_t>(warp * 32 + lane) * 128u;
+    c.tmem_slot = S.tmem + lane_bits + static_cast<uint32_t>(C::TMEM_SLOT_BASE + cq * 16);
+    c.smem_slot = S.sSlots + static_cast<uint32_t>((warp * 32 + lane) * C::LINE);
     c.scratch = static_cast<uint8_t *>(p.scratch) + static_cast<long long>(blockIdx.x) * C::SCRATCH_CTA_BYTES +
-                (warp * 32 + lane) * 128;
+                (warp * 32 + lane) * C::LINE;
     c.lane = lane;
     const int num_tiles = p.m_tiles * p.n_tiles;
     const int NB = p.num_blocks;
 
-    uint32_t A[32], B[32], Cc[32], stg[64];
+    Val A, B, Cc;
+    uint32_t stg[32];
     int acc = 0;                          // accumulator of the next leaf
     uint32_t acc_phase = 0;
     bool ok = true;
     // Waits for the next leaf's accumulator, loads it, hands it back to the
     // MMA (which may then fill it with the leaf NACC ahead) and rounds the
     // leaf into dst.
-    auto take = [&](uint32_t(&dst)[32]) {
+    auto take = [&](Val &dst) {
         const bool got = wait_bounded(S.accf(acc), acc_phase, S.abort_flag, p.status, p.timeout_ns, true);
         if (!__all_sync(0xFFFFFFFFu, got)) {
             ok = false;
@@ -665,7 +668,6 @@ __device__ __forceinline__ void epilogue_role(const Params &p, const Smem<F32> &
         }
         tc_fence_after();
         stage_load<F32>(acc0 + static_cast<uint32_t>(acc * C::BN), stg);
-        stage_wait<F32>(stg);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(S.acce(acc));
@@ -675,16 +677,16 @@ __device__ __forceinline__ void epilogue_role(const Params &p, const Smem<F32> &
         }
         stage_convert<F32>(stg, dst);
     };
-    auto add = [](uint32_t(&left)[32], const uint32_t(&right)[32]) {
+    auto add = [](Val &left, const Val &right) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) left[i] = merge<F32>(left[i], right[i]);
+        for (int i = 0; i < 16; ++i) left[i] = merge<F32>(left[i], right[i]);
     };
 
     for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
         int mt, nt;
         tile_coords(t, p.m_tiles, p.n_tiles, mt, nt);
         c.row = mt * kBM + q * 32 + lane;
-        c.col = nt * C::BN + h * C::COLS;
+        c.col = nt * C::BN + cq * C::COLS;
         for (int b = 0; b < NB; ++b) {
             const uint32_t e = p.blocks[b];
             const int n = static_cast<int>((e >> 10) & 3u) + 1;   // leaves in the block
@@ -708,7 +710,7 @@ __device__ __forceinline__ void epilogue_role(const Params &p, const Smem<F32> &
                 if (!(m & 1u)) continue;
                 load_slot<F32>(static_cast<int>(s), B, c);   // B is free once the block is merged
 #pragma unroll
-                for (int i = 0; i < 32; ++i) A[i] = merge<F32>(B[i], A[i]);
+                for (int i = 0; i < 16; ++i) A[i] = merge<F32>(B[i], A[i]);
             }
             const int st = static_cast<int>(e >> 12);
             if (st == kSlotRoot) store_out<F32>(A, p, c);
@@ -752,11 +754,11 @@ __global__ void __launch_bounds__(kThreads, 1) det_gemm_kernel(const __grid_cons
         mbar_init(S.drain(), 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (warp == 8 && lane == 0) {
+    if (warp == kProducerWarp && lane == 0) {
         tmap_prefetch(&p.tmap_a);
         tmap_prefetch(&p.tmap_b);
     }
-    if (warp == 9) {
+    if (warp == kMmaWarp) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                          smem_u32(tmem_base_smem)),
                      "r"(C::TMEM_COLS)
@@ -768,18 +770,19 @@ __global__ void __launch_bounds__(kThreads, 1) det_gemm_kernel(const __grid_cons
     tc_fence_after();
     S.tmem = *tmem_base_smem;
 
-    // Register split: the producer warpgroup gives up registers and the two
-    // epilogue warpgroups take them (kProdRegs*128 + kEpiRegs*256 equals the
-    // 168 x 384 registers the CTA is launched with). Each role's code sits
+    // Register split: the producer warpgroup gives up registers and the four
+    // epilogue warpgroups take them (kProdRegs*128 + kEpiRegs*512 fits in
+    // the kLaunchRegs*640 the CTA is launched with). Each role's code sits
     // inside its own branch so that the compiler allocates it under the
     // matching limit.
-    if (warp >= kEpiWarps) {
-        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kProdRegs));
-        if (warp == 8 && lane == 0) producer_role<A_MAJOR, B_MAJOR, F32>(p, S);
-        else if (warp == 9 && lane == 0) mma_role<A_MAJOR, B_MAJOR, F32>(p, S);
-    } else {
+    static_assert(kProdRegs * 128 + kEpiRegs * 32 * kEpiWarps <= kLaunchRegs * kThreads, "register split");
+    if (warp < kEpiWarps) {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kEpiRegs));
         epilogue_role<F32>(p, S, warp, lane);
+    } else {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kProdRegs));
+        if (warp == kProducerWarp && lane == 0) producer_role<A_MAJOR, B_MAJOR, F32>(p, S);
+        else if (warp == kMmaWarp && lane == 0) mma_role<A_MAJOR, B_MAJOR, F32>(p, S);
     }
 
     // ---- teardown
@@ -787,7 +790,7 @@ __global__ void __launch_bounds__(kThreads, 1) det_gemm_kernel(const __grid_cons
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 9) {
+    if (warp == kMmaWarp) {
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(S.tmem), "r"(C::TMEM_COLS)
                      : "memory");
     }
