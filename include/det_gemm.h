@@ -145,6 +145,35 @@ det_gemm_status det_gemm_db_transposed(const det_gemm_bf16 *A, const det_gemm_bf
                                        det_gemm_stream stream);
 
 /*
+ * det_gemm_fwd for callers that cannot allocate device memory. The pages
+ * describing det_gemm have no counterpart to this entry point.
+ *
+ * det_gemm_fwd allocates a scratch buffer with cudaMalloc on its first
+ * launch on a stream. Callers that are capturing a CUDA graph, that run on a
+ * memory arena they manage themselves, or that must never trigger an
+ * allocation's device-wide synchronisation cannot accept that. This entry
+ * point computes exactly the same product, bit for bit, with the scratch in
+ * a fixed 15 MiB array compiled into the library (every GPU that loads the
+ * library holds it until the process exits), and allocates nothing: no
+ * cudaMalloc, no cudaFree, no host allocation.
+ *
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) and initialises the library's state for that
+ *     device; make that first call before any stream capture.
+ *   - The array holds scratch for 160 CTAs (one per SM up to 160 SMs). A
+ *     launch that would need more is rejected with DET_GEMM_ERR_INVALID_ARG
+ *     before anything is enqueued (det_gemm_last_error_detail says why).
+ *   - Every call shares the array and nothing in it needs to start at zero
+ *     (each pending partial is written before it is read). Calls that
+ *     overlap on the GPU (different streams, or graphs replayed
+ *     concurrently) race on it: serialise them.
+ *   - Arguments, layouts and errors are those of det_gemm_fwd.
+ */
+det_gemm_status det_gemm_fwd_noalloc(const det_gemm_bf16 *A, const det_gemm_bf16 *B, det_gemm_bf16 *C,
+                                     int64_t M, int64_t N, int64_t K,
+                                     int64_t lda, int64_t ldb, int64_t ldc, det_gemm_stream stream);
+
+/*
  * Waits for `stream`, then reports and clears the device status word of the
  * current device: DET_GEMM_OK, DET_GEMM_ERR_TIMEOUT when a kernel gave up a
  * bounded wait since the last check, or DET_GEMM_ERR_CUDA when the stream

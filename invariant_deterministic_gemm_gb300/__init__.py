@@ -48,7 +48,7 @@ _lock = threading.Lock()
 _GEMM_NAMES = (
     "det_gemm_fwd", "det_gemm_fwd_rhs_transposed", "det_gemm_fwd_fp32",
     "det_gemm_fwd_fp32_rhs_transposed", "det_gemm_da", "det_gemm_db",
-    "det_gemm_db_transposed",
+    "det_gemm_db_transposed", "det_gemm_fwd_noalloc",
 )
 
 
@@ -159,6 +159,26 @@ def det_gemm_fwd(A: torch.Tensor, B: torch.Tensor, out: torch.Tensor | None = No
     c, ldc = _mat(C, "out")
     _call("det_gemm_fwd", a, b, c, M, N, K, lda, ldb, ldc, stream)
     return C
+
+
+def det_gemm_fwd_noalloc(A: torch.Tensor, B: torch.Tensor, out: torch.Tensor, stream=None):
+    """det_gemm_fwd without any allocation, for callers that cannot allocate
+    device memory (graph capture, caller-managed arenas): the output must be
+    given, and the library's scratch is a fixed array in its device image
+    (see det_gemm.h for its limit and for why overlapping calls race)."""
+    M, K = A.shape
+    K2, N = B.shape
+    if K2 != K:
+        raise ValueError("inner dimensions differ: %d vs %d" % (K, K2))
+    if out is None:
+        raise ValueError("det_gemm_fwd_noalloc needs a preallocated out")
+    a, lda = _mat(A, "A")
+    b, ldb = _mat(B, "B")
+    if tuple(out.shape) != (M, N):
+        raise ValueError("out must have shape %s, got %s" % ((M, N), tuple(out.shape)))
+    c, ldc = _mat(out, "out")
+    _call("det_gemm_fwd_noalloc", a, b, c, M, N, K, lda, ldb, ldc, stream)
+    return out
 
 
 def det_gemm_fwd_rhs_transposed(A: torch.Tensor, W: torch.Tensor, out=None, stream=None):
@@ -280,7 +300,7 @@ def det_gemm_debug_force_timeout(enable: bool) -> None:
 
 
 __all__ = [
-    "det_gemm_fwd", "det_gemm_fwd_rhs_transposed", "det_gemm_fwd_fp32",
+    "det_gemm_fwd", "det_gemm_fwd_noalloc", "det_gemm_fwd_rhs_transposed", "det_gemm_fwd_fp32",
     "det_gemm_fwd_fp32_rhs_transposed", "det_gemm_da", "det_gemm_db",
     "det_gemm_db_transposed", "det_gemm_check", "det_gemm_tree_schedule", "det_gemm_block_schedule",
     "det_gemm_debug_force_timeout", "det_gemm_shutdown", "DetGemmError", "lib", "status_string",

@@ -326,8 +326,10 @@ bool encode(CUtensorMap *m, const void *ptr, uint64_t inner, uint64_t outer, uin
 // Aop is `a` stored either K-major ([rows, kc] row-major) or MN-major
 // ([kc, rows] row-major); Bop is `b` stored K-major ([cols, kc]) or MN-major
 // ([kc, cols]).
+// fixed_scratch, when given, replaces the cached per-stream scratch: the
+// launch then allocates nothing at all (see det_gemm_fwd_noalloc).
 det_gemm_status run(Variant v, Mat a, bool a_kmajor, Mat b, bool b_kmajor, Mat out, int64_t rows, int64_t cols,
-                    int64_t kc, cudaStream_t stream)
+                    int64_t kc, cudaStream_t stream, void *fixed_scratch = nullptr, size_t fixed_bytes = 0)
 {
     if (rows < 0 || cols < 0 || kc < 0) return DET_GEMM_ERR_INVALID_ARG;
     if (rows > (int64_t{1} << 31) - 256 || cols > (int64_t{1} << 31) - 256) return DET_GEMM_ERR_INVALID_ARG;
@@ -353,8 +355,11 @@ det_gemm_status run(Variant v, Mat a, bool a_kmajor, Mat b, bool b_kmajor, Mat o
     VariantOps ops = variant_ops(v);
 
     const int64_t L = (kc + kLeaf - 1) / kLeaf;
-    const BlockSchedule *blocks = blocks_for(L);
-    if (!blocks) return DET_GEMM_ERR_LAUNCH;
+    const BlockSchedule *blocks = nullptr;
+    if (!fixed_scratch) {
+        blocks = blocks_for(L);
+        if (!blocks) return DET_GEMM_ERR_LAUNCH;
+    }
 
     Params p;
     std::memset(&p, 0, sizeof(p));
@@ -368,7 +373,9 @@ det_gemm_status run(Variant v, Mat a, bool a_kmajor, Mat b, bool b_kmajor, Mat o
     if (!ok) return DET_GEMM_ERR_LAUNCH;
     p.out = const_cast<void *>(out.ptr);
     p.ldo = out.ld;
-    {
+    if (fixed_scratch) {
+        p.scratch = fixed_scratch;
+    } else {
         int dev = 0;
         cudaGetDevice(&dev);
         // Sized for the largest variant and a grid of one CTA per SM, so
@@ -385,12 +392,25 @@ det_gemm_status run(Variant v, Mat a, bool a_kmajor, Mat b, bool b_kmajor, Mat o
     p.m_tiles = static_cast<int>((rows + kBM - 1) / kBM);
     p.n_tiles = static_cast<int>((cols + ops.bn - 1) / ops.bn);
     p.force_timeout = g_force_timeout;
-    p.num_blocks = static_cast<int>(blocks->count);
-    std::memcpy(p.blocks, blocks->entries, sizeof(uint16_t) * blocks->count);
+    if (blocks) {
+        p.num_blocks = static_cast<int>(blocks->count);
+        std::memcpy(p.blocks, blocks->entries, sizeof(uint16_t) * blocks->count);
+    } else {
+        int64_t nb = 0;
+        build_blocks(L, p.blocks, &nb);
+        p.num_blocks = static_cast<int>(nb);
+    }
 
     const int64_t tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
     if (tiles > (int64_t{1} << 31) - 1) return DET_GEMM_ERR_INVALID_ARG;
     const int grid = static_cast<int>(tiles < st->sm_count ? tiles : st->sm_count);
+    if (fixed_scratch && static_cast<size_t>(grid) * static_cast<size_t>(ops.scratch_cta_bytes) > fixed_bytes) {
+        std::snprintf(g_detail, sizeof g_detail,
+                      "this launch needs %zu bytes of scratch (%d CTAs x %d); the fixed scratch holds %zu",
+                      static_cast<size_t>(grid) * static_cast<size_t>(ops.scratch_cta_bytes), grid,
+                      ops.scratch_cta_bytes, fixed_bytes);
+        return DET_GEMM_ERR_INVALID_ARG;
+    }
     const cudaError_t le = ops.launch(p, grid, stream);
     if (le != cudaSuccess) return fail_cuda(DET_GEMM_ERR_LAUNCH, le, "kernel launch");
     return DET_GEMM_OK;
@@ -400,6 +420,25 @@ Mat bf16(const void *p, int64_t r, int64_t c, int64_t ld) { return Mat{p, r, c, 
 Mat f32(const void *p, int64_t r, int64_t c, int64_t ld) { return Mat{p, r, c, ld, 4}; }
 
 }  // namespace
+
+det_gemm_status fwd_with_fixed_scratch(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t K,
+                                       int64_t lda, int64_t ldb, int64_t ldc, cudaStream_t stream, void *scratch,
+                                       size_t scratch_bytes)
+{
+    if (M < 0 || N < 0 || K < 0) return DET_GEMM_ERR_INVALID_ARG;
+    return run(kBf16KMN, bf16(A, M, K, lda), true, bf16(B, K, N, ldb), false, bf16(C, M, N, ldc), M, N, K, stream,
+               scratch, scratch_bytes);
+}
+
+int fwd_with_fixed_scratch_status(const void *A, const void *B, void *C, long long M, long long N, long long K,
+                                  long long lda, long long ldb, long long ldc, cudaStream_t stream, void *scratch,
+                                  size_t scratch_bytes)
+{
+    return static_cast<int>(fwd_with_fixed_scratch(A, B, C, M, N, K, lda, ldb, ldc, stream, scratch, scratch_bytes));
+}
+
+void record_detail(const char *msg) { std::snprintf(g_detail, sizeof g_detail, "%s", msg); }
+
 }  // namespace detg
 
 using namespace detg;

@@ -71,4 +71,12 @@ VariantOps ops_bf16_mnmn();
 VariantOps ops_f32_kmn();
 VariantOps ops_f32_kk();
 
+// det_gemm_fwd with a caller-provided scratch buffer: nothing is allocated,
+// device or host. Returns a det_gemm_status.
+int fwd_with_fixed_scratch_status(const void *A, const void *B, void *C, long long M, long long N, long long K,
+                                  long long lda, long long ldb, long long ldc, cudaStream_t stream, void *scratch,
+                                  size_t scratch_bytes);
+// Stores a message for det_gemm_last_error_detail().
+void record_detail(const char *msg);
+
 }  // namespace detg
