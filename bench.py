@@ -480,6 +480,88 @@ def single_arm(args):
                       "tflops_best": round(flop / (best * 1e-3) / 1e12, 1)}))
 
 
+def configs_arm(args):
+    """Times every workload of the page on one GPU (not the headline line):
+    the QKV sweep over M, the LM head in BF16 and FP32 output, the long-K
+    product, and the tiny case. Prints one JSON object per workload with
+    TFLOP/s and the fraction of the roofline max(flops / peak, bytes / HBM)."""
+    import invariant_deterministic_gemm_gb300 as dg
+    dg.lib()
+    dev = torch.device("cuda", 0)
+    pk = peaks()
+
+    def timeit(fn, iters=10, flush=None):
+        fn()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(iters):
+            if flush is not None:
+                flush.zero_()
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record()
+            fn()
+            e.record()
+            torch.cuda.synchronize()
+            ts.append(s.elapsed_time(e))
+        st = dg.det_gemm_check()
+        if st != 0:
+            raise RuntimeError(dg.status_string(st))
+        return float(np.median(ts))
+
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)   # 256 MB > L2
+
+    def report(name, ms, flop, nbytes, torch_ms=None):
+        t_roof = max(flop / (pk["bf16_burst"] * 1e12), nbytes / (pk["hbm"] * 1e9))
+        out = {"workload": name, "ms": round(ms, 4), "tflops": round(flop / (ms * 1e-3) / 1e12, 1),
+               "roofline_frac": round(t_roof / (ms * 1e-3), 4),
+               "bound": "tensor" if flop / (pk["bf16_burst"] * 1e12) >= nbytes / (pk["hbm"] * 1e9) else "hbm",
+               "peaks": "%s burst bf16 %.0f TFLOP/s, HBM %.0f GB/s" % (pk["source"], pk["bf16_burst"], pk["hbm"])}
+        if torch_ms is not None:
+            out["torch_matmul_ms"] = round(torch_ms, 4)
+            out["determinism_tax"] = round(ms / torch_ms - 1.0, 3)
+        print(json.dumps(out), flush=True)
+
+    torch.backends.cuda.matmul.allow_tf32 = False
+    torch.backends.cuda.matmul.allow_bf16_reduced_precision_reduction = False
+
+    # QKV: one A, every row count
+    A = W.randn_bf16((4096, 4096), W.STD_ACT, W.seed_for(W.QKV, W.T_A)).to(dev)
+    B = W.randn_bf16((4096, 12288), W.STD_W, W.seed_for(W.QKV, W.T_B)).to(dev)
+    for M in (1, 3, 17, 256, 1024, 4096):
+        a = A[:M]
+        ms = timeit(lambda: dg.det_gemm_fwd(a, B), flush=flush)
+        tms = timeit(lambda: torch.matmul(a, B), flush=flush)
+        report("qkv M=%d [%d,4096]@[4096,12288]" % (M, M), ms, 2.0 * M * 4096 * 12288,
+               2 * (M * 4096 + 4096 * 12288 + M * 12288), tms)
+    del A, B
+    # LM head, weight stored [151936, 4096]
+    A = W.randn_bf16((2048, 4096), W.STD_ACT, W.seed_for(W.LMHEAD, W.T_A)).to(dev)
+    Wt = W.randn_bf16((151936, 4096), W.STD_W, W.seed_for(W.LMHEAD, W.T_B)).to(dev)
+    C = torch.empty((2048, 151936), dtype=torch.bfloat16, device=dev)
+    C32 = torch.empty((2048, 151936), dtype=torch.float32, device=dev)
+    flop = 2.0 * 2048 * 4096 * 151936
+    ins = 2 * (2048 * 4096 + 151936 * 4096)
+    ms = timeit(lambda: dg.det_gemm_fwd_rhs_transposed(A, Wt, out=C), iters=5)
+    tms = timeit(lambda: torch.matmul(A, Wt.t()), iters=5)
+    report("lm_head bf16 out [2048,4096]@[151936,4096]^T", ms, flop, ins + 2 * 2048 * 151936, tms)
+    ms = timeit(lambda: dg.det_gemm_fwd_fp32_rhs_transposed(A, Wt, out=C32), iters=5)
+    report("lm_head fp32 out [2048,4096]@[151936,4096]^T", ms, flop, ins + 4 * 2048 * 151936)
+    del A, Wt, C, C32
+    # long K
+    A = W.randn_bf16((4096, 32768), 1.0, W.seed_for(W.LONGK, W.T_A)).to(dev)
+    B = W.randn_bf16((32768, 4096), 1.0, W.seed_for(W.LONGK, W.T_B)).to(dev)
+    ms = timeit(lambda: dg.det_gemm_fwd(A, B), iters=5)
+    tms = timeit(lambda: torch.matmul(A, B), iters=5)
+    report("long_k [4096,32768]@[32768,4096]", ms, 2.0 * 4096 * 32768 * 4096,
+           2 * (2 * 4096 * 32768 + 4096 * 4096), tms)
+    del A, B
+    # tiny
+    A = W.randn_bf16((64, 256), 1.0, W.seed_for(W.TINY, W.T_A)).to(dev)
+    B = W.randn_bf16((256, 64), 1.0, W.seed_for(W.TINY, W.T_B)).to(dev)
+    ms = timeit(lambda: dg.det_gemm_fwd(A, B), iters=20)
+    report("tiny [64,256]@[256,64]", ms, 2.0 * 64 * 256 * 64, 2 * (64 * 256 + 256 * 64 + 64 * 64))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -492,7 +574,11 @@ def main():
                     help="profiling aid: run only this launch, at --rows token rows")
     ap.add_argument("--rows", type=int, default=2048)
     ap.add_argument("--iters", type=int, default=3)
+    ap.add_argument("--configs", action="store_true", help="time every workload of the page (not the headline line)")
     args = ap.parse_args()
+    if args.configs:
+        configs_arm(args)
+        return
     if args.single:
         single_arm(args)
         return
