@@ -172,6 +172,19 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, vola
     }
 }
 
+// One lane of the (converged) warp: the one that issues TMA copies, MMAs
+// and commits while the whole warp runs the role's control flow.
+__device__ __forceinline__ bool elect_one()
+{
+    uint32_t is_leader;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "elect.sync _|p, 0xffffffff;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(is_leader));
+    return is_leader != 0;
+}
+
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, uint32_t bar, int x,
                                             int y)
 {
@@ -500,11 +513,13 @@ struct Smem {
     __device__ uint32_t drain() const { return never() + 8u; }
 };
 
-// TMA producer (one lane): streams the A and B K-stages of every tile.
+// TMA producer warp: streams the A and B K-stages of every tile. The warp
+// runs the loop and the waits; one elected lane issues the copies.
 template <int A_MAJOR, int B_MAJOR, bool F32>
 __device__ __forceinline__ void producer_role(const Params &p, const Smem<F32> &S)
 {
     using C = Cfg<F32>;
+    const bool leader = elect_one();
     const int num_tiles = p.m_tiles * p.n_tiles;
     const int num_kstages = (p.num_leaves + 1) / 2;
     int stage = 0;
@@ -517,27 +532,32 @@ __device__ __forceinline__ void producer_role(const Params &p, const Smem<F32> &
         tile_coords(t, p.m_tiles, p.n_tiles, mt, nt);
         const int m0 = mt * kBM, n0 = nt * C::BN;
         for (int ks = 0; ks < num_kstages; ++ks) {
-            if (!wait_bounded(S.empty(stage), phase ^ 1u, S.abort_flag, p.status, p.timeout_ns, true)) {
+            const bool got = wait_bounded(S.empty(stage), phase ^ 1u, S.abort_flag, p.status, p.timeout_ns, true);
+            if (!__all_sync(0xFFFFFFFFu, got)) {
                 ok = false;
                 break;
             }
-            const uint32_t fb = S.full(stage);
-            mbar_arrive_expect_tx(fb, C::STAGE_TX);
-            const uint32_t a_dst = S.sA + stage * C::A_STAGE;
-            const uint32_t b_dst = S.sB + stage * C::B_STAGE;
-            const int k0 = ks * kBK;
-            if constexpr (A_MAJOR == kKMajor) {
-                tma_load_2d(a_dst, &p.tmap_a, fb, k0, m0);
-            } else {
-                tma_load_2d(a_dst, &p.tmap_a, fb, m0, k0);
-                tma_load_2d(a_dst + 8192, &p.tmap_a, fb, m0 + 64, k0);
-            }
-            if constexpr (B_MAJOR == kKMajor) {
-                tma_load_2d(b_dst, &p.tmap_b, fb, k0, n0);
-            } else {
+            if (leader) {
+                const uint32_t fb = S.full(stage);
+                mbar_arrive_expect_tx(fb, C::STAGE_TX);
+                const uint32_t a_dst = S.sA + stage * C::A_STAGE;
+                const uint32_t b_dst = S.sB + stage * C::B_STAGE;
+                const int k0 = ks * kBK;
+                if constexpr (A_MAJOR == kKMajor) {
+                    tma_load_2d(a_dst, &p.tmap_a, fb, k0, m0);
+                } else {
+                    tma_load_2d(a_dst, &p.tmap_a, fb, m0, k0);
+                    tma_load_2d(a_dst + 8192, &p.tmap_a, fb, m0 + 64, k0);
+                }
+                if constexpr (B_MAJOR == kKMajor) {
+                    tma_load_2d(b_dst, &p.tmap_b, fb, k0, n0);
+                } else {
 #pragma unroll
-                for (int b = 0; b < C::BN / 64; ++b) tma_load_2d(b_dst + 8192 * b, &p.tmap_b, fb, n0 + 64 * b, k0);
+                    for (int b = 0; b < C::BN / 64; ++b)
+                        tma_load_2d(b_dst + 8192 * b, &p.tmap_b, fb, n0 + 64 * b, k0);
+                }
             }
+            __syncwarp();
             issued |= 1u << stage;
             issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
             if (++stage == C::STAGES) {
@@ -555,7 +575,8 @@ __device__ __forceinline__ void producer_role(const Params &p, const Smem<F32> &
     }
 }
 
-// MMA issuer (one lane): two K=16 MMAs per leaf into a fresh accumulator.
+// MMA warp: two K=16 MMAs per leaf into a fresh accumulator. The warp runs
+// the loop and the waits; one elected lane issues the MMAs and commits.
 template <int A_MAJOR, int B_MAJOR, bool F32>
 __device__ __forceinline__ void mma_role(const Params &p, const Smem<F32> &S)
 {
@@ -570,6 +591,7 @@ __device__ __forceinline__ void mma_role(const Params &p, const Smem<F32> &S)
     constexpr uint32_t B_KSTEP = ((B_MAJOR == kKMajor) ? 32u : 2048u) >> 4;
     constexpr uint32_t A_LBO = (A_MAJOR == kKMajor) ? 16u : 8192u;
     constexpr uint32_t B_LBO = (B_MAJOR == kKMajor) ? 16u : 8192u;
+    const bool leader = elect_one();
     const uint64_t a_desc0 = sdesc(S.sA, A_LBO, 1024u);
     const uint64_t b_desc0 = sdesc(S.sB, B_LBO, 1024u);
     const int num_tiles = p.m_tiles * p.n_tiles;
@@ -582,11 +604,12 @@ __device__ __forceinline__ void mma_role(const Params &p, const Smem<F32> &S)
     bool issued_any = false;
     if (p.force_timeout) {
         // Test hook: a wait that nothing will end.
-        ok = wait_bounded(S.never(), 0, S.abort_flag, p.status, p.timeout_ns, true);
+        ok = __all_sync(0xFFFFFFFFu, wait_bounded(S.never(), 0, S.abort_flag, p.status, p.timeout_ns, true));
     }
     for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
         for (int l = 0; l < L; l += 2) {
-            if (!wait_bounded(S.full(stage), phase, S.abort_flag, p.status, p.timeout_ns, true)) {
+            const bool got = wait_bounded(S.full(stage), phase, S.abort_flag, p.status, p.timeout_ns, true);
+            if (!__all_sync(0xFFFFFFFFu, got)) {
                 ok = false;
                 break;
             }
@@ -596,23 +619,29 @@ __device__ __forceinline__ void mma_role(const Params &p, const Smem<F32> &S)
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
                 if (l + j >= L) break;
-                if (!wait_bounded(S.acce(acc), acc_phase ^ 1u, S.abort_flag, p.status, p.timeout_ns, true)) {
+                const bool free_acc =
+                    wait_bounded(S.acce(acc), acc_phase ^ 1u, S.abort_flag, p.status, p.timeout_ns, true);
+                if (!__all_sync(0xFFFFFFFFu, free_acc)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t d = S.tmem + static_cast<uint32_t>(acc * C::BN);
-                mma_bf16(d, a_st + (2 * j) * A_KSTEP, b_st + (2 * j) * B_KSTEP, IDESC, 0u);   // fresh leaf
-                mma_bf16(d, a_st + (2 * j + 1) * A_KSTEP, b_st + (2 * j + 1) * B_KSTEP, IDESC, 1u);
+                if (leader) {
+                    const uint32_t d = S.tmem + static_cast<uint32_t>(acc * C::BN);
+                    mma_bf16(d, a_st + (2 * j) * A_KSTEP, b_st + (2 * j) * B_KSTEP, IDESC, 0u);   // fresh leaf
+                    mma_bf16(d, a_st + (2 * j + 1) * A_KSTEP, b_st + (2 * j + 1) * B_KSTEP, IDESC, 1u);
+                    mma_commit(S.accf(acc));
+                }
+                __syncwarp();
                 issued_any = true;
-                mma_commit(S.accf(acc));
                 if (++acc == C::NACC) {
                     acc = 0;
                     acc_phase ^= 1u;
                 }
             }
             if (!ok) break;
-            mma_commit(S.empty(stage));
+            if (leader) mma_commit(S.empty(stage));
+            __syncwarp();
             if (++stage == C::STAGES) {
                 stage = 0;
                 phase ^= 1u;
@@ -621,7 +650,8 @@ __device__ __forceinline__ void mma_role(const Params &p, const Smem<F32> &S)
     }
     if (!ok && issued_any) {
         // Abandoned: wait for the MMAs in flight before TMEM is released.
-        mma_commit(S.drain());
+        if (leader) mma_commit(S.drain());
+        __syncwarp();
         wait_bounded(S.drain(), 0, S.abort_flag, p.status, p.timeout_ns, false);
     }
 }
@@ -781,8 +811,8 @@ __global__ void __launch_bounds__(kThreads, 1) det_gemm_kernel(const __grid_cons
         epilogue_role<F32>(p, S, warp, lane);
     } else {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kProdRegs));
-        if (warp == kProducerWarp && lane == 0) producer_role<A_MAJOR, B_MAJOR, F32>(p, S);
-        else if (warp == kMmaWarp && lane == 0) mma_role<A_MAJOR, B_MAJOR, F32>(p, S);
+        if (warp == kProducerWarp) producer_role<A_MAJOR, B_MAJOR, F32>(p, S);
+        else if (warp == kMmaWarp) mma_role<A_MAJOR, B_MAJOR, F32>(p, S);
     }
 
     // ---- teardown
