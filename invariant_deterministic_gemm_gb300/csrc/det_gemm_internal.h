@@ -17,11 +17,12 @@ constexpr int kMaxSlots = 10;             // ceil(log2(kMaxLeaves)) pending part
 constexpr int kBM = 128;                  // output rows per tile (one TMEM lane per row)
 constexpr int kBK = 64;                   // contraction elements per shared-memory stage (two leaves)
 constexpr int kEpiWarps = 16;             // four per scheduler, one TMEM lane quadrant each
-constexpr int kProducerWarp = 16;         // TMA producer
-constexpr int kMmaWarp = 17;              // TMEM allocator and MMA issuer
-constexpr int kThreads = 32 * (kEpiWarps + 4);   // warps 18-19 complete the producer warpgroup
+constexpr int kFirstStageWarp = 16;       // warps 16..19: TMA copies and MMAs of the K-stages
+constexpr int kStageWarps = 4;            // one per SM sub-partition
+constexpr int kTmemWarp = 17;             // allocates and frees TMEM
+constexpr int kThreads = 32 * (kEpiWarps + kStageWarps);
 constexpr int kLaunchRegs = 96;           // registers per thread at launch (65536 / 640, rounded down to 8)
-constexpr int kProdRegs = 40;             // producer warpgroup after setmaxnreg
+constexpr int kProdRegs = 40;             // stage warpgroup after setmaxnreg
 constexpr int kEpiRegs = 104;             // epilogue warpgroups after setmaxnreg
 
 // Operand major-ness as seen by the MMA: K-major = contraction contiguous.

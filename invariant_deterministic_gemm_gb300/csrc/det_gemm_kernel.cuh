@@ -52,13 +52,14 @@ namespace detg {
 
 constexpr int kStatusTimeout = 6;   // DET_GEMM_ERR_TIMEOUT
 
+
 // ------------------------------------------------------------------ config
 
 template <bool F32>
 struct Cfg {
     static constexpr int BN = F32 ? 64 : 128;           // output columns per tile
     static constexpr int NACC = F32 ? 4 : 3;            // TMEM accumulator buffers
-    static constexpr int STAGES = F32 ? 6 : 4;          // shared-memory ring depth
+    static constexpr int STAGES = kStageWarps;          // shared-memory ring depth: one slot per stage warp
     static constexpr int A_STAGE = kBM * kBK * 2;       // bytes of one A stage
     static constexpr int B_STAGE = BN * kBK * 2;        // bytes of one B stage
     static constexpr int STAGE_TX = A_STAGE + B_STAGE;  // TMA bytes per stage
@@ -80,8 +81,9 @@ struct Cfg {
     static constexpr int OFF_B = OFF_A + STAGES * A_STAGE;
     static constexpr int OFF_SLOTS = OFF_B + STAGES * B_STAGE;
     static constexpr int OFF_BAR = OFF_SLOTS + SMEM_SLOTS * SLOT_BYTES;
-    // barriers: full[STAGES], empty[STAGES], acc_full[NACC], acc_empty[NACC], never, drain
-    static constexpr int NUM_BARS = 2 * STAGES + 2 * NACC + 2;
+    // barriers: full[STAGES], empty[STAGES], acc_full[NACC], acc_empty[NACC], never,
+    // drain[kStageWarps], turn[kStageWarps]
+    static constexpr int NUM_BARS = 2 * STAGES + 2 * NACC + 1 + 2 * kStageWarps;
     static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
     static constexpr int BYTES = OFF_MISC + 16;
     static constexpr int SMEM_BYTES = BYTES + 1024;     // slack to align the base to 1024 B
@@ -129,6 +131,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Non-blocking test of the phase with the given parity.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
         : "r"(bar), "r"(parity)
@@ -510,77 +526,31 @@ struct Smem {
     __device__ uint32_t accf(int b) const { return bar0 + 8u * (2 * Cfg<F32>::STAGES + b); }
     __device__ uint32_t acce(int b) const { return bar0 + 8u * (2 * Cfg<F32>::STAGES + Cfg<F32>::NACC + b); }
     __device__ uint32_t never() const { return bar0 + 8u * (2 * Cfg<F32>::STAGES + 2 * Cfg<F32>::NACC); }
-    __device__ uint32_t drain() const { return never() + 8u; }
+    __device__ uint32_t drain(int j) const { return never() + 8u * (1 + j); }
+    __device__ uint32_t turn(int j) const { return never() + 8u * (1 + kStageWarps + j); }
 };
 
-// TMA producer warp: streams the A and B K-stages of every tile. The warp
-// runs the loop and the waits; one elected lane issues the copies.
+// Stage warps: kStageWarps warps, one per SM sub-partition. Warp j owns
+// ring slot j and the K-stages g with g % kStageWarps == j: it issues the
+// stage's TMA copies into its slot, waits for them, then issues the stage's
+// MMAs (two K=16 MMAs per leaf into a fresh accumulator) and the commits that
+// hand the accumulators to the epilogue and the slot back for the stage
+// kStageWarps later. Issuing an MMA holds up the sub-partition that issues
+// it until the tensor core accepts it; rotating the stages over the four
+// sub-partitions spreads that cost over the epilogue warps, which run on all
+// four, instead of slowing the quarter of them that share one.
+//
+// MMAs are still issued in leaf order: warp j issues stage g's MMAs only
+// after warp j-1 has issued stage g-1's (the turn barriers). The barrier
+// waits below test a phase's parity, so only one waiter may be pending per
+// barrier phase pair; the turn order guarantees that for the accumulator
+// barriers, and slot ownership for the ring barriers. The warp runs the loop
+// and the waits; one elected lane issues copies, MMAs and commits.
 template <int A_MAJOR, int B_MAJOR, bool F32>
-__device__ __forceinline__ void producer_role(const Params &p, const Smem<F32> &S)
+__device__ __forceinline__ void stage_role(const Params &p, const Smem<F32> &S, int j)
 {
     using C = Cfg<F32>;
-    const bool leader = elect_one();
-    const int num_tiles = p.m_tiles * p.n_tiles;
-    const int num_kstages = (p.num_leaves + 1) / 2;
-    int stage = 0;
-    uint32_t phase = 0;
-    uint32_t issued = 0;          // bit s: stage s has had a load issued
-    uint32_t issued_parity = 0;   // bit s: parity of that stage's last load
-    bool ok = true;
-    for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
-        int mt, nt;
-        tile_coords(t, p.m_tiles, p.n_tiles, mt, nt);
-        const int m0 = mt * kBM, n0 = nt * C::BN;
-        for (int ks = 0; ks < num_kstages; ++ks) {
-            const bool got = wait_bounded(S.empty(stage), phase ^ 1u, S.abort_flag, p.status, p.timeout_ns, true);
-            if (!__all_sync(0xFFFFFFFFu, got)) {
-                ok = false;
-                break;
-            }
-            if (leader) {
-                const uint32_t fb = S.full(stage);
-                mbar_arrive_expect_tx(fb, C::STAGE_TX);
-                const uint32_t a_dst = S.sA + stage * C::A_STAGE;
-                const uint32_t b_dst = S.sB + stage * C::B_STAGE;
-                const int k0 = ks * kBK;
-                if constexpr (A_MAJOR == kKMajor) {
-                    tma_load_2d(a_dst, &p.tmap_a, fb, k0, m0);
-                } else {
-                    tma_load_2d(a_dst, &p.tmap_a, fb, m0, k0);
-                    tma_load_2d(a_dst + 8192, &p.tmap_a, fb, m0 + 64, k0);
-                }
-                if constexpr (B_MAJOR == kKMajor) {
-                    tma_load_2d(b_dst, &p.tmap_b, fb, k0, n0);
-                } else {
-#pragma unroll
-                    for (int b = 0; b < C::BN / 64; ++b)
-                        tma_load_2d(b_dst + 8192 * b, &p.tmap_b, fb, n0 + 64 * b, k0);
-                }
-            }
-            __syncwarp();
-            issued |= 1u << stage;
-            issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
-            if (++stage == C::STAGES) {
-                stage = 0;
-                phase ^= 1u;
-            }
-        }
-    }
-    if (!ok) {
-        // Abandoned: let every load already issued land before the CTA and
-        // its shared memory go away.
-        for (int s = 0; s < C::STAGES; ++s)
-            if ((issued >> s) & 1u)
-                wait_bounded(S.full(s), (issued_parity >> s) & 1u, S.abort_flag, p.status, p.timeout_ns, false);
-    }
-}
-
-// MMA warp: two K=16 MMAs per leaf into a fresh accumulator. The warp runs
-// the loop and the waits; one elected lane issues the MMAs and commits.
-template <int A_MAJOR, int B_MAJOR, bool F32>
-__device__ __forceinline__ void mma_role(const Params &p, const Smem<F32> &S)
-{
-    using C = Cfg<F32>;
+    static_assert(C::STAGES == kStageWarps, "one ring slot per stage warp");
     constexpr uint32_t IDESC = idesc_bf16(kBM, C::BN, A_MAJOR, B_MAJOR);
     // Byte offset of K step k (16 contraction elements) inside a stage:
     // K-major rows hold the stage's 64 contraction elements (128 B), so a
@@ -592,67 +562,108 @@ __device__ __forceinline__ void mma_role(const Params &p, const Smem<F32> &S)
     constexpr uint32_t A_LBO = (A_MAJOR == kKMajor) ? 16u : 8192u;
     constexpr uint32_t B_LBO = (B_MAJOR == kKMajor) ? 16u : 8192u;
     const bool leader = elect_one();
-    const uint64_t a_desc0 = sdesc(S.sA, A_LBO, 1024u);
-    const uint64_t b_desc0 = sdesc(S.sB, B_LBO, 1024u);
+    const int s = j;                                  // this warp's ring slot
+    const uint32_t full = S.full(s), empty = S.empty(s);
+    const uint32_t my_turn = S.turn(j), next_turn = S.turn((j + 1) % kStageWarps);
+    const uint32_t a_dst = S.sA + s * C::A_STAGE;
+    const uint32_t b_dst = S.sB + s * C::B_STAGE;
+    const uint64_t a_st = sdesc(a_dst, A_LBO, 1024u);
+    const uint64_t b_st = sdesc(b_dst, B_LBO, 1024u);
     const int num_tiles = p.m_tiles * p.n_tiles;
     const int L = p.num_leaves;
-    int stage = 0;
-    uint32_t phase = 0;
-    int acc = 0;
-    uint32_t acc_phase = 0;
+    const int KS = (L + 1) / 2;                       // K-stages per tile
+    const int my_tiles = blockIdx.x < num_tiles ? (num_tiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+    const int total = my_tiles * KS;                  // K-stages of this CTA (< 2^31)
+    bool tma_pending = false;     // a load into the slot may be in flight
+    uint32_t tma_parity = 0;      // parity of the slot's last load
+    bool mma_issued = false;
     bool ok = true;
-    bool issued_any = false;
-    if (p.force_timeout) {
+    if (j == 0 && p.force_timeout) {
         // Test hook: a wait that nothing will end.
         ok = __all_sync(0xFFFFFFFFu, wait_bounded(S.never(), 0, S.abort_flag, p.status, p.timeout_ns, true));
     }
-    for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
-        for (int l = 0; l < L; l += 2) {
-            const bool got = wait_bounded(S.full(stage), phase, S.abort_flag, p.status, p.timeout_ns, true);
+    for (int g = j; ok && g < total; g += kStageWarps) {
+        const uint32_t round = static_cast<uint32_t>(g / kStageWarps) & 1u;
+        const int tl = g / KS;                        // tile of this CTA
+        const int ks = g - tl * KS;
+        int mt, nt;
+        tile_coords(blockIdx.x + tl * gridDim.x, p.m_tiles, p.n_tiles, mt, nt);
+        // ---- copy the stage into the slot once the MMAs of its last use are done
+        bool got = wait_bounded(empty, round ^ 1u, S.abort_flag, p.status, p.timeout_ns, true);
+        if (!__all_sync(0xFFFFFFFFu, got)) {
+            ok = false;
+            break;
+        }
+        if (leader) {
+            mbar_arrive_expect_tx(full, C::STAGE_TX);
+            const int k0 = ks * kBK, m0 = mt * kBM, n0 = nt * C::BN;
+            if constexpr (A_MAJOR == kKMajor) {
+                tma_load_2d(a_dst, &p.tmap_a, full, k0, m0);
+            } else {
+                tma_load_2d(a_dst, &p.tmap_a, full, m0, k0);
+                tma_load_2d(a_dst + 8192, &p.tmap_a, full, m0 + 64, k0);
+            }
+            if constexpr (B_MAJOR == kKMajor) {
+                tma_load_2d(b_dst, &p.tmap_b, full, k0, n0);
+            } else {
+#pragma unroll
+                for (int b = 0; b < C::BN / 64; ++b) tma_load_2d(b_dst + 8192 * b, &p.tmap_b, full, n0 + 64 * b, k0);
+            }
+        }
+        __syncwarp();
+        tma_pending = true;
+        tma_parity = round;
+        // ---- wait for the data and for this stage's turn to issue MMAs
+        got = wait_bounded(full, round, S.abort_flag, p.status, p.timeout_ns, true);
+        if (got && g > 0)
+            got = wait_bounded(my_turn, static_cast<uint32_t>((g - 1) / kStageWarps) & 1u, S.abort_flag, p.status,
+                               p.timeout_ns, true);
+        if (!__all_sync(0xFFFFFFFFu, got)) {
+            ok = false;
+            break;
+        }
+        tma_pending = false;
+        tc_fence_after();
+#pragma unroll
+        for (int jj = 0; jj < 2; ++jj) {
+            const int leaf = 2 * ks + jj;
+            if (leaf >= L) break;
+            // position of the leaf in this CTA's stream -> accumulator and use
+            const int G = tl * L + leaf;
+            const int use = G / C::NACC;
+            const int acc = G - use * C::NACC;
+            got = wait_bounded(S.acce(acc), (static_cast<uint32_t>(use) & 1u) ^ 1u, S.abort_flag, p.status,
+                               p.timeout_ns, true);
             if (!__all_sync(0xFFFFFFFFu, got)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            const uint64_t a_st = a_desc0 + static_cast<uint64_t>(stage * (C::A_STAGE >> 4));
-            const uint64_t b_st = b_desc0 + static_cast<uint64_t>(stage * (C::B_STAGE >> 4));
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                if (l + j >= L) break;
-                const bool free_acc =
-                    wait_bounded(S.acce(acc), acc_phase ^ 1u, S.abort_flag, p.status, p.timeout_ns, true);
-                if (!__all_sync(0xFFFFFFFFu, free_acc)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                if (leader) {
-                    const uint32_t d = S.tmem + static_cast<uint32_t>(acc * C::BN);
-                    mma_bf16(d, a_st + (2 * j) * A_KSTEP, b_st + (2 * j) * B_KSTEP, IDESC, 0u);   // fresh leaf
-                    mma_bf16(d, a_st + (2 * j + 1) * A_KSTEP, b_st + (2 * j + 1) * B_KSTEP, IDESC, 1u);
-                    mma_commit(S.accf(acc));
-                }
-                __syncwarp();
-                issued_any = true;
-                if (++acc == C::NACC) {
-                    acc = 0;
-                    acc_phase ^= 1u;
-                }
+            if (leader) {
+                const uint32_t d = S.tmem + static_cast<uint32_t>(acc * C::BN);
+                mma_bf16(d, a_st + (2 * jj) * A_KSTEP, b_st + (2 * jj) * B_KSTEP, IDESC, 0u);   // fresh leaf
+                mma_bf16(d, a_st + (2 * jj + 1) * A_KSTEP, b_st + (2 * jj + 1) * B_KSTEP, IDESC, 1u);
+                mma_commit(S.accf(acc));
             }
-            if (!ok) break;
-            if (leader) mma_commit(S.empty(stage));
             __syncwarp();
-            if (++stage == C::STAGES) {
-                stage = 0;
-                phase ^= 1u;
-            }
+            mma_issued = true;
         }
-    }
-    if (!ok && issued_any) {
-        // Abandoned: wait for the MMAs in flight before TMEM is released.
-        if (leader) mma_commit(S.drain());
+        if (!ok) break;
+        if (leader) {
+            mma_commit(empty);
+            mbar_arrive(next_turn);
+        }
         __syncwarp();
-        wait_bounded(S.drain(), 0, S.abort_flag, p.status, p.timeout_ns, false);
+    }
+    if (!ok) {
+        // Abandoned: let the load this warp issued land and its MMAs finish
+        // before the CTA's shared memory and TMEM go away.
+        if (tma_pending) wait_bounded(full, tma_parity, S.abort_flag, p.status, p.timeout_ns, false);
+        if (mma_issued) {
+            if (leader) mma_commit(S.drain(j));
+            __syncwarp();
+            wait_bounded(S.drain(j), 0, S.abort_flag, p.status, p.timeout_ns, false);
+        }
     }
 }
 
@@ -781,14 +792,17 @@ __global__ void __launch_bounds__(kThreads, 1) det_gemm_kernel(const __grid_cons
             mbar_init(S.acce(b), kEpiWarps);
         }
         mbar_init(S.never(), 1);
-        mbar_init(S.drain(), 1);
+        for (int j = 0; j < kStageWarps; ++j) {
+            mbar_init(S.drain(j), 1);
+            mbar_init(S.turn(j), 1);
+        }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (warp == kProducerWarp && lane == 0) {
+    if (warp == kFirstStageWarp && lane == 0) {
         tmap_prefetch(&p.tmap_a);
         tmap_prefetch(&p.tmap_b);
     }
-    if (warp == kMmaWarp) {
+    if (warp == kTmemWarp) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                          smem_u32(tmem_base_smem)),
                      "r"(C::TMEM_COLS)
@@ -800,7 +814,7 @@ __global__ void __launch_bounds__(kThreads, 1) det_gemm_kernel(const __grid_cons
     tc_fence_after();
     S.tmem = *tmem_base_smem;
 
-    // Register split: the producer warpgroup gives up registers and the four
+    // Register split: the stage warpgroup gives up registers and the four
     // epilogue warpgroups take them (kProdRegs*128 + kEpiRegs*512 fits in
     // the kLaunchRegs*640 the CTA is launched with). Each role's code sits
     // inside its own branch so that the compiler allocates it under the
@@ -811,8 +825,7 @@ __global__ void __launch_bounds__(kThreads, 1) det_gemm_kernel(const __grid_cons
         epilogue_role<F32>(p, S, warp, lane);
     } else {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kProdRegs));
-        if (warp == kProducerWarp) producer_role<A_MAJOR, B_MAJOR, F32>(p, S);
-        else if (warp == kMmaWarp) mma_role<A_MAJOR, B_MAJOR, F32>(p, S);
+        stage_role<A_MAJOR, B_MAJOR, F32>(p, S, warp - kFirstStageWarp);
     }
 
     // ---- teardown
@@ -820,7 +833,7 @@ __global__ void __launch_bounds__(kThreads, 1) det_gemm_kernel(const __grid_cons
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == kMmaWarp) {
+    if (warp == kTmemWarp) {
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(S.tmem), "r"(C::TMEM_COLS)
                      : "memory");
     }
