@@ -17,18 +17,20 @@
 //              column quarter w/4 of the tile; each thread owns one row and
 //              BN/4 columns, and keeps the tree's pending partials for them.
 //              Four epilogue warps per scheduler hide each other's waits.
-//   warp 16    TMA producer (one lane).
-//   warp 17    TMEM allocator and MMA issuer (one lane).
-//   warps 18-19 idle (they complete the producer warpgroup for setmaxnreg).
+//   warps 16-19 stage warps, one per scheduler: warp 16+j owns ring slot j
+//              and the K-stages g = j (mod 4) of the CTA's tile sequence. It
+//              copies the stage's A and B tiles in with TMA, then issues the
+//              stage's MMAs; MMA issue is handed from warp to warp in stage
+//              order (turn barriers). Warp 17 also allocates and frees TMEM.
 //
-// Per tile: the producer streams 64-wide K stages (two leaves) of the A and B
-// operand tiles into a ring of swizzled shared-memory buffers. For leaf l the
-// MMA lane issues two K=16 MMAs into accumulator buffer l % NACC (the first
-// one overwrites, so each leaf starts from zero) and commits to that
-// buffer's "full" barrier. The epilogue loads the leaf, frees the buffer at
-// once (so the MMA can run NACC-1 leaves ahead), rounds it (bf16 variant)
-// and merges it into its pending partials following the block schedule,
-// and writes the root after the last leaf.
+// Per tile: 64-wide K stages (two leaves) of the A and B operand tiles go
+// through a ring of four swizzled shared-memory slots. For leaf l the stage
+// warp issues two K=16 MMAs into accumulator buffer l % NACC (the first one
+// overwrites, so each leaf starts from zero) and commits to that buffer's
+// "full" barrier. The epilogue loads the leaf, frees the buffer at once (so
+// the MMAs can run NACC-1 leaves ahead), rounds it (bf16 variant) and merges
+// it into its pending partials following the block schedule, and writes the
+// root after the last leaf.
 //
 // Pending partials ("slots"): slot s holds the finished left child of a tree
 // node of height s + 1, so at most ceil(log2 L) <= 10 are live, and slot s
