@@ -49,6 +49,8 @@ struct Params {
     unsigned long long timeout_ns;
     int rows, cols, kc, num_leaves;
     int m_tiles, n_tiles;
+    int group;                    // tile order: tiles of this many row (or column) panels per group
+    int rows_fast;                // 1: row tiles vary fastest (A panels stay in L2), 0: column tiles
     int force_timeout;
     int num_blocks;
     uint16_t blocks[kMaxLeaves];  // block schedule (see det_gemm_block_schedule)

@@ -359,19 +359,26 @@ __device__ __forceinline__ uint32_t merge(uint32_t left, uint32_t right)
 
 // ------------------------------------------------------------- schedule
 
-// Tile t of the persistent walk -> (m tile, n tile). Tiles are grouped 8
-// m-tiles at a time so that CTAs running together share operand panels in
-// L2. Only timing depends on this order.
-__device__ __forceinline__ void tile_coords(int t, int m_tiles, int n_tiles, int &mt, int &nt)
+// Tile t of the persistent walk -> (m tile, n tile). Tiles come in groups
+// of `group` panels of the operand that stays in L2 (row panels of A when
+// rows_fast, column panels of B otherwise) times every panel of the other
+// operand; within a group the resident operand's panel varies fastest, so
+// the CTAs running at the same time share the streamed operand's panel and
+// each streamed panel is read from DRAM once per group. The host picks the
+// order; only timing depends on it.
+__device__ __forceinline__ void tile_coords(int t, const Params &p, int &mt, int &nt)
 {
-    constexpr int G = 8;
-    const int group = G * n_tiles;
-    const int g = t / group;
-    const int first = g * G;
-    const int gm = min(G, m_tiles - first);
-    const int r = t - g * group;
-    mt = first + r % gm;
-    nt = r / gm;
+    const int fast_tiles = p.rows_fast ? p.m_tiles : p.n_tiles;
+    const int slow_tiles = p.rows_fast ? p.n_tiles : p.m_tiles;
+    const int span = p.group * slow_tiles;
+    const int g = t / span;
+    const int first = g * p.group;
+    const int gf = min(p.group, fast_tiles - first);
+    const int r = t - g * span;
+    const int f = first + r % gf;
+    const int o = r / gf;
+    mt = p.rows_fast ? f : o;
+    nt = p.rows_fast ? o : f;
 }
 
 // ------------------------------------------------------------- epilogue
@@ -589,7 +596,7 @@ __device__ __forceinline__ void stage_role(const Params &p, const Smem<F32> &S, 
         const int tl = g / KS;                        // tile of this CTA
         const int ks = g - tl * KS;
         int mt, nt;
-        tile_coords(blockIdx.x + tl * gridDim.x, p.m_tiles, p.n_tiles, mt, nt);
+        tile_coords(blockIdx.x + tl * gridDim.x, p, mt, nt);
         // ---- copy the stage into the slot once the MMAs of its last use are done
         bool got = wait_bounded(empty, round ^ 1u, S.abort_flag, p.status, p.timeout_ns, true);
         if (!__all_sync(0xFFFFFFFFu, got)) {
@@ -727,7 +734,7 @@ __device__ __forceinline__ void epilogue_role(const Params &p, const Smem<F32> &
 
     for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
         int mt, nt;
-        tile_coords(t, p.m_tiles, p.n_tiles, mt, nt);
+        tile_coords(t, p, mt, nt);
         c.row = mt * kBM + q * 32 + lane;
         c.col = nt * C::BN + cq * C::COLS;
         for (int b = 0; b < NB; ++b) {
