@@ -65,6 +65,23 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(x: float, ws: int, device) -> float:
+    """The largest of every rank's x (the slowest replica's time): a plain
+    all-reduce on the replicas' process group; x itself when ws == 1."""
+    if ws == 1:
+        return float(x)
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(flop_per_rank_step: float, ws: int, ms_step: float) -> float:
+    """Whole-job throughput: every replica's work over the slowest replica's
+    time per step."""
+    return flop_per_rank_step * ws / (ms_step * 1e-3) / 1e12
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -250,14 +267,10 @@ def gpu_arm(args):
         raise RuntimeError("device status after the timed region: " + dg.status_string(st))
     per_launch_ms = np.array([[ev[k][i][0].elapsed_time(ev[k][i][1]) for i in range(n_l)]
                               for k in range(args.steps)])
-    if ws > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([ms_total], device=device)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms_total = float(tt.item())
+    ms_total = max_over_ranks(ms_total, ws, device)
     ms_step = ms_total / args.steps
     flop_step = FLOP_PER_GEMM * n_l
-    value = flop_step * ws / (ms_step * 1e-3) / 1e12
+    value = whole_job_tflops(flop_step, ws, ms_step)
 
     # ---- end to end: host buffers in, results back to host, every step
     pinned = {k: v.pin_memory() for k, v in host.items()}
@@ -290,12 +303,7 @@ def gpu_arm(args):
     e2.record()
     torch.cuda.synchronize()
     barrier()
-    e2e_ms = s2.elapsed_time(e2) / e2e_steps
-    if ws > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([e2e_ms], device=device)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
+    e2e_ms = max_over_ranks(s2.elapsed_time(e2) / e2e_steps, ws, device)
     st = dg.det_gemm_check()
     if st != 0:
         raise RuntimeError("device status after the e2e region: " + dg.status_string(st))
@@ -344,7 +352,7 @@ def gpu_arm(args):
                      "peak_source": "%s bf16_tflops_sustained (kernel timed inside a long step)" % pk["source"],
                      "flop_per_launch": FLOP_PER_GEMM, "traffic": traffic},
         "launches": launches,
-        "e2e": {"value": round(flop_step * ws / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+        "e2e": {"value": round(whole_job_tflops(flop_step, ws, e2e_ms), 2), "unit": "TFLOP/s",
                 "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "path": "Python binding -> C-ABI, pinned host inputs copied in and results copied out every step"},
         "gpu_launches": n_l * args.steps,
