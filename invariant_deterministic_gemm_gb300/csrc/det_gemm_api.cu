@@ -341,6 +341,26 @@ void choose_tile_order(Params &p, int bn)
     p.group = std::max(1, std::min(tiles, fit));
 }
 
+// Contraction parts per tile. A launch with few output tiles (skinny M)
+// leaves SMs idle while each tile walks all its leaves; splitting every
+// tile's leaves into 2, 4 or 8 equal contiguous ranges that are subtrees of
+// the merge tree gives that many work units per tile, and the tree's top
+// levels are applied afterwards (launch_merge_parts). The bits are the same
+// for every choice. The busiest CTA walks ceil(units / SMs) * leaves-per-unit
+// leaves; the fewest parts that cut that by a quarter or more are taken
+// (each range keeps at least 8 leaves), since every part costs a round trip
+// of partial results through memory and a merge launch.
+int choose_parts(int64_t tiles, int64_t L, int sms)
+{
+    auto busiest = [&](int parts) { return (tiles * parts + sms - 1) / sms * (L / parts); };
+    int best = 1;
+    for (int parts = 2; parts <= 8; parts *= 2) {
+        if (L % parts != 0 || L / parts < 8) break;
+        if (busiest(parts) * 5 <= busiest(best) * 4) best = parts;
+    }
+    return best;
+}
+
 // One GEMM: out[rows, cols] = sum over kc of Aop[row, k] * Bop[k, col].
 // Aop is `a` stored either K-major ([rows, kc] row-major) or MN-major
 // ([kc, rows] row-major); Bop is `b` stored K-major ([cols, kc]) or MN-major
@@ -374,17 +394,31 @@ det_gemm_status run(Variant v, Mat a, bool a_kmajor, Mat b, bool b_kmajor, Mat o
     VariantOps ops = variant_ops(v);
 
     const int64_t L = (kc + kLeaf - 1) / kLeaf;
+    const int64_t tiles = ((rows + kBM - 1) / kBM) * ((cols + ops.bn - 1) / ops.bn);
+    if (tiles > (int64_t{1} << 31) - 1) return DET_GEMM_ERR_INVALID_ARG;
+    // The allocation-free path never splits: the partial results need memory.
+    const int parts = fixed_scratch ? 1 : choose_parts(tiles, L, st->sm_count);
+    const int64_t Lp = L / parts;
     const BlockSchedule *blocks = nullptr;
     if (!fixed_scratch) {
-        blocks = blocks_for(L);
+        blocks = blocks_for(Lp);
         if (!blocks) return DET_GEMM_ERR_LAUNCH;
     }
 
     Params p;
     std::memset(&p, 0, sizeof(p));
     bool ok;
-    if (a_kmajor) ok = encode(&p.tmap_a, a.ptr, kc, rows, a.ld, 64, kBM);
+    // A K-major A operand with fewer rows than a tile is copied with a box of
+    // only its rows (rounded up to 8, at least 16): on GB300 a copy whose
+    // box is mostly outside the tensor, here 128 rows for fewer than 16,
+    // took the QKV launch from 35 to 57 us. The tile's other rows keep
+    // whatever the shared-memory slot holds; MMA row i reads only row i of
+    // A, and those rows are never stored.
+    const int a_box_rows = (a_kmajor && rows < kBM) ? static_cast<int>(std::max<int64_t>(16, (rows + 7) / 8 * 8))
+                                                    : kBM;
+    if (a_kmajor) ok = encode(&p.tmap_a, a.ptr, kc, rows, a.ld, 64, static_cast<uint32_t>(a_box_rows));
     else ok = encode(&p.tmap_a, a.ptr, rows, kc, a.ld, 64, 64);
+    p.stage_tx = a_box_rows * kBK * 2 + ops.bn * kBK * 2;
     if (ok) {
         if (b_kmajor) ok = encode(&p.tmap_b, b.ptr, kc, cols, b.ld, 64, ops.bn);
         else ok = encode(&p.tmap_b, b.ptr, cols, kc, b.ld, 64, 64);
@@ -392,22 +426,33 @@ det_gemm_status run(Variant v, Mat a, bool a_kmajor, Mat b, bool b_kmajor, Mat o
     if (!ok) return DET_GEMM_ERR_LAUNCH;
     p.out = const_cast<void *>(out.ptr);
     p.ldo = out.ld;
+    // A split launch's part slabs: rows x part_ld each, the row pitch a
+    // multiple of 8 elements (16 bytes).
+    const int64_t part_ld = (cols + 7) / 8 * 8;
+    const size_t part_bytes = parts > 1 ? static_cast<size_t>(parts) * rows * part_ld * out.esize : 0;
     if (fixed_scratch) {
         p.scratch = fixed_scratch;
     } else {
         int dev = 0;
         cudaGetDevice(&dev);
-        // Sized for the largest variant and a grid of one CTA per SM, so
-        // every launch on this stream can reuse it.
-        p.scratch = scratch_for(dev, stream, static_cast<size_t>(st->sm_count) * kMaxScratchCtaBytes);
-        if (!p.scratch) return DET_GEMM_ERR_LAUNCH;
+        // The deep-slot part is sized for the largest variant and a grid of
+        // one CTA per SM, so every launch on this stream can reuse it; the
+        // part slabs of a split launch follow it.
+        const size_t slot_bytes = static_cast<size_t>(st->sm_count) * kMaxScratchCtaBytes;
+        uint8_t *base = static_cast<uint8_t *>(scratch_for(dev, stream, slot_bytes + part_bytes));
+        if (!base) return DET_GEMM_ERR_LAUNCH;
+        p.scratch = base;
+        p.part_out = parts > 1 ? base + slot_bytes : nullptr;
     }
+    p.parts = parts;
+    p.part_ld = part_ld;
+    p.part_stride = rows * part_ld;
     p.status = st->status_ptr;
     p.timeout_ns = timeout_ns();
     p.rows = static_cast<int>(rows);
     p.cols = static_cast<int>(cols);
     p.kc = static_cast<int>(kc);
-    p.num_leaves = static_cast<int>(L);
+    p.num_leaves = static_cast<int>(Lp);
     p.m_tiles = static_cast<int>((rows + kBM - 1) / kBM);
     p.n_tiles = static_cast<int>((cols + ops.bn - 1) / ops.bn);
     choose_tile_order(p, ops.bn);
@@ -417,13 +462,13 @@ det_gemm_status run(Variant v, Mat a, bool a_kmajor, Mat b, bool b_kmajor, Mat o
         std::memcpy(p.blocks, blocks->entries, sizeof(uint16_t) * blocks->count);
     } else {
         int64_t nb = 0;
-        build_blocks(L, p.blocks, &nb);
+        build_blocks(Lp, p.blocks, &nb);
         p.num_blocks = static_cast<int>(nb);
     }
 
-    const int64_t tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
-    if (tiles > (int64_t{1} << 31) - 1) return DET_GEMM_ERR_INVALID_ARG;
-    const int grid = static_cast<int>(tiles < st->sm_count ? tiles : st->sm_count);
+    const int64_t units = tiles * parts;
+    if (units > (int64_t{1} << 31) - 1) return DET_GEMM_ERR_INVALID_ARG;
+    const int grid = static_cast<int>(units < st->sm_count ? units : st->sm_count);
     if (fixed_scratch && static_cast<size_t>(grid) * static_cast<size_t>(ops.scratch_cta_bytes) > fixed_bytes) {
         std::snprintf(g_detail, sizeof g_detail,
                       "this launch needs %zu bytes of scratch (%d CTAs x %d); the fixed scratch holds %zu",
@@ -433,6 +478,11 @@ det_gemm_status run(Variant v, Mat a, bool a_kmajor, Mat b, bool b_kmajor, Mat o
     }
     const cudaError_t le = ops.launch(p, grid, stream);
     if (le != cudaSuccess) return fail_cuda(DET_GEMM_ERR_LAUNCH, le, "kernel launch");
+    if (parts > 1) {
+        const cudaError_t me = launch_merge_parts(out.esize == 4, p.part_out, parts, p.rows, p.cols, part_ld,
+                                                  p.part_stride, const_cast<void *>(out.ptr), out.ld, stream);
+        if (me != cudaSuccess) return fail_cuda(DET_GEMM_ERR_LAUNCH, me, "merge launch");
+    }
     return DET_GEMM_OK;
 }
 

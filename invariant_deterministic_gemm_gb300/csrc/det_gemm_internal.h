@@ -47,7 +47,12 @@ struct Params {
     void *scratch;                // deep-slot scratch: grid x VariantOps::scratch_cta_bytes
     int *status;                  // device status word (first int = code)
     unsigned long long timeout_ns;
-    int rows, cols, kc, num_leaves;
+    int rows, cols, kc;
+    int stage_tx;                 // bytes one K-stage's TMA copies bring in (A box + B box)
+    int num_leaves;               // leaves per work unit (the whole contraction when parts == 1)
+    int parts;                    // contraction parts per tile: subtrees of the merge tree (1, 2, 4, 8)
+    void *part_out;               // parts > 1: part p of tile rows/cols goes to part_out + p * part_stride
+    long long part_ld, part_stride;   // elements
     int m_tiles, n_tiles;
     int group;                    // tile order: tiles of this many row (or column) panels per group
     int rows_fast;                // 1: row tiles vary fastest (A panels stay in L2), 0: column tiles
@@ -64,6 +69,12 @@ struct VariantOps {
     int smem_bytes;
     int scratch_cta_bytes;        // global scratch each CTA needs for its deep slots
 };
+
+// Merges the `parts` partial results of a split launch into the output with
+// the top levels of the merge tree (parts is a power of two; part p is leaf
+// range p of equal ranges, so the tree over them is the balanced one).
+cudaError_t launch_merge_parts(bool f32, const void *part, int parts, int rows, int cols, long long part_ld,
+                               long long part_stride, void *out, long long ldo, cudaStream_t stream);
 
 // Largest scratch_cta_bytes over all variants (bf16: 3 slots x 32 KiB).
 constexpr int kMaxScratchCtaBytes = 3 * 32768;

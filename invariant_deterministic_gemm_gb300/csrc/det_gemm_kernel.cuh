@@ -64,7 +64,7 @@ struct Cfg {
     static constexpr int STAGES = kStageWarps;          // shared-memory ring depth: one slot per stage warp
     static constexpr int A_STAGE = kBM * kBK * 2;       // bytes of one A stage
     static constexpr int B_STAGE = BN * kBK * 2;        // bytes of one B stage
-    static constexpr int STAGE_TX = A_STAGE + B_STAGE;  // TMA bytes per stage
+    static constexpr int STAGE_TX = A_STAGE + B_STAGE;  // TMA bytes per stage with a full A box
     static constexpr int COLS = BN / 4;                 // output columns per epilogue thread
     static constexpr int WORDS = F32 ? COLS : COLS / 2; // 32-bit words per value per thread (16)
     static constexpr int TMEM_COLS = 512;
@@ -394,6 +394,8 @@ struct EpiCtx {
     uint8_t *scratch;     // this thread's 64-byte line in the first global slot
     int lane;
     int row, col;         // first output element owned by this thread
+    uint8_t *out;         // matrix the roots go to (the output, or this unit's part slab)
+    long long ldo;        // its leading dimension, elements
 };
 
 // 16-byte chunk k (0..3) of a thread's 64-byte shared-memory line. Lines of
@@ -417,7 +419,7 @@ __device__ __forceinline__ void store_out(const Val &v, const Params &p, const E
     const int ncols = p.cols - c.col;
     if (ncols <= 0) return;
     const bool full = ncols >= C::COLS;
-    uint8_t *dst = static_cast<uint8_t *>(p.out) + (static_cast<long long>(c.row) * p.ldo + c.col) * ES;
+    uint8_t *dst = c.out + (static_cast<long long>(c.row) * c.ldo + c.col) * ES;
     uint8_t *vec = full ? dst : c.scratch;
 #pragma unroll
     for (int k = 0; k < 4; ++k)
@@ -578,11 +580,11 @@ __device__ __forceinline__ void stage_role(const Params &p, const Smem<F32> &S, 
     const uint32_t b_dst = S.sB + s * C::B_STAGE;
     const uint64_t a_st = sdesc(a_dst, A_LBO, 1024u);
     const uint64_t b_st = sdesc(b_dst, B_LBO, 1024u);
-    const int num_tiles = p.m_tiles * p.n_tiles;
-    const int L = p.num_leaves;
-    const int KS = (L + 1) / 2;                       // K-stages per tile
-    const int my_tiles = blockIdx.x < num_tiles ? (num_tiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
-    const int total = my_tiles * KS;                  // K-stages of this CTA (< 2^31)
+    const int units = p.m_tiles * p.n_tiles * p.parts;   // work units: (tile, contraction part)
+    const int L = p.num_leaves;                       // leaves per unit
+    const int KS = (L + 1) / 2;                       // K-stages per unit
+    const int my_units = blockIdx.x < units ? (units - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+    const int total = my_units * KS;                  // K-stages of this CTA (< 2^31)
     bool tma_pending = false;     // a load into the slot may be in flight
     uint32_t tma_parity = 0;      // parity of the slot's last load
     bool mma_issued = false;
@@ -593,10 +595,13 @@ __device__ __forceinline__ void stage_role(const Params &p, const Smem<F32> &S, 
     }
     for (int g = j; ok && g < total; g += kStageWarps) {
         const uint32_t round = static_cast<uint32_t>(g / kStageWarps) & 1u;
-        const int tl = g / KS;                        // tile of this CTA
+        const int tl = g / KS;                        // unit of this CTA
         const int ks = g - tl * KS;
+        const int u = blockIdx.x + tl * gridDim.x;
+        const int t = u / p.parts;
+        const int part = u - t * p.parts;
         int mt, nt;
-        tile_coords(blockIdx.x + tl * gridDim.x, p, mt, nt);
+        tile_coords(t, p, mt, nt);
         // ---- copy the stage into the slot once the MMAs of its last use are done
         bool got = wait_bounded(empty, round ^ 1u, S.abort_flag, p.status, p.timeout_ns, true);
         if (!__all_sync(0xFFFFFFFFu, got)) {
@@ -604,8 +609,8 @@ __device__ __forceinline__ void stage_role(const Params &p, const Smem<F32> &S, 
             break;
         }
         if (leader) {
-            mbar_arrive_expect_tx(full, C::STAGE_TX);
-            const int k0 = ks * kBK, m0 = mt * kBM, n0 = nt * C::BN;
+            mbar_arrive_expect_tx(full, static_cast<uint32_t>(p.stage_tx));
+            const int k0 = part * L * kLeaf + ks * kBK, m0 = mt * kBM, n0 = nt * C::BN;
             if constexpr (A_MAJOR == kKMajor) {
                 tma_load_2d(a_dst, &p.tmap_a, full, k0, m0);
             } else {
@@ -699,7 +704,7 @@ __device__ __forceinline__ void epilogue_role(const Params &p, const Smem<F32> &
     c.scratch = static_cast<uint8_t *>(p.scratch) + static_cast<long long>(blockIdx.x) * C::SCRATCH_CTA_BYTES +
                 (warp * 32 + lane) * C::LINE;
     c.lane = lane;
-    const int num_tiles = p.m_tiles * p.n_tiles;
+    const int units = p.m_tiles * p.n_tiles * p.parts;
     const int NB = p.num_blocks;
 
     Val A, B, Cc;
@@ -732,11 +737,20 @@ __device__ __forceinline__ void epilogue_role(const Params &p, const Smem<F32> &
         for (int i = 0; i < 16; ++i) left[i] = merge<F32>(left[i], right[i]);
     };
 
-    for (int t = blockIdx.x; ok && t < num_tiles; t += gridDim.x) {
+    for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
+        const int t = u / p.parts;
+        const int part = u - t * p.parts;
         int mt, nt;
         tile_coords(t, p, mt, nt);
         c.row = mt * kBM + q * 32 + lane;
         c.col = nt * C::BN + cq * C::COLS;
+        if (p.parts > 1) {
+            c.out = static_cast<uint8_t *>(p.part_out) + part * p.part_stride * (F32 ? 4 : 2);
+            c.ldo = p.part_ld;
+        } else {
+            c.out = static_cast<uint8_t *>(p.out);
+            c.ldo = p.ldo;
+        }
         for (int b = 0; b < NB; ++b) {
             const uint32_t e = p.blocks[b];
             const int n = static_cast<int>((e >> 10) & 3u) + 1;   // leaves in the block

@@ -1,0 +1,75 @@
+// The last step of a split launch: the top of the merge tree.
+//
+// A launch with few output tiles splits the contraction of every tile into
+// `parts` equal, contiguous leaf ranges, one work unit each. Each range is a
+// subtree of the fixed mid-split tree (RL-Kernel, "Batch-Invariant
+// Deterministic GEMM (det_gemm)", section "Ascend NPU backend": a contiguous
+// half-K GEMM is one child of the tree; the same holds level by level for
+// quarters and eighths when the leaf count divides evenly), so each unit
+// computes exactly the subtree the unsplit kernel would. This kernel merges
+// the units' roots with the tree's top levels, in the tree's order:
+// ((p0 + p1) + (p2 + p3)) for four parts, each add rounded once (BF16 adds
+// for the bf16 variant, FP32 adds for the fp32 one). The result is the same
+// bits as the unsplit launch; only the CTA doing the work differs.
+#include "det_gemm_kernel.cuh"
+
+namespace detg {
+namespace {
+
+constexpr int kMaxParts = 8;
+
+// One thread per (row, two columns) for BF16 output or (row, column) for FP32.
+template <bool F32>
+__global__ void merge_parts_kernel(const uint8_t *part, int parts, int rows, int cols, long long part_ld,
+                                   long long part_stride, uint8_t *out, long long ldo)
+{
+    constexpr int ES = F32 ? 4 : 2;
+    const int per_row = F32 ? cols : (cols + 1) / 2;
+    const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (idx >= static_cast<long long>(rows) * per_row) return;
+    const int r = static_cast<int>(idx / per_row);
+    const int j = static_cast<int>(idx - static_cast<long long>(r) * per_row);
+    const int col = F32 ? j : 2 * j;
+    // A part slab's row pitch is a multiple of 8 elements, so the word at an
+    // even column is aligned and exists even when col + 1 == cols.
+    uint32_t v[kMaxParts];
+#pragma unroll
+    for (int i = 0; i < kMaxParts; ++i) {
+        if (i < parts)
+            v[i] = *reinterpret_cast<const uint32_t *>(part + (i * part_stride + r * part_ld + col) * ES);
+    }
+    // balanced tree over the parts, left operand first at every node
+#pragma unroll
+    for (int w = 1; w < kMaxParts; w *= 2) {
+#pragma unroll
+        for (int i = 0; i + w < kMaxParts; i += 2 * w)
+            if (i + w < parts) v[i] = merge<F32>(v[i], v[i + w]);
+    }
+    uint8_t *dst = out + (static_cast<long long>(r) * ldo + col) * ES;
+    if (F32 || col + 1 < cols) *reinterpret_cast<uint32_t *>(dst) = v[0];
+    else *reinterpret_cast<uint16_t *>(dst) = static_cast<uint16_t>(v[0] & 0xFFFFu);
+}
+
+}  // namespace
+
+cudaError_t launch_merge_parts(bool f32, const void *part, int parts, int rows, int cols, long long part_ld,
+                               long long part_stride, void *out, long long ldo, cudaStream_t stream)
+{
+    if (parts < 2 || parts > kMaxParts || (parts & (parts - 1)) != 0) return cudaErrorInvalidValue;
+    const long long per_row = f32 ? cols : (cols + 1) / 2;
+    const long long n = static_cast<long long>(rows) * per_row;
+    const int threads = 256;
+    const long long blocks = (n + threads - 1) / threads;
+    if (blocks > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+    const uint8_t *src = static_cast<const uint8_t *>(part);
+    uint8_t *dst = static_cast<uint8_t *>(out);
+    if (f32)
+        merge_parts_kernel<true><<<static_cast<unsigned>(blocks), threads, 0, stream>>>(src, parts, rows, cols, part_ld,
+                                                                                        part_stride, dst, ldo);
+    else
+        merge_parts_kernel<false><<<static_cast<unsigned>(blocks), threads, 0, stream>>>(src, parts, rows, cols,
+                                                                                         part_ld, part_stride, dst, ldo);
+    return cudaGetLastError();
+}
+
+}  // namespace detg
