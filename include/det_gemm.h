@@ -145,6 +145,42 @@ det_gemm_status det_gemm_db_transposed(const det_gemm_bf16 *A, const det_gemm_bf
                                        det_gemm_stream stream);
 
 /*
+ * Merges partial products over contiguous contraction ranges into the full
+ * product: the deterministic composition of a contraction sharded over n
+ * GPUs or streams (RL-Kernel, "Batch-Invariant Deterministic GEMM
+ * (det_gemm)", section "Ascend NPU backend": a contiguous half-K GEMM is one
+ * child of the merge tree, so two half-K results merge to the full-K result
+ * bit for bit; tensor-parallel GEMM itself is outside det_gemm, section
+ * "Scope").
+ *
+ * parts[i] (i < n, n = 2, 4 or 8) is the det_gemm result [M,N] of the i-th
+ * of n equal contiguous leaf ranges of the contraction: with L = ceil(Kc/32)
+ * leaves and L divisible by n, part i covers contraction indices
+ * [i*Kc/n, (i+1)*Kc/n) when Kc is a multiple of 32*n (the last part may end
+ * in a partial leaf). Then every range is a subtree of the fixed mid-split
+ * tree and this call applies the tree's top log2(n) levels in their order,
+ * ((p0 + p1) + (p2 + p3)) for n = 4, each add rounded once to BF16 (RNE):
+ * C equals the full det_gemm bit for bit. With other ranges the result is
+ * still deterministic but is not that tree.
+ *
+ *   parts  host array of n device pointers, each [M,N] BF16, row pitch ldp
+ *          elements (the same for all parts)
+ *   C      device, [M,N] BF16, row pitch ldc; must not overlap any part
+ * Pointers and row pitches must be 16-byte aligned. Asynchronous on
+ * `stream`; nothing is allocated. Errors: DET_GEMM_ERR_INVALID_ARG (n not 2,
+ * 4 or 8, null pointer, negative size, ld < N, overlap),
+ * DET_GEMM_ERR_ALIGNMENT, DET_GEMM_ERR_UNSUPPORTED_DEVICE,
+ * DET_GEMM_ERR_LAUNCH.
+ */
+det_gemm_status det_gemm_merge(const det_gemm_bf16 *const *parts, int n, det_gemm_bf16 *C, int64_t M, int64_t N,
+                               int64_t ldp, int64_t ldc, det_gemm_stream stream);
+
+/* det_gemm_merge for FP32 partial products (det_gemm_fwd_fp32 and
+ * det_gemm_fwd_fp32_rhs_transposed): the same tree with FP32 adds (RNE). */
+det_gemm_status det_gemm_merge_fp32(const float *const *parts, int n, float *C, int64_t M, int64_t N, int64_t ldp,
+                                    int64_t ldc, det_gemm_stream stream);
+
+/*
  * det_gemm_fwd for callers that cannot allocate device memory. The pages
  * describing det_gemm have no counterpart to this entry point.
  *

@@ -78,6 +78,10 @@ def lib() -> ctypes.CDLL:
             fn = getattr(L, name)
             fn.argtypes = [p, p, p, i64, i64, i64, i64, i64, i64, p]
             fn.restype = ctypes.c_int
+        for name in ("det_gemm_merge", "det_gemm_merge_fp32"):
+            fn = getattr(L, name)
+            fn.argtypes = [p, ctypes.c_int, p, i64, i64, i64, i64, p]
+            fn.restype = ctypes.c_int
         L.det_gemm_check.argtypes = [p]
         L.det_gemm_check.restype = ctypes.c_int
         L.det_gemm_status_string.argtypes = [ctypes.c_int]
@@ -265,6 +269,37 @@ def det_gemm_db_transposed(A: torch.Tensor, dC: torch.Tensor, out=None, stream=N
     return dBt
 
 
+def _merge(name, parts, out, dtype, stream):
+    if not isinstance(parts, (list, tuple)) or len(parts) not in (2, 4, 8):
+        raise ValueError("parts must be a list of 2, 4 or 8 tensors")
+    mats = [_mat(t, "parts[%d]" % i, dtype) for i, t in enumerate(parts)]
+    shape = tuple(parts[0].shape)
+    if any(tuple(t.shape) != shape for t in parts):
+        raise ValueError("parts must all have the same shape")
+    lds = {ld for _, ld in mats}
+    if len(lds) != 1:
+        raise ValueError("parts must share one row pitch")
+    M, N = shape
+    C = _out(out, M, N, dtype, parts[0])
+    c_ptr, ldc = _mat(C, "out", dtype)
+    arr = (ctypes.c_void_p * len(parts))(*[ptr for ptr, _ in mats])
+    st = getattr(lib(), name)(arr, len(parts), c_ptr, M, N, lds.pop(), ldc, _stream_handle(stream))
+    if st != 0:
+        raise DetGemmError(st, name)
+    return C
+
+
+def det_gemm_merge(parts, out=None, stream=None):
+    """The full-contraction det_gemm product from n = 2, 4 or 8 partial
+    products over equal contiguous leaf ranges (the merge tree's top levels)."""
+    return _merge("det_gemm_merge", parts, out, torch.bfloat16, stream)
+
+
+def det_gemm_merge_fp32(parts, out=None, stream=None):
+    """det_gemm_merge for FP32 partial products (FP32 adds)."""
+    return _merge("det_gemm_merge_fp32", parts, out, torch.float32, stream)
+
+
 def det_gemm_check(stream=None) -> int:
     """Synchronise the stream and return (and clear) the device status code."""
     return int(lib().det_gemm_check(_stream_handle(stream)))
@@ -304,4 +339,6 @@ __all__ = [
     "det_gemm_fwd_fp32_rhs_transposed", "det_gemm_da", "det_gemm_db",
     "det_gemm_db_transposed", "det_gemm_check", "det_gemm_tree_schedule", "det_gemm_block_schedule",
     "det_gemm_debug_force_timeout", "det_gemm_shutdown", "DetGemmError", "lib", "status_string",
+    "det_gemm_merge",
+    "det_gemm_merge_fp32",
 ]

@@ -489,6 +489,31 @@ det_gemm_status run(Variant v, Mat a, bool a_kmajor, Mat b, bool b_kmajor, Mat o
 Mat bf16(const void *p, int64_t r, int64_t c, int64_t ld) { return Mat{p, r, c, ld, 2}; }
 Mat f32(const void *p, int64_t r, int64_t c, int64_t ld) { return Mat{p, r, c, ld, 4}; }
 
+// det_gemm_merge / det_gemm_merge_fp32: argument checks, then the merge of
+// n parts in the tree's top-level order.
+det_gemm_status merge_parts(const void *const *parts, int n, void *C, int64_t M, int64_t N, int64_t ldp,
+                            int64_t ldc, int esize, cudaStream_t stream)
+{
+    if (n != 2 && n != 4 && n != 8) return DET_GEMM_ERR_INVALID_ARG;
+    if (M < 0 || N < 0 || parts == nullptr) return DET_GEMM_ERR_INVALID_ARG;
+    if (M > (int64_t{1} << 31) - 256 || N > (int64_t{1} << 31) - 256) return DET_GEMM_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return DET_GEMM_OK;
+    const Mat out{C, M, N, ldc, esize};
+    det_gemm_status s = check_mat(out);
+    if (s != DET_GEMM_OK) return s;
+    for (int i = 0; i < n; ++i) {
+        const Mat part{parts[i], M, N, ldp, esize};
+        if ((s = check_mat(part)) != DET_GEMM_OK) return s;
+        if (overlaps(out, part)) return DET_GEMM_ERR_INVALID_ARG;
+    }
+    DeviceState *st = nullptr;
+    if ((s = device_state(&st)) != DET_GEMM_OK) return s;
+    const cudaError_t e = launch_merge_list(esize == 4, parts, n, static_cast<int>(M), static_cast<int>(N), ldp, C,
+                                            ldc, stream);
+    if (e != cudaSuccess) return fail_cuda(DET_GEMM_ERR_LAUNCH, e, "merge launch");
+    return DET_GEMM_OK;
+}
+
 }  // namespace
 
 det_gemm_status fwd_with_fixed_scratch(const void *A, const void *B, void *C, int64_t M, int64_t N, int64_t K,
@@ -579,6 +604,20 @@ det_gemm_status det_gemm_db_transposed(const det_gemm_bf16 *A, const det_gemm_bf
     if (M < 0 || N < 0 || K < 0) return DET_GEMM_ERR_INVALID_ARG;
     return run(kBf16MNMN, bf16(dC, M, N, lddc), false, bf16(A, M, K, lda), false, bf16(dBt, N, K, lddbt), N, K, M,
                reinterpret_cast<cudaStream_t>(stream));
+}
+
+det_gemm_status det_gemm_merge(const det_gemm_bf16 *const *parts, int n, det_gemm_bf16 *C, int64_t M, int64_t N,
+                               int64_t ldp, int64_t ldc, det_gemm_stream stream)
+{
+    return merge_parts(reinterpret_cast<const void *const *>(parts), n, C, M, N, ldp, ldc, 2,
+                       reinterpret_cast<cudaStream_t>(stream));
+}
+
+det_gemm_status det_gemm_merge_fp32(const float *const *parts, int n, float *C, int64_t M, int64_t N, int64_t ldp,
+                                    int64_t ldc, det_gemm_stream stream)
+{
+    return merge_parts(reinterpret_cast<const void *const *>(parts), n, C, M, N, ldp, ldc, 4,
+                       reinterpret_cast<cudaStream_t>(stream));
 }
 
 det_gemm_status det_gemm_check(det_gemm_stream stream)

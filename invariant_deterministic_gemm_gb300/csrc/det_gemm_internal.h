@@ -76,6 +76,10 @@ struct VariantOps {
 cudaError_t launch_merge_parts(bool f32, const void *part, int parts, int rows, int cols, long long part_ld,
                                long long part_stride, void *out, long long ldo, cudaStream_t stream);
 
+// The same merge over n separately allocated parts (det_gemm_merge).
+cudaError_t launch_merge_list(bool f32, const void *const *parts, int n, int rows, int cols, long long ldp, void *out,
+                              long long ldo, cudaStream_t stream);
+
 // Largest scratch_cta_bytes over all variants (bf16: 3 slots x 32 KiB).
 constexpr int kMaxScratchCtaBytes = 3 * 32768;
 

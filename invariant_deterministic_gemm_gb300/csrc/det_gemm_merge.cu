@@ -18,10 +18,15 @@ namespace {
 
 constexpr int kMaxParts = 8;
 
+// The parts' base addresses, passed by value.
+struct PartPtrs {
+    const uint8_t *p[kMaxParts];
+};
+
 // One thread per (row, two columns) for BF16 output or (row, column) for FP32.
 template <bool F32>
-__global__ void merge_parts_kernel(const uint8_t *part, int parts, int rows, int cols, long long part_ld,
-                                   long long part_stride, uint8_t *out, long long ldo)
+__global__ void merge_parts_kernel(PartPtrs parts_at, int parts, int rows, int cols, long long part_ld,
+                                   uint8_t *out, long long ldo)
 {
     constexpr int ES = F32 ? 4 : 2;
     const int per_row = F32 ? cols : (cols + 1) / 2;
@@ -30,13 +35,14 @@ __global__ void merge_parts_kernel(const uint8_t *part, int parts, int rows, int
     const int r = static_cast<int>(idx / per_row);
     const int j = static_cast<int>(idx - static_cast<long long>(r) * per_row);
     const int col = F32 ? j : 2 * j;
-    // A part slab's row pitch is a multiple of 8 elements, so the word at an
-    // even column is aligned and exists even when col + 1 == cols.
+    const bool pair = F32 || col + 1 < cols;
     uint32_t v[kMaxParts];
 #pragma unroll
     for (int i = 0; i < kMaxParts; ++i) {
-        if (i < parts)
-            v[i] = *reinterpret_cast<const uint32_t *>(part + (i * part_stride + r * part_ld + col) * ES);
+        if (i < parts) {
+            const uint8_t *src = parts_at.p[i] + (r * part_ld + col) * ES;
+            v[i] = pair ? *reinterpret_cast<const uint32_t *>(src) : *reinterpret_cast<const uint16_t *>(src);
+        }
     }
     // balanced tree over the parts, left operand first at every node
 #pragma unroll
@@ -46,8 +52,28 @@ __global__ void merge_parts_kernel(const uint8_t *part, int parts, int rows, int
             if (i + w < parts) v[i] = merge<F32>(v[i], v[i + w]);
     }
     uint8_t *dst = out + (static_cast<long long>(r) * ldo + col) * ES;
-    if (F32 || col + 1 < cols) *reinterpret_cast<uint32_t *>(dst) = v[0];
+    if (pair) *reinterpret_cast<uint32_t *>(dst) = v[0];
     else *reinterpret_cast<uint16_t *>(dst) = static_cast<uint16_t>(v[0] & 0xFFFFu);
+}
+
+cudaError_t launch_merge(bool f32, const PartPtrs &at, int parts, int rows, int cols, long long part_ld, void *out,
+                         long long ldo, cudaStream_t stream)
+{
+    if (parts < 2 || parts > kMaxParts || (parts & (parts - 1)) != 0) return cudaErrorInvalidValue;
+    const long long per_row = f32 ? cols : (cols + 1) / 2;
+    const long long n = static_cast<long long>(rows) * per_row;
+    if (n == 0) return cudaSuccess;
+    const int threads = 256;
+    const long long blocks = (n + threads - 1) / threads;
+    if (blocks > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+    uint8_t *dst = static_cast<uint8_t *>(out);
+    if (f32)
+        merge_parts_kernel<true><<<static_cast<unsigned>(blocks), threads, 0, stream>>>(at, parts, rows, cols, part_ld,
+                                                                                        dst, ldo);
+    else
+        merge_parts_kernel<false><<<static_cast<unsigned>(blocks), threads, 0, stream>>>(at, parts, rows, cols,
+                                                                                         part_ld, dst, ldo);
+    return cudaGetLastError();
 }
 
 }  // namespace
@@ -55,21 +81,19 @@ __global__ void merge_parts_kernel(const uint8_t *part, int parts, int rows, int
 cudaError_t launch_merge_parts(bool f32, const void *part, int parts, int rows, int cols, long long part_ld,
                                long long part_stride, void *out, long long ldo, cudaStream_t stream)
 {
-    if (parts < 2 || parts > kMaxParts || (parts & (parts - 1)) != 0) return cudaErrorInvalidValue;
-    const long long per_row = f32 ? cols : (cols + 1) / 2;
-    const long long n = static_cast<long long>(rows) * per_row;
-    const int threads = 256;
-    const long long blocks = (n + threads - 1) / threads;
-    if (blocks > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
-    const uint8_t *src = static_cast<const uint8_t *>(part);
-    uint8_t *dst = static_cast<uint8_t *>(out);
-    if (f32)
-        merge_parts_kernel<true><<<static_cast<unsigned>(blocks), threads, 0, stream>>>(src, parts, rows, cols, part_ld,
-                                                                                        part_stride, dst, ldo);
-    else
-        merge_parts_kernel<false><<<static_cast<unsigned>(blocks), threads, 0, stream>>>(src, parts, rows, cols,
-                                                                                         part_ld, part_stride, dst, ldo);
-    return cudaGetLastError();
+    if (parts < 2 || parts > kMaxParts) return cudaErrorInvalidValue;
+    PartPtrs at{};
+    for (int i = 0; i < parts; ++i) at.p[i] = static_cast<const uint8_t *>(part) + i * part_stride * (f32 ? 4 : 2);
+    return launch_merge(f32, at, parts, rows, cols, part_ld, out, ldo, stream);
+}
+
+cudaError_t launch_merge_list(bool f32, const void *const *parts, int n, int rows, int cols, long long ldp, void *out,
+                              long long ldo, cudaStream_t stream)
+{
+    if (n < 2 || n > kMaxParts) return cudaErrorInvalidValue;
+    PartPtrs at{};
+    for (int i = 0; i < n; ++i) at.p[i] = static_cast<const uint8_t *>(parts[i]);
+    return launch_merge(f32, at, n, rows, cols, ldp, out, ldo, stream);
 }
 
 }  // namespace detg

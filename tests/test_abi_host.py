@@ -193,3 +193,32 @@ def test_block_schedule_replays_the_mid_split_tree_for_every_leaf_count(dg):
         if L > 4:
             assert set(sizes) <= {2, 3, 4}, L
         assert replay_blocks(blocks, L) == mid_split_tree(0, L), L
+
+
+# ---------------------------------------------------------------- merge API
+
+def merge_call(dg, name, parts, n, out, M, N, ldp, ldc):
+    L = dg.lib()
+    arr = (ctypes.c_void_p * max(1, len(parts)))(*parts) if parts else None
+    return getattr(L, name)(arr, n, out, M, N, ldp, ldc, None)
+
+
+@pytest.mark.parametrize("name", ["det_gemm_merge", "det_gemm_merge_fp32"])
+def test_merge_argument_errors_are_returned_before_any_launch(dg, name):
+    parts = [P * (i + 2) for i in range(4)]
+    out = P * 64
+    assert merge_call(dg, name, parts[:3], 3, out, 4, 8, 8, 8) == 1          # n must be 2, 4 or 8
+    assert merge_call(dg, name, parts, 4, out, -1, 8, 8, 8) == 1             # negative size
+    assert merge_call(dg, name, [], 2, out, 4, 8, 8, 8) == 1                 # no part array
+    assert merge_call(dg, name, [0, parts[1]], 2, out, 4, 8, 8, 8) == 1      # null part
+    assert merge_call(dg, name, parts[:2], 2, 0, 4, 8, 8, 8) == 1            # null output
+    assert merge_call(dg, name, parts[:2], 2, out, 4, 8, 4, 8) == 1          # ldp < N
+    assert merge_call(dg, name, [parts[0] + 4, parts[1]], 2, out, 4, 8, 8, 8) == 3   # misaligned part
+    assert merge_call(dg, name, parts[:2], 2, out, 4, 8, 10, 8) == 3         # row pitch not a multiple of 16 B
+    assert merge_call(dg, name, [out, parts[1]], 2, out, 4, 8, 8, 8) == 1    # output overlaps a part
+    assert merge_call(dg, name, parts[:2], 2, out, 0, 8, 8, 8) == 0          # empty: nothing to do
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU answer")
+def test_merge_without_a_gpu_reports_unsupported_device(dg):
+    assert merge_call(dg, "det_gemm_merge", [P * 2, P * 3], 2, P * 64, 4, 8, 8, 8) == 4
