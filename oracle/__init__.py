@@ -67,6 +67,8 @@ def _load():
         lib.oracle_round_bf16.argtypes = [p, p, i64]
         lib.oracle_round_bf16.restype = None
         lib.oracle_add_bf16.argtypes = [p, p, p, i64]
+        lib.oracle_rmsnorm.argtypes = [p, i64, p, i64, i64, ctypes.c_float, p, i64]
+        lib.oracle_rmsnorm.restype = ctypes.c_int
         lib.oracle_add_bf16.restype = None
         _lib = lib
         return lib
@@ -191,3 +193,19 @@ def add_bf16(a: np.ndarray, b: np.ndarray) -> np.ndarray:
 def bf16_bits_to_f32(h: np.ndarray) -> np.ndarray:
     """BF16 bit patterns -> float32 values (a bit shift; no rounding)."""
     return (np.asarray(h, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+def rmsnorm(x: np.ndarray, w: np.ndarray, eps: float) -> np.ndarray:
+    """Batch-invariant RMSNorm of every row of x (BF16 bits [M, D]) with
+    weight w (BF16 bits [D]): the arithmetic is spelled out in
+    det_gemm_oracle.c (oracle_rmsnorm)."""
+    lib = _load()
+    x = np.ascontiguousarray(x, dtype=np.uint16)
+    w = np.ascontiguousarray(w, dtype=np.uint16)
+    M, D = x.shape
+    assert w.shape == (D,)
+    y = np.empty((M, D), dtype=np.uint16)
+    rc = lib.oracle_rmsnorm(x.ctypes.data, D, w.ctypes.data, M, D, float(eps), y.ctypes.data, D)
+    if rc != 0:
+        raise ValueError("oracle_rmsnorm: bad arguments")
+    return y

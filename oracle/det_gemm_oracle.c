@@ -273,3 +273,49 @@ void oracle_add_bf16(const uint16_t *a, const uint16_t *b, uint16_t *out, int64_
 {
     for (int64_t t = 0; t < n; ++t) out[t] = bf16_add(a[t], b[t]);
 }
+
+/* ------------------------------------------------------------- RMSNorm ---- */
+
+/*
+ * Batch-invariant RMSNorm, one row at a time ("Comment vaincre le
+ * non-déterminisme dans l'inférence des LLM", section "RMSNorm": each row is
+ * handled by one core, a data-parallel strategy, so the reduction order never
+ * depends on the batch). The page fixes the strategy, not the arithmetic;
+ * this oracle's reading, every step rounded once to nearest even:
+ *   ss  = sum of x_j * x_j over j in [0, D), reduced like det_gemm's FP32
+ *         variant: FP32 leaves of 32 consecutive squares in ascending j
+ *         (each square of a BF16 value is exact in FP32), merged by the
+ *         mid-split tree of FP32 adds;
+ *   m   = ss / D,   v = m + eps,   s = sqrt(v),   r = 1 / s   (FP32);
+ *   y_j = RNE_bf16((x_j * r) * w_j)   (two FP32 products, then BF16).
+ * Returns 0, or -1 on bad arguments.
+ */
+int oracle_rmsnorm(const uint16_t *x, int64_t ldx, const uint16_t *w, int64_t M, int64_t D, float eps,
+                   uint16_t *y, int64_t ldy)
+{
+    if (M < 0 || D < 1 || D > KC_MAX || ldx < D || ldy < D) return -1;
+    const int64_t L = (D + LEAF - 1) / LEAF;
+    float *leaves = (float *)malloc(sizeof(float) * (size_t)L);
+    if (!leaves) return -1;
+    for (int64_t i = 0; i < M; ++i) {
+        const uint16_t *xr = x + i * ldx;
+        for (int64_t l = 0; l < L; ++l) {
+            int64_t k0 = l * LEAF;
+            int64_t k1 = (k0 + LEAF < D) ? k0 + LEAF : D;
+            leaves[l] = leaf_f32(xr, 1, xr, 1, k0, k1);
+        }
+        float mx = 0.0f;
+        const float ss = tree_f32(leaves, 0, L, &mx);
+        const float m = ss / (float)D;
+        const float v = m + eps;
+        const float sq = sqrtf(v);
+        const float r = 1.0f / sq;
+        for (int64_t j = 0; j < D; ++j) {
+            const float t = bf16_to_f32(xr[j]) * r;
+            const float u = t * bf16_to_f32(w[j]);
+            y[i * ldy + j] = f32_to_bf16_rne(u);
+        }
+    }
+    free(leaves);
+    return 0;
+}

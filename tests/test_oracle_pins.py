@@ -349,3 +349,69 @@ def test_threads_do_not_change_bits():
     A = W.bits(W.randn_bf16((37, 500), 1.0, 1500))
     B = W.bits(W.randn_bf16((500, 9), 1.0, 1501))
     assert np.array_equal(oracle.gemm(A, B, threads=1), oracle.gemm(A, B, threads=7))
+
+
+# -------------------------------------------------------------- RMSNorm --
+
+def _ulp_bf16(v):
+    v = np.maximum(np.abs(np.asarray(v, dtype=np.float64)), 2.0 ** -126)
+    return np.ldexp(1.0, (np.floor(np.log2(v)) - 7).astype(np.int64))
+
+
+def test_rmsnorm_power_of_two_rows_give_the_weight_exactly():
+    # x_j = +-2^k, eps = 0: every step is exact, x_j * r = +-1, so y_j = +-w_j.
+    D = 96
+    w = W.bits(W.randn_bf16((D,), 1.0, 31))
+    for k in (-6, 0, 5):
+        signs = np.where(np.arange(D) % 3 == 0, -1.0, 1.0)
+        x = W.bits(torch.tensor(signs * 2.0 ** k, dtype=torch.float32).to(torch.bfloat16)).reshape(1, D)
+        y = oracle.rmsnorm(x, w, 0.0)[0]
+        want = np.where(signs < 0, w ^ 0x8000, w).astype(np.uint16)
+        assert np.array_equal(y, want), k
+
+
+def test_rmsnorm_is_invariant_to_power_of_two_scaling():
+    # eps = 0: squares, sums, the mean and sqrt all scale exactly, r by 2^-k.
+    x = W.randn_bf16((4, 1000), 1.0, 32)
+    w = W.bits(W.randn_bf16((1000,), 1.0, 33))
+    base = oracle.rmsnorm(W.bits(x), w, 0.0)
+    for k in (-3, 4):
+        scaled = W.bits((x.float() * 2.0 ** k).to(torch.bfloat16))
+        assert np.array_equal(oracle.rmsnorm(scaled, w, 0.0), base), k
+
+
+def test_rmsnorm_matches_the_exact_formula_within_one_bf16_ulp():
+    x = W.randn_bf16((6, 4096), 1.0, 34)
+    w = W.randn_bf16((4096,), 1.0, 35)
+    eps = 1e-5
+    y = oracle.bf16_bits_to_f32(oracle.rmsnorm(W.bits(x), W.bits(w), eps)).astype(np.float64)
+    xd = x.double().numpy()
+    wd = w.double().numpy()
+    exact = xd / np.sqrt((xd * xd).mean(axis=1, keepdims=True) + eps) * wd
+    # FP32 rounding before the final BF16 round is far below half a BF16 ulp
+    assert np.all(np.abs(y - exact) <= _ulp_bf16(exact) * 0.5 + np.abs(exact) * 2.0 ** -20)
+
+
+def test_rmsnorm_rows_are_independent_and_zero_rows_give_zero():
+    x = W.bits(W.randn_bf16((5, 300), 1.0, 36))
+    x[2] = 0
+    w = W.bits(W.randn_bf16((300,), 1.0, 37))
+    y = oracle.rmsnorm(x, w, 1e-6)
+    for i in range(5):
+        assert np.array_equal(oracle.rmsnorm(x[i:i + 1], w, 1e-6)[0], y[i])
+    assert np.all((y[2] & 0x7FFF) == 0)          # +0 or -0 (0 * r * w keeps w's sign)
+
+
+def test_rmsnorm_sum_of_squares_is_the_fp32_tree_of_the_row_with_itself():
+    # With w = 1 and eps = 0, y_j = RNE_bf16(x_j * r) with r = 1 / sqrt(ss / D);
+    # rebuild r from det_gemm's FP32 variant applied to the row and itself.
+    D = 1000
+    x = W.bits(W.randn_bf16((3, D), 1.0, 38))
+    ones = W.bits(torch.ones(D, dtype=torch.bfloat16))
+    y = oracle.rmsnorm(x, ones, 0.0)
+    for i in range(3):
+        ss = oracle.gemm(x[i:i + 1], np.ascontiguousarray(x[i:i + 1].T), out_fp32=True)[0, 0]
+        m = np.float32(ss) / np.float32(D)
+        r = np.float32(1.0) / np.sqrt(m, dtype=np.float32)
+        want = oracle.round_bf16((oracle.bf16_bits_to_f32(x[i]) * r).astype(np.float32))
+        assert np.array_equal(y[i], want), i
