@@ -181,6 +181,31 @@ det_gemm_status det_gemm_merge_fp32(const float *const *parts, int n, float *C, 
                                     int64_t ldc, det_gemm_stream stream);
 
 /*
+ * Batch-invariant RMSNorm: y[i, :] = x[i, :] / sqrt(mean_j x[i, j]^2 + eps)
+ * * w, BF16 in and out ("Comment vaincre le non-déterminisme dans
+ * l'inférence des LLM", section "RMSNorm": every row reduced by one core in
+ * a fixed order, whatever the batch size). The pages give the strategy; the
+ * arithmetic is this library's reading, each step rounded once to nearest
+ * even: ss = sum of x_j^2 reduced as det_gemm's FP32 variant reduces a
+ * contraction (32-element FP32 leaves, mid-split tree of FP32 adds);
+ * r = 1 / sqrt(ss / D + eps) in FP32; y_j = RNE_bf16((x_j * r) * w_j).
+ * A row's result therefore depends on that row, w and eps only: not on M,
+ * on the other rows, or on the run.
+ *
+ *   x  device, [M,D] BF16, row pitch ldx elements
+ *   w  device, [D] BF16
+ *   y  device, [M,D] BF16, row pitch ldy; y == x with ldy == ldx (in place)
+ *      is allowed, any other overlap with x or w is not
+ * Pointers and row pitches must be 16-byte aligned; D <= 32768; eps >= 0.
+ * Asynchronous on `stream`; nothing is allocated. Errors:
+ * DET_GEMM_ERR_INVALID_ARG, DET_GEMM_ERR_K_TOO_LARGE (D > 32768),
+ * DET_GEMM_ERR_ALIGNMENT, DET_GEMM_ERR_UNSUPPORTED_DEVICE,
+ * DET_GEMM_ERR_LAUNCH. M == 0 or D == 0 enqueues nothing.
+ */
+det_gemm_status det_rmsnorm(const det_gemm_bf16 *x, const det_gemm_bf16 *w, det_gemm_bf16 *y, int64_t M,
+                            int64_t D, float eps, int64_t ldx, int64_t ldy, det_gemm_stream stream);
+
+/*
  * det_gemm_fwd for callers that cannot allocate device memory. The pages
  * describing det_gemm have no counterpart to this entry point.
  *

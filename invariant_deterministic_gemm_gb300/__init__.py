@@ -82,6 +82,8 @@ def lib() -> ctypes.CDLL:
             fn = getattr(L, name)
             fn.argtypes = [p, ctypes.c_int, p, i64, i64, i64, i64, p]
             fn.restype = ctypes.c_int
+        L.det_rmsnorm.argtypes = [p, p, p, i64, i64, ctypes.c_float, i64, i64, p]
+        L.det_rmsnorm.restype = ctypes.c_int
         L.det_gemm_check.argtypes = [p]
         L.det_gemm_check.restype = ctypes.c_int
         L.det_gemm_status_string.argtypes = [ctypes.c_int]
@@ -300,6 +302,23 @@ def det_gemm_merge_fp32(parts, out=None, stream=None):
     return _merge("det_gemm_merge_fp32", parts, out, torch.float32, stream)
 
 
+def det_rmsnorm(x: torch.Tensor, w: torch.Tensor, eps: float = 1e-6, out=None, stream=None):
+    """Batch-invariant RMSNorm of every row of x [M, D] with weight w [D]
+    (BF16 in and out). out may be x itself (in place)."""
+    x_ptr, ldx = _mat(x, "x")
+    if not isinstance(w, torch.Tensor) or w.dtype != torch.bfloat16 or w.dim() != 1 or w.device.type != "cuda":
+        raise TypeError("w must be a 1-D bfloat16 CUDA tensor")
+    if w.shape[0] != x.shape[1] or (w.numel() > 1 and w.stride(0) != 1):
+        raise ValueError("w must be contiguous with x.shape[1] elements")
+    M, D = x.shape
+    y = _out(out, M, D, torch.bfloat16, x)
+    y_ptr, ldy = _mat(y, "out")
+    st = lib().det_rmsnorm(x_ptr, w.data_ptr(), y_ptr, M, D, float(eps), ldx, ldy, _stream_handle(stream))
+    if st != 0:
+        raise DetGemmError(st, "det_rmsnorm")
+    return y
+
+
 def det_gemm_check(stream=None) -> int:
     """Synchronise the stream and return (and clear) the device status code."""
     return int(lib().det_gemm_check(_stream_handle(stream)))
@@ -341,4 +360,5 @@ __all__ = [
     "det_gemm_debug_force_timeout", "det_gemm_shutdown", "DetGemmError", "lib", "status_string",
     "det_gemm_merge",
     "det_gemm_merge_fp32",
+    "det_rmsnorm",
 ]

@@ -52,6 +52,7 @@ ScratchEntry g_scratch[kMaxScratch];
 int g_scratch_count = 0;
 int g_scratch_next_evict = 0;
 int g_force_timeout = 0;
+std::mutex g_rms_mu;
 thread_local char g_detail[256] = "";
 
 // Records the CUDA error behind a DET_GEMM_ERR_LAUNCH / _CUDA status.
@@ -618,6 +619,41 @@ det_gemm_status det_gemm_merge_fp32(const float *const *parts, int n, float *C, 
 {
     return merge_parts(reinterpret_cast<const void *const *>(parts), n, C, M, N, ldp, ldc, 4,
                        reinterpret_cast<cudaStream_t>(stream));
+}
+
+det_gemm_status det_rmsnorm(const det_gemm_bf16 *x, const det_gemm_bf16 *w, det_gemm_bf16 *y, int64_t M,
+                            int64_t D, float eps, int64_t ldx, int64_t ldy, det_gemm_stream stream)
+{
+    if (M < 0 || D < 0 || !(eps >= 0.0f)) return DET_GEMM_ERR_INVALID_ARG;
+    if (M > (int64_t{1} << 31) - 256) return DET_GEMM_ERR_INVALID_ARG;
+    if (M == 0 || D == 0) return DET_GEMM_OK;
+    if (D > kKcMax) return DET_GEMM_ERR_K_TOO_LARGE;
+    const Mat xm = bf16(x, M, D, ldx), ym = bf16(y, M, D, ldy), wm = bf16(w, 1, D, D + (8 - D % 8) % 8);
+    det_gemm_status s;
+    if ((s = check_mat(xm)) != DET_GEMM_OK) return s;
+    if ((s = check_mat(ym)) != DET_GEMM_OK) return s;
+    if ((s = check_mat(wm)) != DET_GEMM_OK) return s;
+    // In place (y == x with the same pitch) is fine: a warp reads its whole
+    // row before it writes any of it. Any other overlap is not.
+    const bool in_place = static_cast<const void *>(x) == static_cast<const void *>(y) && ldx == ldy;
+    if ((!in_place && overlaps(xm, ym)) || overlaps(wm, ym)) return DET_GEMM_ERR_INVALID_ARG;
+    DeviceState *st = nullptr;
+    if ((s = device_state(&st)) != DET_GEMM_OK) return s;
+    static RmsParams p;   // 2 KiB of schedule: kept off the stack; guarded below
+    std::lock_guard<std::mutex> lk(g_rms_mu);
+    p.x = x;
+    p.w = w;
+    p.y = y;
+    p.ldx = ldx;
+    p.ldy = ldy;
+    p.rows = static_cast<int>(M);
+    p.d = static_cast<int>(D);
+    p.num_leaves = static_cast<int>((D + kLeaf - 1) / kLeaf);
+    p.eps = eps;
+    if (det_gemm_tree_schedule(p.num_leaves, p.sched) != DET_GEMM_OK) return DET_GEMM_ERR_INVALID_ARG;
+    const cudaError_t e = launch_rmsnorm(p, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail_cuda(DET_GEMM_ERR_LAUNCH, e, "rmsnorm launch");
+    return DET_GEMM_OK;
 }
 
 det_gemm_status det_gemm_check(det_gemm_stream stream)

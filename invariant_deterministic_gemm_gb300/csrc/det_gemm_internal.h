@@ -80,6 +80,19 @@ cudaError_t launch_merge_parts(bool f32, const void *part, int parts, int rows, 
 cudaError_t launch_merge_list(bool f32, const void *const *parts, int n, int rows, int cols, long long ldp, void *out,
                               long long ldo, cudaStream_t stream);
 
+// Batch-invariant RMSNorm (det_rmsnorm): one warp per row.
+struct RmsParams {
+    const uint16_t *x;            // [rows, d] BF16, row pitch ldx
+    const uint16_t *w;            // [d] BF16
+    uint16_t *y;                  // [rows, d] BF16, row pitch ldy
+    long long ldx, ldy;           // elements
+    int rows, d, num_leaves;
+    float eps;
+    uint16_t sched[kMaxLeaves];   // per-leaf merge schedule (det_gemm_tree_schedule)
+};
+constexpr int kRmsWarps = 8;      // rows per CTA
+cudaError_t launch_rmsnorm(const RmsParams &p, cudaStream_t stream);
+
 // Largest scratch_cta_bytes over all variants (bf16: 3 slots x 32 KiB).
 constexpr int kMaxScratchCtaBytes = 3 * 32768;
 

@@ -24,7 +24,7 @@ def dg():
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(det_gemm_[a-z0-9_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(det_[a-z0-9_]+)\s*\(", text)))
 
 
 def test_header_declares_the_page_surface():
@@ -222,3 +222,29 @@ def test_merge_argument_errors_are_returned_before_any_launch(dg, name):
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU answer")
 def test_merge_without_a_gpu_reports_unsupported_device(dg):
     assert merge_call(dg, "det_gemm_merge", [P * 2, P * 3], 2, P * 64, 4, 8, 8, 8) == 4
+
+
+# ---------------------------------------------------------------- RMSNorm
+
+def rms_call(dg, x, w, y, M, D, eps, ldx, ldy):
+    return dg.lib().det_rmsnorm(x, w, y, M, D, eps, ldx, ldy, None)
+
+
+def test_rmsnorm_argument_errors_are_returned_before_any_launch(dg):
+    x, w, y = P, P * 8, P * 64
+    assert rms_call(dg, x, w, y, 4, 32769, 1e-6, 32776, 32776) == 2      # D too large
+    assert rms_call(dg, x, w, y, -1, 8, 1e-6, 8, 8) == 1                 # negative size
+    assert rms_call(dg, x, w, y, 4, 8, -1.0, 8, 8) == 1                  # negative eps
+    assert rms_call(dg, x, w, y, 4, 8, float("nan"), 8, 8) == 1          # NaN eps
+    assert rms_call(dg, 0, w, y, 4, 8, 1e-6, 8, 8) == 1                  # null x
+    assert rms_call(dg, x, 0, y, 4, 8, 1e-6, 8, 8) == 1                  # null w
+    assert rms_call(dg, x, w + 2, y, 4, 8, 1e-6, 8, 8) == 3              # misaligned w
+    assert rms_call(dg, x, w, y, 4, 12, 1e-6, 12, 12) == 3               # pitch not 16 bytes
+    assert rms_call(dg, x, w, x + 16, 4, 8, 1e-6, 8, 8) == 1             # partial overlap with x
+    assert rms_call(dg, x, w, w, 4, 8, 1e-6, 8, 8) == 1                  # y overlaps w
+    assert rms_call(dg, x, w, y, 0, 8, 1e-6, 8, 8) == 0                  # empty
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU answer")
+def test_rmsnorm_in_place_passes_the_checks_and_needs_a_gpu(dg):
+    assert rms_call(dg, P, P * 8, P, 4, 8, 1e-6, 8, 8) == 4
