@@ -563,6 +563,20 @@ def configs_arm(args):
     report("long_k [4096,32768]@[32768,4096]", ms, 2.0 * 4096 * 32768 * 4096,
            2 * (2 * 4096 * 32768 + 4096 * 4096), tms)
     del A, B
+    # batch-invariant RMSNorm over the MLP activations (HBM-bound: read x and
+    # w, write y)
+    x = W.randn_bf16((8192, 4096), W.STD_ACT, W.seed_for(W.MLP, W.T_A)).to(dev)
+    wn = W.randn_bf16((4096,), 1.0, W.seed_for(W.MLP, W.T_B) + 200).to(dev)
+    yn = torch.empty_like(x)
+    ms = timeit(lambda: dg.det_rmsnorm(x, wn, 1e-6, out=yn), flush=flush)
+    nbytes = 2 * (2 * 8192 * 4096 + 4096)
+    tms = timeit(lambda: torch.nn.functional.rms_norm(x, (4096,), wn, 1e-6), flush=flush)
+    print(json.dumps({"workload": "rmsnorm [8192,4096]", "ms": round(ms, 4),
+                      "gb_per_s": round(nbytes / (ms * 1e-3) / 1e9, 1),
+                      "roofline_frac": round(nbytes / (pk["hbm"] * 1e9) / (ms * 1e-3), 4), "bound": "hbm",
+                      "peaks": "%s HBM %.0f GB/s" % (pk["source"], pk["hbm"]),
+                      "torch_rms_norm_ms": round(tms, 4)}), flush=True)
+    del x, yn
     # tiny
     A = W.randn_bf16((64, 256), 1.0, W.seed_for(W.TINY, W.T_A)).to(dev)
     B = W.randn_bf16((256, 64), 1.0, W.seed_for(W.TINY, W.T_B)).to(dev)

@@ -52,7 +52,6 @@ ScratchEntry g_scratch[kMaxScratch];
 int g_scratch_count = 0;
 int g_scratch_next_evict = 0;
 int g_force_timeout = 0;
-std::mutex g_rms_mu;
 thread_local char g_detail[256] = "";
 
 // Records the CUDA error behind a DET_GEMM_ERR_LAUNCH / _CUDA status.
@@ -639,8 +638,7 @@ det_gemm_status det_rmsnorm(const det_gemm_bf16 *x, const det_gemm_bf16 *w, det_
     if ((!in_place && overlaps(xm, ym)) || overlaps(wm, ym)) return DET_GEMM_ERR_INVALID_ARG;
     DeviceState *st = nullptr;
     if ((s = device_state(&st)) != DET_GEMM_OK) return s;
-    static RmsParams p;   // 2 KiB of schedule: kept off the stack; guarded below
-    std::lock_guard<std::mutex> lk(g_rms_mu);
+    RmsParams p;
     p.x = x;
     p.w = w;
     p.y = y;
@@ -650,7 +648,6 @@ det_gemm_status det_rmsnorm(const det_gemm_bf16 *x, const det_gemm_bf16 *w, det_
     p.d = static_cast<int>(D);
     p.num_leaves = static_cast<int>((D + kLeaf - 1) / kLeaf);
     p.eps = eps;
-    if (det_gemm_tree_schedule(p.num_leaves, p.sched) != DET_GEMM_OK) return DET_GEMM_ERR_INVALID_ARG;
     const cudaError_t e = launch_rmsnorm(p, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return fail_cuda(DET_GEMM_ERR_LAUNCH, e, "rmsnorm launch");
     return DET_GEMM_OK;

@@ -88,7 +88,6 @@ struct RmsParams {
     long long ldx, ldy;           // elements
     int rows, d, num_leaves;
     float eps;
-    uint16_t sched[kMaxLeaves];   // per-leaf merge schedule (det_gemm_tree_schedule)
 };
 constexpr int kRmsWarps = 8;      // rows per CTA
 cudaError_t launch_rmsnorm(const RmsParams &p, cudaStream_t stream);

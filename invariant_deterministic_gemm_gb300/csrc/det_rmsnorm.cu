@@ -11,6 +11,9 @@
 //   m = ss / D, v = m + eps, s = sqrt(v), r = 1 / s, each rounded once to
 //   nearest even (explicit _rn intrinsics, no approximations);
 //   y_j = RNE_bf16((x_j * r) * w_j).
+// The tree is evaluated bottom-up by the warp's lanes, level by level; it
+// is the same tree (the same nodes and operands), so the order of the adds
+// within a node never changes.
 // Every step is an IEEE round-to-nearest operation in a fixed order, so the
 // result is a function of the row alone: identical for every batch size,
 // and equal bit for bit to the CPU oracle that spells out the same steps.
@@ -56,58 +59,77 @@ __device__ __forceinline__ float leaf_squares(const uint16_t *x, int k0, int k1)
     return s;
 }
 
+// Node i of depth d of the mid-split tree over leaves [0, L): the path from
+// the root follows the bits of i, most significant first (0 = left child).
+__device__ __forceinline__ void tree_node(int L, int d, int i, int &lo, int &mid, int &hi)
+{
+    lo = 0;
+    hi = L;
+    for (int b = d - 1; b >= 0; --b) {
+        const int m = (lo + hi) >> 1;
+        if ((i >> b) & 1) lo = m;
+        else hi = m;
+    }
+    mid = (lo + hi) >> 1;
+}
+
 __global__ void __launch_bounds__(32 * kRmsWarps) rmsnorm_kernel(const __grid_constant__ RmsParams p)
 {
     __shared__ float leaves[kRmsWarps][kMaxLeaves];
-    __shared__ float slots[kRmsWarps][kMaxSlots];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int row = blockIdx.x * kRmsWarps + warp;
     if (row >= p.rows) return;
     const uint16_t *x = p.x + static_cast<long long>(row) * p.ldx;
     float *lv = leaves[warp];
+    const int L = p.num_leaves;
     // leaves, in parallel
-    for (int l = lane; l < p.num_leaves; l += 32) {
-        const int k0 = l * kLeaf;
-        const int k1 = min(k0 + kLeaf, p.d);
-        lv[l] = leaf_squares(x, k0, k1);
-    }
+#pragma unroll 4
+    for (int l = lane; l < L; l += 32) lv[l] = leaf_squares(x, l * kLeaf, min(l * kLeaf + kLeaf, p.d));
     __syncwarp();
-    // the mid-split tree, walked leaf by leaf (pending left children in slots)
-    float r = 0.0f;
-    if (lane == 0) {
-        float* st = slots[warp];
-        float root = 0.0f;
-        for (int l = 0; l < p.num_leaves; ++l) {
-            const uint32_t e = p.sched[l];
-            float v = lv[l];
-            for (uint32_t m = e & 0x3FFu, s = 0; m != 0; m >>= 1, ++s)
-                if (m & 1u) v = __fadd_rn(st[s], v);
-            const uint32_t dst = e >> 12;
-            if (dst == kSlotRoot) root = v;
-            else st[dst] = v;
+    // The mid-split tree, bottom-up, in place: node (lo, hi) keeps its value
+    // in lv[lo]; an internal node adds its children's values, lv[lo] (left)
+    // and lv[mid] (right). Nodes of one depth cover disjoint ranges.
+    int depth = 0;
+    while ((1 << depth) < L) ++depth;
+    for (int d = depth - 1; d >= 0; --d) {
+        for (int i = lane; i < (1 << d); i += 32) {
+            int lo, mid, hi;
+            tree_node(L, d, i, lo, mid, hi);
+            if (hi - lo >= 2) lv[lo] = __fadd_rn(lv[lo], lv[mid]);
         }
-        const float m = __fdiv_rn(root, static_cast<float>(p.d));
-        const float sq = __fsqrt_rn(__fadd_rn(m, p.eps));
-        r = __fdiv_rn(1.0f, sq);
+        __syncwarp();
     }
-    r = __shfl_sync(0xFFFFFFFFu, r, 0);
-    // y = RNE_bf16((x * r) * w)
+    const float m = __fdiv_rn(lv[0], static_cast<float>(p.d));
+    const float r = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(m, p.eps)));
+    // y = RNE_bf16((x * r) * w), four 16-byte chunks per lane at a time
     uint16_t *y = p.y + static_cast<long long>(row) * p.ldy;
-    const bool vec = ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y) |
-                       reinterpret_cast<uintptr_t>(p.w)) & 15u) == 0;
-    const int dv = vec ? p.d / 8 * 8 : 0;
-    for (int j = lane * 8; j < dv; j += 32 * 8) {
-        const uint4 xv = *reinterpret_cast<const uint4 *>(x + j);
-        const uint4 wv = *reinterpret_cast<const uint4 *>(p.w + j);
-        const uint32_t xs[4] = {xv.x, xv.y, xv.z, xv.w}, ws[4] = {wv.x, wv.y, wv.z, wv.w};
-        uint32_t out[4];
+    const int dv = p.d / 8 * 8;
+    constexpr int U = 4;
+    for (int j0 = lane * 8; j0 < dv; j0 += 32 * 8 * U) {
+        uint4 xv[U], wv[U];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float lo = __fmul_rn(__fmul_rn(bf16_lo(xs[i]), r), bf16_lo(ws[i]));
-            const float hi = __fmul_rn(__fmul_rn(bf16_hi(xs[i]), r), bf16_hi(ws[i]));
-            out[i] = static_cast<uint32_t>(to_bf16(lo)) | (static_cast<uint32_t>(to_bf16(hi)) << 16);
+        for (int u = 0; u < U; ++u) {
+            const int j = j0 + u * 32 * 8;
+            if (j < dv) {
+                xv[u] = *reinterpret_cast<const uint4 *>(x + j);
+                wv[u] = *reinterpret_cast<const uint4 *>(p.w + j);
+            }
         }
-        *reinterpret_cast<uint4 *>(y + j) = make_uint4(out[0], out[1], out[2], out[3]);
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int j = j0 + u * 32 * 8;
+            if (j >= dv) break;
+            const uint32_t xs[4] = {xv[u].x, xv[u].y, xv[u].z, xv[u].w};
+            const uint32_t ws[4] = {wv[u].x, wv[u].y, wv[u].z, wv[u].w};
+            uint32_t out[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float lo = __fmul_rn(__fmul_rn(bf16_lo(xs[k]), r), bf16_lo(ws[k]));
+                const float hi = __fmul_rn(__fmul_rn(bf16_hi(xs[k]), r), bf16_hi(ws[k]));
+                out[k] = static_cast<uint32_t>(to_bf16(lo)) | (static_cast<uint32_t>(to_bf16(hi)) << 16);
+            }
+            *reinterpret_cast<uint4 *>(y + j) = make_uint4(out[0], out[1], out[2], out[3]);
+        }
     }
     for (int j = dv + lane; j < p.d; j += 32)
         y[j] = to_bf16(__fmul_rn(__fmul_rn(bf16_at(x + j), r), bf16_at(p.w + j)));
