@@ -69,6 +69,8 @@ def _load():
         lib.oracle_add_bf16.argtypes = [p, p, p, i64]
         lib.oracle_rmsnorm.argtypes = [p, i64, p, i64, i64, ctypes.c_float, p, i64]
         lib.oracle_rmsnorm.restype = ctypes.c_int
+        lib.oracle_rowdot.argtypes = [p, i64, p, i64, i64, i64, p]
+        lib.oracle_rowdot.restype = ctypes.c_int
         lib.oracle_add_bf16.restype = None
         _lib = lib
         return lib
@@ -209,3 +211,18 @@ def rmsnorm(x: np.ndarray, w: np.ndarray, eps: float) -> np.ndarray:
     if rc != 0:
         raise ValueError("oracle_rmsnorm: bad arguments")
     return y
+
+
+def rowdot(C: np.ndarray, D: np.ndarray) -> np.ndarray:
+    """rowdot[i] = sum_n C[i, n] * D[i, n] (BF16 bits in, FP32 out) in the
+    grouped-GEMM epilogue's fixed order (see oracle_rowdot in
+    det_gemm_oracle.c)."""
+    lib = _load()
+    C = np.ascontiguousarray(C, dtype=np.uint16)
+    D = np.ascontiguousarray(D, dtype=np.uint16)
+    assert C.shape == D.shape
+    M, N = C.shape
+    out = np.empty(M, dtype=np.float32)
+    if lib.oracle_rowdot(C.ctypes.data, N, D.ctypes.data, N, M, N, out.ctypes.data) != 0:
+        raise ValueError("oracle_rowdot: bad arguments")
+    return out

@@ -415,3 +415,45 @@ def test_rmsnorm_sum_of_squares_is_the_fp32_tree_of_the_row_with_itself():
         r = np.float32(1.0) / np.sqrt(m, dtype=np.float32)
         want = oracle.round_bf16((oracle.bf16_bits_to_f32(x[i]) * r).astype(np.float32))
         assert np.array_equal(y[i], want), i
+
+
+# -------------------------------------------------- grouped row reduction --
+
+def test_rowdot_is_the_exact_dot_on_integer_inputs():
+    # small integers: every product and partial sum is an exact FP32 integer,
+    # so any order gives the exact dot product; a dropped or misplaced term,
+    # a wrong row or a transposed operand does not
+    C = W.bits(W.randint_bf16((7, 1000), -4, 4, 41))
+    D = W.bits(W.randint_bf16((7, 1000), -4, 4, 42))
+    got = oracle.rowdot(C, D)
+    want = (oracle.bf16_bits_to_f32(C).astype(np.float64) * oracle.bf16_bits_to_f32(D)).sum(axis=1)
+    assert np.array_equal(got.astype(np.float64), want)
+
+
+def test_rowdot_order_separates_tiles_from_a_running_sum():
+    # Three column tiles with dot values 1, 2^-24, 2^-24. The fixed order is
+    # the mid-split tree over tiles: 1 + (2^-24 + 2^-24) = 1 + 2^-23 (exact);
+    # a running sum would give (1 + 2^-24) + 2^-24 = 1 (ties to even twice).
+    N = 3 * 128
+    C = np.zeros((1, N), dtype=np.float32)
+    D = np.zeros((1, N), dtype=np.float32)
+    C[0, 0], D[0, 0] = 1.0, 1.0
+    C[0, 128], D[0, 128] = 2.0 ** -12, 2.0 ** -12
+    C[0, 256], D[0, 256] = 2.0 ** -12, 2.0 ** -12
+    cb = W.bits(torch.from_numpy(C).to(torch.bfloat16))
+    db = W.bits(torch.from_numpy(D).to(torch.bfloat16))
+    assert oracle.rowdot(cb, db)[0] == np.float32(1.0 + 2.0 ** -23)
+
+
+def test_rowdot_quarters_combine_as_two_pairs():
+    # One tile with quarter values 2^-24, 2^-24, 1, 0 (one product each).
+    # Pairs: (2^-24 + 2^-24) + (1 + 0) = 2^-23 + 1, exact. A running sum over
+    # the quarters would give ((2^-24 + 2^-24) + 1) + 0, the same here, but a
+    # running sum over the row's columns or the pair (q0 + q2) first would
+    # not: 2^-24 + 1 rounds to 1 (a tie, to even).
+    C = np.zeros((1, 128), dtype=np.float32)
+    C[0, 0] = 2.0 ** -12
+    C[0, 32] = 2.0 ** -12
+    C[0, 64] = 1.0
+    cb = W.bits(torch.from_numpy(C).to(torch.bfloat16))
+    assert oracle.rowdot(cb, cb)[0] == np.float32(1.0 + 2.0 ** -23)
