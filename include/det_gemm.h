@@ -145,6 +145,45 @@ det_gemm_status det_gemm_db_transposed(const det_gemm_bf16 *A, const det_gemm_bf
                                        det_gemm_stream stream);
 
 /*
+ * Grouped forward product: C_g = A_g @ B_g for g < G (the expert GEMMs of a
+ * mixture-of-experts layer), every group with its own rows M[g] and
+ * operands, all with the same N and K. Groups are taken eight at a time,
+ * each eight in one persistent launch over all their output tiles. Every
+ * tile is computed end to end by one CTA with the same leaves and merge
+ * tree as det_gemm_fwd, so C_g is det_gemm_fwd(A_g, B_g) bit for bit: a
+ * token's result does not depend on how many tokens its expert received.
+ *
+ * Optional row reduction (the per-token quantity the Megatron Core notes
+ * describe as accumulated atomically across N-tiles, section "Kernel
+ * redesign: the grouped-GEMM epilogue"): when rowdot and rowdot[g] are not
+ * NULL, rowdot[g][i] = sum over n of C_g[i, n] * D_g[i, n] in FP32, formed
+ * with private per-tile partial slots and a fixed reduction order, never
+ * with atomics: for each 128-column tile t and 32-column quarter q the FP32
+ * sum of the (exact) products in ascending column order; each tile's
+ * quarters combined as ((q0 + q1) + (q2 + q3)); the tiles by the mid-split
+ * tree of FP32 adds. Same bits every run. N must then be <= 131072 (1024
+ * column tiles).
+ *
+ *   A[g]    device, [M[g],K] BF16, row pitch lda[g]
+ *   B[g]    device, [K,N] BF16, row pitch ldb[g]
+ *   C[g]    device, [M[g],N] BF16, row pitch ldc[g]
+ *   D[g], ldd[g]  device, [M[g],N] BF16 (only where rowdot[g] is used)
+ *   rowdot[g]     device, [M[g]] FP32, 16-byte aligned, or NULL
+ * A, B, C, M, lda, ldb, ldc, D, ldd and rowdot are host arrays of G entries
+ * (D, ldd and rowdot may be NULL altogether). Alignment and aliasing rules
+ * are det_gemm_fwd's; the outputs of different groups must not overlap.
+ * Asynchronous on `stream`. Errors as det_gemm_fwd; every group's arguments
+ * are checked before the first launch of a call is enqueued only for the
+ * counts and pointers above, so a later batch of eight can still fail its
+ * own checks after an earlier one was enqueued.
+ */
+det_gemm_status det_gemm_fwd_grouped(int G, const det_gemm_bf16 *const *A, const det_gemm_bf16 *const *B,
+                                     det_gemm_bf16 *const *C, const int64_t *M, int64_t N, int64_t K,
+                                     const int64_t *lda, const int64_t *ldb, const int64_t *ldc,
+                                     const det_gemm_bf16 *const *D, const int64_t *ldd, float *const *rowdot,
+                                     det_gemm_stream stream);
+
+/*
  * Merges partial products over contiguous contraction ranges into the full
  * product: the deterministic composition of a contraction sharded over n
  * GPUs or streams (RL-Kernel, "Batch-Invariant Deterministic GEMM

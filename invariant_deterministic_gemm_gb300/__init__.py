@@ -82,6 +82,8 @@ def lib() -> ctypes.CDLL:
             fn = getattr(L, name)
             fn.argtypes = [p, ctypes.c_int, p, i64, i64, i64, i64, p]
             fn.restype = ctypes.c_int
+        L.det_gemm_fwd_grouped.argtypes = [ctypes.c_int, p, p, p, p, i64, i64, p, p, p, p, p, p, p]
+        L.det_gemm_fwd_grouped.restype = ctypes.c_int
         L.det_rmsnorm.argtypes = [p, p, p, i64, i64, ctypes.c_float, i64, i64, p]
         L.det_rmsnorm.restype = ctypes.c_int
         L.det_gemm_check.argtypes = [p]
@@ -302,6 +304,49 @@ def det_gemm_merge_fp32(parts, out=None, stream=None):
     return _merge("det_gemm_merge_fp32", parts, out, torch.float32, stream)
 
 
+def det_gemm_fwd_grouped(As, Bs, outs=None, D=None, stream=None):
+    """C_g = A_g @ B_g for every group g (mixture-of-experts expert GEMMs):
+    As[g] [M_g, K], Bs[g] [K, N] BF16. With D (a list of [M_g, N] BF16
+    tensors, None entries allowed) also returns rowdot[g][i] = sum_n C_g[i, n]
+    * D_g[i, n] (FP32) in a fixed order. Returns the list of C (and the list
+    of rowdot tensors, None where D[g] is None, when D is given)."""
+    G = len(As)
+    if len(Bs) != G or (outs is not None and len(outs) != G) or (D is not None and len(D) != G):
+        raise ValueError("As, Bs, outs and D must have one entry per group")
+    if G == 0:
+        return ([], []) if D is not None else []
+    K, N = Bs[0].shape
+    mats_a = [_mat(a, "As[%d]" % g) for g, a in enumerate(As)]
+    mats_b = [_mat(b, "Bs[%d]" % g) for g, b in enumerate(Bs)]
+    for g in range(G):
+        if As[g].shape[1] != K or tuple(Bs[g].shape) != (K, N):
+            raise ValueError("group %d: A must be [M, %d] and B [%d, %d]" % (g, K, K, N))
+    Cs = [_out(None if outs is None else outs[g], As[g].shape[0], N, torch.bfloat16, As[g]) for g in range(G)]
+    mats_c = [_mat(c, "outs[%d]" % g) for g, c in enumerate(Cs)]
+    ptrs = lambda xs: (ctypes.c_void_p * G)(*xs)
+    lds = lambda xs: (ctypes.c_int64 * G)(*xs)
+    Ms = lds([a.shape[0] for a in As])
+    rowdots = None
+    d_arr = ld_arr = rd_arr = None
+    if D is not None:
+        rowdots = [None if D[g] is None else torch.empty(As[g].shape[0], dtype=torch.float32, device=As[g].device)
+                   for g in range(G)]
+        dm = [(0, N) if D[g] is None else _mat(D[g], "D[%d]" % g) for g in range(G)]
+        for g in range(G):
+            if D[g] is not None and tuple(D[g].shape) != (As[g].shape[0], N):
+                raise ValueError("D[%d] must be [M, N]" % g)
+        d_arr = ptrs([x for x, _ in dm])
+        ld_arr = lds([x for _, x in dm])
+        rd_arr = ptrs([0 if r is None else r.data_ptr() for r in rowdots])
+    st = lib().det_gemm_fwd_grouped(G, ptrs([x for x, _ in mats_a]), ptrs([x for x, _ in mats_b]),
+                                    ptrs([x for x, _ in mats_c]), Ms, N, K, lds([x for _, x in mats_a]),
+                                    lds([x for _, x in mats_b]), lds([x for _, x in mats_c]), d_arr, ld_arr, rd_arr,
+                                    _stream_handle(stream))
+    if st != 0:
+        raise DetGemmError(st, "det_gemm_fwd_grouped")
+    return (Cs, rowdots) if D is not None else Cs
+
+
 def det_rmsnorm(x: torch.Tensor, w: torch.Tensor, eps: float = 1e-6, out=None, stream=None):
     """Batch-invariant RMSNorm of every row of x [M, D] with weight w [D]
     (BF16 in and out). out may be x itself (in place)."""
@@ -361,4 +406,5 @@ __all__ = [
     "det_gemm_merge",
     "det_gemm_merge_fp32",
     "det_rmsnorm",
+    "det_gemm_fwd_grouped",
 ]

@@ -330,15 +330,15 @@ bool encode(CUtensorMap *m, const void *ptr, uint64_t inner, uint64_t outer, uin
 // dA launch (8192 x 14336 x 4096): groups of 8, 32 and 63 one-MiB A panels
 // read 999, 307 and 1512 MB from DRAM; a quarter of the L2 keeps the
 // resident panels from being evicted by the streamed ones and the output.
-void choose_tile_order(Params &p, int bn)
+void choose_tile_order(Problem &pb, int64_t rows, int64_t cols, int64_t kc, int bn, int n_tiles)
 {
     constexpr double kResidentBytes = 32.0 * 1024 * 1024;
-    const double a_bytes = 2.0 * p.rows * p.kc, b_bytes = 2.0 * p.cols * p.kc;
-    p.rows_fast = a_bytes <= b_bytes ? 1 : 0;
-    const double panel = 2.0 * (p.rows_fast ? kBM : bn) * p.kc;
-    const int tiles = p.rows_fast ? p.m_tiles : p.n_tiles;
+    const double a_bytes = 2.0 * rows * kc, b_bytes = 2.0 * cols * kc;
+    pb.rows_fast = a_bytes <= b_bytes ? 1 : 0;
+    const double panel = 2.0 * (pb.rows_fast ? kBM : bn) * kc;
+    const int tiles = pb.rows_fast ? pb.m_tiles : n_tiles;
     const int fit = panel > 0 ? static_cast<int>(kResidentBytes / panel) : tiles;
-    p.group = std::max(1, std::min(tiles, fit));
+    pb.group = std::max(1, std::min(tiles, fit));
 }
 
 // Contraction parts per tile. A launch with few output tiles (skinny M)
@@ -361,43 +361,84 @@ int choose_parts(int64_t tiles, int64_t L, int sms)
     return best;
 }
 
-// One GEMM: out[rows, cols] = sum over kc of Aop[row, k] * Bop[k, col].
-// Aop is `a` stored either K-major ([rows, kc] row-major) or MN-major
-// ([kc, rows] row-major); Bop is `b` stored K-major ([cols, kc]) or MN-major
-// ([kc, cols]).
+// One GEMM of a launch: out[rows, cols] = sum over kc of Aop[row, k] *
+// Bop[k, col]. Aop is `a` stored either K-major ([rows, kc] row-major) or
+// MN-major ([kc, rows] row-major); Bop is `b` stored K-major ([cols, kc]) or
+// MN-major ([kc, cols]). d / rowdot: the optional row reduction of a grouped
+// launch (rowdot[i] = sum_n out[i, n] * d[i, n], fixed order).
+struct ProblemArgs {
+    Mat a, b, out;
+    int64_t rows;
+    const void *d;
+    int64_t ldd;
+    float *rowdot;
+};
+
+constexpr size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+// The launch of one or several GEMMs sharing cols and kc (a plain launch:
+// g == 1; a grouped one: every group's tiles in one persistent launch).
 // fixed_scratch, when given, replaces the cached per-stream scratch: the
 // launch then allocates nothing at all (see det_gemm_fwd_noalloc).
-det_gemm_status run(Variant v, Mat a, bool a_kmajor, Mat b, bool b_kmajor, Mat out, int64_t rows, int64_t cols,
-                    int64_t kc, cudaStream_t stream, void *fixed_scratch = nullptr, size_t fixed_bytes = 0)
+det_gemm_status run_problems(Variant v, bool a_kmajor, bool b_kmajor, const ProblemArgs *pa, int g, int64_t cols,
+                             int64_t kc, cudaStream_t stream, void *fixed_scratch = nullptr, size_t fixed_bytes = 0)
 {
-    if (rows < 0 || cols < 0 || kc < 0) return DET_GEMM_ERR_INVALID_ARG;
-    if (rows > (int64_t{1} << 31) - 256 || cols > (int64_t{1} << 31) - 256) return DET_GEMM_ERR_INVALID_ARG;
-    if (rows == 0 || cols == 0) return DET_GEMM_OK;
+    if (g < 1 || g > kMaxProblems || cols < 0 || kc < 0) return DET_GEMM_ERR_INVALID_ARG;
+    if (cols > (int64_t{1} << 31) - 256) return DET_GEMM_ERR_INVALID_ARG;
     if (kc > kKcMax) return DET_GEMM_ERR_K_TOO_LARGE;
-    det_gemm_status s = check_mat(out);
-    if (s != DET_GEMM_OK) return s;
-    if (kc > 0) {
-        if ((s = check_mat(a)) != DET_GEMM_OK) return s;
-        if ((s = check_mat(b)) != DET_GEMM_OK) return s;
-        if (overlaps(out, a) || overlaps(out, b)) return DET_GEMM_ERR_INVALID_ARG;
+    det_gemm_status s;
+    bool any = false;
+    for (int i = 0; i < g; ++i) {
+        const ProblemArgs &q = pa[i];
+        if (q.rows < 0 || q.rows > (int64_t{1} << 31) - 256) return DET_GEMM_ERR_INVALID_ARG;
+        if (q.rows == 0 || cols == 0) continue;
+        any = true;
+        if ((s = check_mat(q.out)) != DET_GEMM_OK) return s;
+        if (kc > 0) {
+            if ((s = check_mat(q.a)) != DET_GEMM_OK) return s;
+            if ((s = check_mat(q.b)) != DET_GEMM_OK) return s;
+            if (overlaps(q.out, q.a) || overlaps(q.out, q.b)) return DET_GEMM_ERR_INVALID_ARG;
+        }
+        if (q.rowdot) {
+            const Mat dm{q.d, q.rows, cols, q.ldd, 2};
+            if (q.d == nullptr) return DET_GEMM_ERR_INVALID_ARG;
+            if ((s = check_mat(dm)) != DET_GEMM_OK) return s;
+            if (reinterpret_cast<uintptr_t>(q.rowdot) % 16 != 0) return DET_GEMM_ERR_ALIGNMENT;
+            const Mat rm{q.rowdot, 1, q.rows, q.rows, 4};
+            if (overlaps(rm, q.out) || overlaps(rm, dm) || overlaps(q.out, dm)) return DET_GEMM_ERR_INVALID_ARG;
+        }
+        for (int j = 0; j < i; ++j)
+            if (pa[j].rows > 0 && overlaps(q.out, pa[j].out)) return DET_GEMM_ERR_INVALID_ARG;
     }
+    if (!any) return DET_GEMM_OK;
     DeviceState *st = nullptr;
     if ((s = device_state(&st)) != DET_GEMM_OK) return s;
 
     if (kc == 0) {
-        // Empty contraction: every element is the empty sum, +0.
-        cudaError_t e = cudaMemset2DAsync(const_cast<void *>(out.ptr), static_cast<size_t>(out.ld * out.esize), 0,
-                                          static_cast<size_t>(cols * out.esize), static_cast<size_t>(rows), stream);
-        return e == cudaSuccess ? DET_GEMM_OK : (cudaGetLastError(), DET_GEMM_ERR_LAUNCH);
+        // Empty contraction: every element is the empty sum, +0 (and so is
+        // every row reduction).
+        for (int i = 0; i < g; ++i) {
+            const ProblemArgs &q = pa[i];
+            if (q.rows == 0 || cols == 0) continue;
+            cudaError_t e = cudaMemset2DAsync(const_cast<void *>(q.out.ptr), static_cast<size_t>(q.out.ld * q.out.esize),
+                                              0, static_cast<size_t>(cols * q.out.esize), static_cast<size_t>(q.rows),
+                                              stream);
+            if (e == cudaSuccess && q.rowdot) e = cudaMemsetAsync(q.rowdot, 0, sizeof(float) * q.rows, stream);
+            if (e != cudaSuccess) return (cudaGetLastError(), DET_GEMM_ERR_LAUNCH);
+        }
+        return DET_GEMM_OK;
     }
     if ((s = prepare_variant(st, v)) != DET_GEMM_OK) return s;
     VariantOps ops = variant_ops(v);
 
     const int64_t L = (kc + kLeaf - 1) / kLeaf;
-    const int64_t tiles = ((rows + kBM - 1) / kBM) * ((cols + ops.bn - 1) / ops.bn);
+    const int64_t n_tiles = (cols + ops.bn - 1) / ops.bn;
+    int64_t tiles = 0;
+    for (int i = 0; i < g; ++i) tiles += (pa[i].rows + kBM - 1) / kBM * n_tiles;
     if (tiles > (int64_t{1} << 31) - 1) return DET_GEMM_ERR_INVALID_ARG;
-    // The allocation-free path never splits: the partial results need memory.
-    const int parts = fixed_scratch ? 1 : choose_parts(tiles, L, st->sm_count);
+    // Only a plain launch splits (the allocation-free path never does: the
+    // partial results need memory).
+    const int parts = (fixed_scratch || g > 1) ? 1 : choose_parts(tiles, L, st->sm_count);
     const int64_t Lp = L / parts;
     const BlockSchedule *blocks = nullptr;
     if (!fixed_scratch) {
@@ -407,29 +448,51 @@ det_gemm_status run(Variant v, Mat a, bool a_kmajor, Mat b, bool b_kmajor, Mat o
 
     Params p;
     std::memset(&p, 0, sizeof(p));
-    bool ok;
-    // A K-major A operand with fewer rows than a tile is copied with a box of
-    // only its rows (rounded up to 8, at least 16): on GB300 a copy whose
-    // box is mostly outside the tensor, here 128 rows for fewer than 16,
-    // took the QKV launch from 35 to 57 us. The tile's other rows keep
-    // whatever the shared-memory slot holds; MMA row i reads only row i of
-    // A, and those rows are never stored.
-    const int a_box_rows = (a_kmajor && rows < kBM) ? static_cast<int>(std::max<int64_t>(16, (rows + 7) / 8 * 8))
-                                                    : kBM;
-    if (a_kmajor) ok = encode(&p.tmap_a, a.ptr, kc, rows, a.ld, 64, static_cast<uint32_t>(a_box_rows));
-    else ok = encode(&p.tmap_a, a.ptr, rows, kc, a.ld, 64, 64);
-    p.stage_tx = a_box_rows * kBK * 2 + ops.bn * kBK * 2;
-    if (ok) {
-        if (b_kmajor) ok = encode(&p.tmap_b, b.ptr, kc, cols, b.ld, 64, ops.bn);
-        else ok = encode(&p.tmap_b, b.ptr, cols, kc, b.ld, 64, 64);
+    p.num_problems = g;
+    p.n_tiles = static_cast<int>(n_tiles);
+    int64_t units = 0;
+    size_t rd_bytes = 0;
+    for (int i = 0; i < g; ++i) {
+        const ProblemArgs &q = pa[i];
+        Problem &pb = p.prob[i];
+        pb.first_unit = static_cast<int>(units);
+        pb.rows = static_cast<int>(q.rows);
+        pb.m_tiles = static_cast<int>((q.rows + kBM - 1) / kBM);
+        if (q.rows == 0) continue;
+        units += static_cast<int64_t>(pb.m_tiles) * n_tiles * parts;
+        // A K-major A operand with fewer rows than a tile is copied with a box
+        // of only its rows (rounded up to 8, at least 16): on GB300 a copy
+        // whose box is mostly outside the tensor, here 128 rows for fewer than
+        // 16, took the QKV launch from 35 to 57 us. The tile's other rows keep
+        // whatever the shared-memory slot holds; MMA row i reads only row i
+        // of A, and those rows are never stored.
+        const int a_box_rows =
+            (a_kmajor && q.rows < kBM) ? static_cast<int>(std::max<int64_t>(16, (q.rows + 7) / 8 * 8)) : kBM;
+        bool ok;
+        if (a_kmajor) ok = encode(&pb.tmap_a, q.a.ptr, kc, q.rows, q.a.ld, 64, static_cast<uint32_t>(a_box_rows));
+        else ok = encode(&pb.tmap_a, q.a.ptr, q.rows, kc, q.a.ld, 64, 64);
+        if (ok) {
+            if (b_kmajor) ok = encode(&pb.tmap_b, q.b.ptr, kc, cols, q.b.ld, 64, ops.bn);
+            else ok = encode(&pb.tmap_b, q.b.ptr, cols, kc, q.b.ld, 64, 64);
+        }
+        if (!ok) return DET_GEMM_ERR_LAUNCH;
+        pb.stage_tx = a_box_rows * kBK * 2 + ops.bn * kBK * 2;
+        pb.out = const_cast<void *>(q.out.ptr);
+        pb.ldo = q.out.ld;
+        choose_tile_order(pb, q.rows, cols, kc, ops.bn, p.n_tiles);
+        if (q.rowdot) {
+            pb.rd_d = static_cast<const uint16_t *>(q.d);
+            pb.rd_ldd = q.ldd;
+            rd_bytes += align256(sizeof(float) * 4 * n_tiles * q.rows);
+        }
     }
-    if (!ok) return DET_GEMM_ERR_LAUNCH;
-    p.out = const_cast<void *>(out.ptr);
-    p.ldo = out.ld;
+    if (units > (int64_t{1} << 31) - 1) return DET_GEMM_ERR_INVALID_ARG;
+    p.units = static_cast<int>(units);
     // A split launch's part slabs: rows x part_ld each, the row pitch a
     // multiple of 8 elements (16 bytes).
     const int64_t part_ld = (cols + 7) / 8 * 8;
-    const size_t part_bytes = parts > 1 ? static_cast<size_t>(parts) * rows * part_ld * out.esize : 0;
+    const size_t part_bytes =
+        parts > 1 ? align256(static_cast<size_t>(parts) * pa[0].rows * part_ld * pa[0].out.esize) : 0;
     if (fixed_scratch) {
         p.scratch = fixed_scratch;
     } else {
@@ -437,25 +500,28 @@ det_gemm_status run(Variant v, Mat a, bool a_kmajor, Mat b, bool b_kmajor, Mat o
         cudaGetDevice(&dev);
         // The deep-slot part is sized for the largest variant and a grid of
         // one CTA per SM, so every launch on this stream can reuse it; the
-        // part slabs of a split launch follow it.
+        // part slabs of a split launch and the row-reduction partials
+        // follow it.
         const size_t slot_bytes = static_cast<size_t>(st->sm_count) * kMaxScratchCtaBytes;
-        uint8_t *base = static_cast<uint8_t *>(scratch_for(dev, stream, slot_bytes + part_bytes));
+        uint8_t *base = static_cast<uint8_t *>(scratch_for(dev, stream, slot_bytes + part_bytes + rd_bytes));
         if (!base) return DET_GEMM_ERR_LAUNCH;
         p.scratch = base;
         p.part_out = parts > 1 ? base + slot_bytes : nullptr;
+        uint8_t *rd = base + slot_bytes + part_bytes;
+        for (int i = 0; i < g; ++i) {
+            if (!pa[i].rowdot || pa[i].rows == 0) continue;
+            p.prob[i].rd_part = reinterpret_cast<float *>(rd);
+            rd += align256(sizeof(float) * 4 * n_tiles * pa[i].rows);
+        }
     }
     p.parts = parts;
     p.part_ld = part_ld;
-    p.part_stride = rows * part_ld;
+    p.part_stride = pa[0].rows * part_ld;
     p.status = st->status_ptr;
     p.timeout_ns = timeout_ns();
-    p.rows = static_cast<int>(rows);
     p.cols = static_cast<int>(cols);
     p.kc = static_cast<int>(kc);
     p.num_leaves = static_cast<int>(Lp);
-    p.m_tiles = static_cast<int>((rows + kBM - 1) / kBM);
-    p.n_tiles = static_cast<int>((cols + ops.bn - 1) / ops.bn);
-    choose_tile_order(p, ops.bn);
     p.force_timeout = g_force_timeout;
     if (blocks) {
         p.num_blocks = static_cast<int>(blocks->count);
@@ -466,8 +532,6 @@ det_gemm_status run(Variant v, Mat a, bool a_kmajor, Mat b, bool b_kmajor, Mat o
         p.num_blocks = static_cast<int>(nb);
     }
 
-    const int64_t units = tiles * parts;
-    if (units > (int64_t{1} << 31) - 1) return DET_GEMM_ERR_INVALID_ARG;
     const int grid = static_cast<int>(units < st->sm_count ? units : st->sm_count);
     if (fixed_scratch && static_cast<size_t>(grid) * static_cast<size_t>(ops.scratch_cta_bytes) > fixed_bytes) {
         std::snprintf(g_detail, sizeof g_detail,
@@ -479,11 +543,26 @@ det_gemm_status run(Variant v, Mat a, bool a_kmajor, Mat b, bool b_kmajor, Mat o
     const cudaError_t le = ops.launch(p, grid, stream);
     if (le != cudaSuccess) return fail_cuda(DET_GEMM_ERR_LAUNCH, le, "kernel launch");
     if (parts > 1) {
-        const cudaError_t me = launch_merge_parts(out.esize == 4, p.part_out, parts, p.rows, p.cols, part_ld,
-                                                  p.part_stride, const_cast<void *>(out.ptr), out.ld, stream);
+        const cudaError_t me = launch_merge_parts(pa[0].out.esize == 4, p.part_out, parts, p.prob[0].rows, p.cols,
+                                                  part_ld, p.part_stride, const_cast<void *>(pa[0].out.ptr),
+                                                  pa[0].out.ld, stream);
         if (me != cudaSuccess) return fail_cuda(DET_GEMM_ERR_LAUNCH, me, "merge launch");
     }
+    for (int i = 0; i < g; ++i) {
+        if (!pa[i].rowdot || pa[i].rows == 0) continue;
+        const cudaError_t re = launch_rowdot_reduce(p.prob[i].rd_part, p.prob[i].rows, p.n_tiles, pa[i].rowdot, stream);
+        if (re != cudaSuccess) return fail_cuda(DET_GEMM_ERR_LAUNCH, re, "row reduction launch");
+    }
     return DET_GEMM_OK;
+}
+
+// One plain GEMM (see run_problems).
+det_gemm_status run(Variant v, Mat a, bool a_kmajor, Mat b, bool b_kmajor, Mat out, int64_t rows, int64_t cols,
+                    int64_t kc, cudaStream_t stream, void *fixed_scratch = nullptr, size_t fixed_bytes = 0)
+{
+    if (rows < 0 || cols < 0 || kc < 0) return DET_GEMM_ERR_INVALID_ARG;
+    const ProblemArgs pa{a, b, out, rows, nullptr, 0, nullptr};
+    return run_problems(v, a_kmajor, b_kmajor, &pa, 1, cols, kc, stream, fixed_scratch, fixed_bytes);
 }
 
 Mat bf16(const void *p, int64_t r, int64_t c, int64_t ld) { return Mat{p, r, c, ld, 2}; }
@@ -604,6 +683,41 @@ det_gemm_status det_gemm_db_transposed(const det_gemm_bf16 *A, const det_gemm_bf
     if (M < 0 || N < 0 || K < 0) return DET_GEMM_ERR_INVALID_ARG;
     return run(kBf16MNMN, bf16(dC, M, N, lddc), false, bf16(A, M, K, lda), false, bf16(dBt, N, K, lddbt), N, K, M,
                reinterpret_cast<cudaStream_t>(stream));
+}
+
+det_gemm_status det_gemm_fwd_grouped(int G, const det_gemm_bf16 *const *A, const det_gemm_bf16 *const *B,
+                                     det_gemm_bf16 *const *C, const int64_t *M, int64_t N, int64_t K,
+                                     const int64_t *lda, const int64_t *ldb, const int64_t *ldc,
+                                     const det_gemm_bf16 *const *D, const int64_t *ldd, float *const *rowdot,
+                                     det_gemm_stream stream)
+{
+    if (G < 0 || N < 0 || K < 0) return DET_GEMM_ERR_INVALID_ARG;
+    if (G == 0) return DET_GEMM_OK;
+    if (!A || !B || !C || !M || !lda || !ldb || !ldc) return DET_GEMM_ERR_INVALID_ARG;
+    if (rowdot && (!D || !ldd)) return DET_GEMM_ERR_INVALID_ARG;
+    if (rowdot && N > int64_t{kMaxLeaves} * 128) {
+        for (int i = 0; i < G; ++i)
+            if (rowdot[i]) return DET_GEMM_ERR_INVALID_ARG;   // more column tiles than the tree covers
+    }
+    // Every argument is checked before anything is enqueued.
+    for (int i = 0; i < G; ++i) {
+        if (M[i] < 0) return DET_GEMM_ERR_INVALID_ARG;
+        if (rowdot && rowdot[i] && (!D[i] || ldd[i] < N)) return DET_GEMM_ERR_INVALID_ARG;
+    }
+    for (int base = 0; base < G; base += kMaxProblems) {
+        const int g = std::min(kMaxProblems, G - base);
+        ProblemArgs pa[kMaxProblems];
+        for (int j = 0; j < g; ++j) {
+            const int i = base + j;
+            const bool rd = rowdot && rowdot[i];
+            pa[j] = ProblemArgs{bf16(A[i], M[i], K, lda[i]), bf16(B[i], K, N, ldb[i]), bf16(C[i], M[i], N, ldc[i]),
+                                M[i], rd ? D[i] : nullptr, rd ? ldd[i] : 0, rd ? rowdot[i] : nullptr};
+        }
+        const det_gemm_status s =
+            run_problems(kBf16KMN, true, false, pa, g, N, K, reinterpret_cast<cudaStream_t>(stream));
+        if (s != DET_GEMM_OK) return s;
+    }
+    return DET_GEMM_OK;
 }
 
 det_gemm_status det_gemm_merge(const det_gemm_bf16 *const *parts, int n, det_gemm_bf16 *C, int64_t M, int64_t N,

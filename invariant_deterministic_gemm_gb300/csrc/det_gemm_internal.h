@@ -39,23 +39,40 @@ enum Variant {
 };
 
 // Everything a launch needs; passed by value as a __grid_constant__ param.
-struct Params {
+// One GEMM of a launch. A plain launch has one; a grouped launch
+// (det_gemm_fwd_grouped) has one per group, all with the same columns and
+// contraction.
+struct Problem {
     CUtensorMap tmap_a;           // "A operand": output rows x contraction
     CUtensorMap tmap_b;           // "B operand": contraction x output columns
     void *out;                    // row-major output, rows x cols
     long long ldo;                // output leading dimension, elements
+    float *rd_part;               // row reduction: per (column tile, quarter) partials [4 n_tiles][rows], or null
+    const uint16_t *rd_d;         // row reduction: the BF16 [rows, cols] operand D, row pitch rd_ldd
+    long long rd_ldd;
+    int rows;                     // output rows
+    int m_tiles;
+    int first_unit;               // index of this problem's first work unit in the launch
+    int stage_tx;                 // bytes one K-stage's TMA copies bring in (A box + B box)
+    int group;                    // tile order: tiles of this many row (or column) panels per group
+    int rows_fast;                // 1: row tiles vary fastest (A panels stay in L2), 0: column tiles
+};
+
+constexpr int kMaxProblems = 8;
+
+struct Params {
+    Problem prob[kMaxProblems];
+    int num_problems;
+    int units;                    // work units of the launch (all problems)
     void *scratch;                // deep-slot scratch: grid x VariantOps::scratch_cta_bytes
     int *status;                  // device status word (first int = code)
     unsigned long long timeout_ns;
-    int rows, cols, kc;
-    int stage_tx;                 // bytes one K-stage's TMA copies bring in (A box + B box)
+    int cols, kc;
+    int n_tiles;
     int num_leaves;               // leaves per work unit (the whole contraction when parts == 1)
     int parts;                    // contraction parts per tile: subtrees of the merge tree (1, 2, 4, 8)
     void *part_out;               // parts > 1: part p of tile rows/cols goes to part_out + p * part_stride
     long long part_ld, part_stride;   // elements
-    int m_tiles, n_tiles;
-    int group;                    // tile order: tiles of this many row (or column) panels per group
-    int rows_fast;                // 1: row tiles vary fastest (A panels stay in L2), 0: column tiles
     int force_timeout;
     int num_blocks;
     uint16_t blocks[kMaxLeaves];  // block schedule (see det_gemm_block_schedule)
@@ -79,6 +96,10 @@ cudaError_t launch_merge_parts(bool f32, const void *part, int parts, int rows, 
 // The same merge over n separately allocated parts (det_gemm_merge).
 cudaError_t launch_merge_list(bool f32, const void *const *parts, int n, int rows, int cols, long long ldp, void *out,
                               long long ldo, cudaStream_t stream);
+
+// Row reduction of a grouped launch: rowdot[i] = the partials of row i
+// (four per column tile, written by the kernel) combined in a fixed order.
+cudaError_t launch_rowdot_reduce(const float *part, int rows, int n_tiles, float *rowdot, cudaStream_t stream);
 
 // Batch-invariant RMSNorm (det_rmsnorm): one warp per row.
 struct RmsParams {

@@ -366,19 +366,27 @@ __device__ __forceinline__ uint32_t merge(uint32_t left, uint32_t right)
 // the CTAs running at the same time share the streamed operand's panel and
 // each streamed panel is read from DRAM once per group. The host picks the
 // order; only timing depends on it.
-__device__ __forceinline__ void tile_coords(int t, const Params &p, int &mt, int &nt)
+__device__ __forceinline__ void tile_coords(int t, const Problem &pb, int n_tiles, int &mt, int &nt)
 {
-    const int fast_tiles = p.rows_fast ? p.m_tiles : p.n_tiles;
-    const int slow_tiles = p.rows_fast ? p.n_tiles : p.m_tiles;
-    const int span = p.group * slow_tiles;
+    const int fast_tiles = pb.rows_fast ? pb.m_tiles : n_tiles;
+    const int slow_tiles = pb.rows_fast ? n_tiles : pb.m_tiles;
+    const int span = pb.group * slow_tiles;
     const int g = t / span;
-    const int first = g * p.group;
-    const int gf = min(p.group, fast_tiles - first);
+    const int first = g * pb.group;
+    const int gf = min(pb.group, fast_tiles - first);
     const int r = t - g * span;
     const int f = first + r % gf;
     const int o = r / gf;
-    mt = p.rows_fast ? f : o;
-    nt = p.rows_fast ? o : f;
+    mt = pb.rows_fast ? f : o;
+    nt = pb.rows_fast ? o : f;
+}
+
+// The problem (GEMM of a grouped launch) work unit u belongs to.
+__device__ __forceinline__ int problem_of(const Params &p, int u)
+{
+    int pi = 0;
+    while (pi + 1 < p.num_problems && u >= p.prob[pi + 1].first_unit) ++pi;
+    return pi;
 }
 
 // ------------------------------------------------------------- epilogue
@@ -394,6 +402,7 @@ struct EpiCtx {
     uint8_t *scratch;     // this thread's 64-byte line in the first global slot
     int lane;
     int row, col;         // first output element owned by this thread
+    int rows;             // rows of the output (the problem's)
     uint8_t *out;         // matrix the roots go to (the output, or this unit's part slab)
     long long ldo;        // its leading dimension, elements
 };
@@ -415,7 +424,7 @@ __device__ __forceinline__ void store_out(const Val &v, const Params &p, const E
 {
     using C = Cfg<F32>;
     constexpr int ES = F32 ? 4 : 2;
-    if (c.row >= p.rows) return;
+    if (c.row >= c.rows) return;
     const int ncols = p.cols - c.col;
     if (ncols <= 0) return;
     const bool full = ncols >= C::COLS;
@@ -439,6 +448,49 @@ __device__ __forceinline__ void store_out(const Val &v, const Params &p, const E
             asm volatile("st.global.u16 [%0], %1;" ::"l"(dst + 2 * j), "h"(w) : "memory");
         }
     }
+}
+
+// Row reduction of a grouped launch (bf16 variant): this thread's share of
+// rowdot[row] = sum over columns n of C[row, n] * D[row, n], for its 32
+// columns of column tile nt and quarter cq: the FP32 sum of the products
+// (exact: BF16 x BF16) in ascending column order, from +0 (+0 for a quarter
+// entirely past the last column). It goes to its own slot; no other thread
+// writes there, and the slots are combined later in a fixed order.
+__device__ __forceinline__ void row_partial(const Val &v, const Params &p, const Problem &pb, const EpiCtx &c,
+                                            int nt, int cq)
+{
+    if (c.row >= c.rows) return;
+    const int ncols = p.cols - c.col;
+    float s = 0.0f;
+    if (ncols > 0) {
+        const uint16_t *d = pb.rd_d + static_cast<long long>(c.row) * pb.rd_ldd + c.col;
+        uint32_t dw[16];
+        if (ncols >= 32) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const uint4 x = *reinterpret_cast<const uint4 *>(d + 8 * k);
+                dw[4 * k] = x.x;
+                dw[4 * k + 1] = x.y;
+                dw[4 * k + 2] = x.z;
+                dw[4 * k + 3] = x.w;
+            }
+        } else {
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                const uint32_t lo = 2 * k < ncols ? d[2 * k] : 0u;
+                const uint32_t hi = 2 * k + 1 < ncols ? d[2 * k + 1] : 0u;
+                dw[k] = lo | (hi << 16);
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            if (2 * k < ncols)
+                s = __fadd_rn(s, __fmul_rn(__uint_as_float(v[k] << 16), __uint_as_float(dw[k] << 16)));
+            if (2 * k + 1 < ncols)
+                s = __fadd_rn(s, __fmul_rn(__uint_as_float(v[k] & 0xFFFF0000u), __uint_as_float(dw[k] & 0xFFFF0000u)));
+        }
+    }
+    pb.rd_part[static_cast<long long>(nt * 4 + cq) * pb.rows + c.row] = s;
 }
 
 // Slot s >= 2 (TMEM, shared memory or global scratch) -> t.
@@ -580,7 +632,7 @@ __device__ __forceinline__ void stage_role(const Params &p, const Smem<F32> &S, 
     const uint32_t b_dst = S.sB + s * C::B_STAGE;
     const uint64_t a_st = sdesc(a_dst, A_LBO, 1024u);
     const uint64_t b_st = sdesc(b_dst, B_LBO, 1024u);
-    const int units = p.m_tiles * p.n_tiles * p.parts;   // work units: (tile, contraction part)
+    const int units = p.units;                        // work units: (problem, tile, contraction part)
     const int L = p.num_leaves;                       // leaves per unit
     const int KS = (L + 1) / 2;                       // K-stages per unit
     const int my_units = blockIdx.x < units ? (units - 1 - blockIdx.x) / gridDim.x + 1 : 0;
@@ -598,10 +650,12 @@ __device__ __forceinline__ void stage_role(const Params &p, const Smem<F32> &S, 
         const int tl = g / KS;                        // unit of this CTA
         const int ks = g - tl * KS;
         const int u = blockIdx.x + tl * gridDim.x;
-        const int t = u / p.parts;
-        const int part = u - t * p.parts;
+        const Problem &pb = p.prob[problem_of(p, u)];
+        const int ul = u - pb.first_unit;
+        const int t = ul / p.parts;
+        const int part = ul - t * p.parts;
         int mt, nt;
-        tile_coords(t, p, mt, nt);
+        tile_coords(t, pb, p.n_tiles, mt, nt);
         // ---- copy the stage into the slot once the MMAs of its last use are done
         bool got = wait_bounded(empty, round ^ 1u, S.abort_flag, p.status, p.timeout_ns, true);
         if (!__all_sync(0xFFFFFFFFu, got)) {
@@ -609,19 +663,19 @@ __device__ __forceinline__ void stage_role(const Params &p, const Smem<F32> &S, 
             break;
         }
         if (leader) {
-            mbar_arrive_expect_tx(full, static_cast<uint32_t>(p.stage_tx));
+            mbar_arrive_expect_tx(full, static_cast<uint32_t>(pb.stage_tx));
             const int k0 = part * L * kLeaf + ks * kBK, m0 = mt * kBM, n0 = nt * C::BN;
             if constexpr (A_MAJOR == kKMajor) {
-                tma_load_2d(a_dst, &p.tmap_a, full, k0, m0);
+                tma_load_2d(a_dst, &pb.tmap_a, full, k0, m0);
             } else {
-                tma_load_2d(a_dst, &p.tmap_a, full, m0, k0);
-                tma_load_2d(a_dst + 8192, &p.tmap_a, full, m0 + 64, k0);
+                tma_load_2d(a_dst, &pb.tmap_a, full, m0, k0);
+                tma_load_2d(a_dst + 8192, &pb.tmap_a, full, m0 + 64, k0);
             }
             if constexpr (B_MAJOR == kKMajor) {
-                tma_load_2d(b_dst, &p.tmap_b, full, k0, n0);
+                tma_load_2d(b_dst, &pb.tmap_b, full, k0, n0);
             } else {
 #pragma unroll
-                for (int b = 0; b < C::BN / 64; ++b) tma_load_2d(b_dst + 8192 * b, &p.tmap_b, full, n0 + 64 * b, k0);
+                for (int b = 0; b < C::BN / 64; ++b) tma_load_2d(b_dst + 8192 * b, &pb.tmap_b, full, n0 + 64 * b, k0);
             }
         }
         __syncwarp();
@@ -704,7 +758,7 @@ __device__ __forceinline__ void epilogue_role(const Params &p, const Smem<F32> &
     c.scratch = static_cast<uint8_t *>(p.scratch) + static_cast<long long>(blockIdx.x) * C::SCRATCH_CTA_BYTES +
                 (warp * 32 + lane) * C::LINE;
     c.lane = lane;
-    const int units = p.m_tiles * p.n_tiles * p.parts;
+    const int units = p.units;
     const int NB = p.num_blocks;
 
     Val A, B, Cc;
@@ -738,18 +792,21 @@ __device__ __forceinline__ void epilogue_role(const Params &p, const Smem<F32> &
     };
 
     for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
-        const int t = u / p.parts;
-        const int part = u - t * p.parts;
+        const Problem &pb = p.prob[problem_of(p, u)];
+        const int ul = u - pb.first_unit;
+        const int t = ul / p.parts;
+        const int part = ul - t * p.parts;
         int mt, nt;
-        tile_coords(t, p, mt, nt);
+        tile_coords(t, pb, p.n_tiles, mt, nt);
         c.row = mt * kBM + q * 32 + lane;
         c.col = nt * C::BN + cq * C::COLS;
+        c.rows = pb.rows;
         if (p.parts > 1) {
             c.out = static_cast<uint8_t *>(p.part_out) + part * p.part_stride * (F32 ? 4 : 2);
             c.ldo = p.part_ld;
         } else {
-            c.out = static_cast<uint8_t *>(p.out);
-            c.ldo = p.ldo;
+            c.out = static_cast<uint8_t *>(pb.out);
+            c.ldo = pb.ldo;
         }
         for (int b = 0; b < NB; ++b) {
             const uint32_t e = p.blocks[b];
@@ -777,8 +834,14 @@ __device__ __forceinline__ void epilogue_role(const Params &p, const Smem<F32> &
                 for (int i = 0; i < 16; ++i) A[i] = merge<F32>(B[i], A[i]);
             }
             const int st = static_cast<int>(e >> 12);
-            if (st == kSlotRoot) store_out<F32>(A, p, c);
-            else store_slot<F32>(st, A, c);
+            if (st == kSlotRoot) {
+                store_out<F32>(A, p, c);
+                if constexpr (!F32) {
+                    if (pb.rd_part != nullptr) row_partial(A, p, pb, c, nt, cq);
+                }
+            } else {
+                store_slot<F32>(st, A, c);
+            }
         }
     }
 }
@@ -822,8 +885,10 @@ __global__ void __launch_bounds__(kThreads, 1) det_gemm_kernel(const __grid_cons
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == kFirstStageWarp && lane == 0) {
-        tmap_prefetch(&p.tmap_a);
-        tmap_prefetch(&p.tmap_b);
+        for (int pi = 0; pi < p.num_problems; ++pi) {
+            tmap_prefetch(&p.prob[pi].tmap_a);
+            tmap_prefetch(&p.prob[pi].tmap_b);
+        }
     }
     if (warp == kTmemWarp) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(

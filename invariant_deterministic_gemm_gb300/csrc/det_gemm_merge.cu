@@ -11,6 +11,7 @@
 // ((p0 + p1) + (p2 + p3)) for four parts, each add rounded once (BF16 adds
 // for the bf16 variant, FP32 adds for the fp32 one). The result is the same
 // bits as the unsplit launch; only the CTA doing the work differs.
+#include "det_gemm.h"
 #include "det_gemm_kernel.cuh"
 
 namespace detg {
@@ -76,6 +77,44 @@ cudaError_t launch_merge(bool f32, const PartPtrs &at, int parts, int rows, int 
     return cudaGetLastError();
 }
 
+// Row reduction of a grouped launch. The kernel leaves, for every row i,
+// one FP32 partial per (column tile t, quarter q): part[(4 t + q) rows + i].
+// rowdot[i] combines them in a fixed order: each tile's four quarters as
+// ((q0 + q1) + (q2 + q3)), then the tiles by the same mid-split tree of FP32
+// adds the contraction uses, walked with its per-leaf schedule (pending left
+// children in slots). No atomics: the same bits every run, whichever CTA
+// wrote which partial first (Megatron Core notes, "Kernel redesign: the
+// grouped-GEMM epilogue": private per-tile slots, then a fixed tree).
+struct RowdotParams {
+    const float *part;
+    float *rowdot;
+    int rows, n_tiles;
+    uint16_t sched[kMaxLeaves];
+};
+
+__global__ void rowdot_reduce_kernel(const __grid_constant__ RowdotParams p)
+{
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= p.rows) return;
+    float slot[kMaxSlots];
+    float root = 0.0f;
+    const long long stride = p.rows;
+    for (int t = 0; t < p.n_tiles; ++t) {
+        const float *q = p.part + static_cast<long long>(4 * t) * stride + i;
+        float v = __fadd_rn(__fadd_rn(q[0], q[stride]), __fadd_rn(q[2 * stride], q[3 * stride]));
+        const uint32_t e = p.sched[t];
+#pragma unroll
+        for (int s = 0; s < kMaxSlots; ++s)
+            if ((e >> s) & 1u) v = __fadd_rn(slot[s], v);
+        const uint32_t dst = e >> 12;
+#pragma unroll
+        for (int s = 0; s < kMaxSlots; ++s)
+            if (dst == static_cast<uint32_t>(s)) slot[s] = v;
+        if (dst == kSlotRoot) root = v;
+    }
+    p.rowdot[i] = root;
+}
+
 }  // namespace
 
 cudaError_t launch_merge_parts(bool f32, const void *part, int parts, int rows, int cols, long long part_ld,
@@ -94,6 +133,21 @@ cudaError_t launch_merge_list(bool f32, const void *const *parts, int n, int row
     PartPtrs at{};
     for (int i = 0; i < n; ++i) at.p[i] = static_cast<const uint8_t *>(parts[i]);
     return launch_merge(f32, at, n, rows, cols, ldp, out, ldo, stream);
+}
+
+cudaError_t launch_rowdot_reduce(const float *part, int rows, int n_tiles, float *rowdot, cudaStream_t stream)
+{
+    if (rows <= 0) return cudaSuccess;
+    if (n_tiles < 1 || n_tiles > kMaxLeaves) return cudaErrorInvalidValue;
+    RowdotParams p;
+    p.part = part;
+    p.rowdot = rowdot;
+    p.rows = rows;
+    p.n_tiles = n_tiles;
+    if (det_gemm_tree_schedule(n_tiles, p.sched) != DET_GEMM_OK) return cudaErrorInvalidValue;
+    const int threads = 128;
+    rowdot_reduce_kernel<<<(rows + threads - 1) / threads, threads, 0, stream>>>(p);
+    return cudaGetLastError();
 }
 
 }  // namespace detg

@@ -248,3 +248,28 @@ def test_rmsnorm_argument_errors_are_returned_before_any_launch(dg):
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU answer")
 def test_rmsnorm_in_place_passes_the_checks_and_needs_a_gpu(dg):
     assert rms_call(dg, P, P * 8, P, 4, 8, 1e-6, 8, 8) == 4
+
+
+# ---------------------------------------------------------- grouped GEMM
+
+def grouped_call(dg, G, A, B, C, M, N, K, lda, ldb, ldc, D=None, ldd=None, rd=None):
+    arr = lambda xs: (ctypes.c_void_p * len(xs))(*xs) if xs is not None else None
+    i64s = lambda xs: (ctypes.c_int64 * len(xs))(*xs) if xs is not None else None
+    return dg.lib().det_gemm_fwd_grouped(G, arr(A), arr(B), arr(C), i64s(M), N, K, i64s(lda), i64s(ldb),
+                                         i64s(ldc), arr(D), i64s(ldd), arr(rd), None)
+
+
+def test_grouped_argument_errors_are_returned_before_any_launch(dg):
+    A, B, C = [P, P * 2], [P * 4, P * 8], [P * 16, P * 32]
+    ok = dict(M=[4, 4], N=8, K=8, lda=[8, 8], ldb=[8, 8], ldc=[8, 8])
+    assert grouped_call(dg, 0, None, None, None, None, 8, 8, None, None, None) == 0     # no groups
+    assert grouped_call(dg, -1, A, B, C, ok["M"], 8, 8, ok["lda"], ok["ldb"], ok["ldc"]) == 1
+    assert grouped_call(dg, 2, None, B, C, ok["M"], 8, 8, ok["lda"], ok["ldb"], ok["ldc"]) == 1
+    assert grouped_call(dg, 2, A, B, C, [4, -1], 8, 8, ok["lda"], ok["ldb"], ok["ldc"]) == 1
+    assert grouped_call(dg, 2, A, B, C, ok["M"], 8, 32769, [32776] * 2, [8, 8], [8, 8]) == 2
+    assert grouped_call(dg, 2, [P + 2, P * 2], B, C, ok["M"], 8, 8, ok["lda"], ok["ldb"], ok["ldc"]) == 3
+    assert grouped_call(dg, 2, A, B, [P * 16, P * 16], ok["M"], 8, 8, ok["lda"], ok["ldb"], ok["ldc"]) == 1
+    # a row reduction without its operand
+    assert grouped_call(dg, 2, A, B, C, ok["M"], 8, 8, ok["lda"], ok["ldb"], ok["ldc"],
+                        D=[0, 0], ldd=[8, 8], rd=[P * 64, 0]) == 1
+    assert grouped_call(dg, 2, A, B, C, ok["M"], 8, 8, ok["lda"], ok["ldb"], ok["ldc"], rd=[P * 64, 0]) == 1
