@@ -563,6 +563,24 @@ def configs_arm(args):
     report("long_k [4096,32768]@[32768,4096]", ms, 2.0 * 4096 * 32768 * 4096,
            2 * (2 * 4096 * 32768 + 4096 * 4096), tms)
     del A, B
+    # mixture-of-experts: 8 experts of an MLP up projection (4096 -> 14336),
+    # 8192 routed tokens split unevenly, one grouped launch vs one launch per
+    # expert; with the fixed-order row reduction against a second operand
+    counts = [2048, 1536, 1280, 1024, 896, 768, 384, 256]
+    Ae = [W.randn_bf16((m, 4096), W.STD_ACT, W.seed_for(W.MLP, W.T_A) + 300 + g).to(dev) for g, m in enumerate(counts)]
+    Be = [W.randn_bf16((4096, 1792), W.STD_W, W.seed_for(W.MLP, W.T_B) + 300 + g).to(dev) for g in range(8)]
+    De = [W.randn_bf16((m, 1792), W.STD_DC, W.seed_for(W.MLP, W.T_DC) + 300 + g).to(dev) for g, m in enumerate(counts)]
+    Ce = [torch.empty((m, 1792), dtype=torch.bfloat16, device=dev) for m in counts]
+    flop = 2.0 * sum(counts) * 4096 * 1792
+    ms = timeit(lambda: dg.det_gemm_fwd_grouped(Ae, Be, outs=Ce), iters=10, flush=flush)
+    ms_loop = timeit(lambda: [dg.det_gemm_fwd(a, b, out=c) for a, b, c in zip(Ae, Be, Ce)], iters=10, flush=flush)
+    ms_rd = timeit(lambda: dg.det_gemm_fwd_grouped(Ae, Be, outs=Ce, D=De), iters=10, flush=flush)
+    print(json.dumps({"workload": "moe grouped 8 experts, 8192 tokens [m_g,4096]@[4096,1792]", "ms": round(ms, 4),
+                      "tflops": round(flop / (ms * 1e-3) / 1e12, 1),
+                      "one_launch_per_expert_ms": round(ms_loop, 4), "with_row_reduction_ms": round(ms_rd, 4),
+                      "roofline_frac": round(flop / (pk["bf16_burst"] * 1e12) / (ms * 1e-3), 4), "bound": "tensor",
+                      "peaks": "%s burst bf16 %.0f TFLOP/s" % (pk["source"], pk["bf16_burst"])}), flush=True)
+    del Ae, Be, De, Ce
     # batch-invariant RMSNorm over the MLP activations (HBM-bound: read x and
     # w, write y)
     x = W.randn_bf16((8192, 4096), W.STD_ACT, W.seed_for(W.MLP, W.T_A)).to(dev)

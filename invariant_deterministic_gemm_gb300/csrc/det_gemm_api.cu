@@ -71,6 +71,7 @@ VariantOps variant_ops(Variant v)
     case kBf16MNMN: return ops_bf16_mnmn();
     case kF32KMN: return ops_f32_kmn();
     case kF32KK: return ops_f32_kk();
+    case kBf16KMNGrouped: return ops_bf16_kmn_grouped();
     default: return VariantOps{};
     }
 }
@@ -713,8 +714,11 @@ det_gemm_status det_gemm_fwd_grouped(int G, const det_gemm_bf16 *const *A, const
             pa[j] = ProblemArgs{bf16(A[i], M[i], K, lda[i]), bf16(B[i], K, N, ldb[i]), bf16(C[i], M[i], N, ldc[i]),
                                 M[i], rd ? D[i] : nullptr, rd ? ldd[i] : 0, rd ? rowdot[i] : nullptr};
         }
-        const det_gemm_status s =
-            run_problems(kBf16KMN, true, false, pa, g, N, K, reinterpret_cast<cudaStream_t>(stream));
+        // One problem without a row reduction is a plain launch (same bits).
+        bool reduce = false;
+        for (int j = 0; j < g; ++j) reduce = reduce || pa[j].rowdot != nullptr;
+        const Variant v = (g > 1 || reduce) ? kBf16KMNGrouped : kBf16KMN;
+        const det_gemm_status s = run_problems(v, true, false, pa, g, N, K, reinterpret_cast<cudaStream_t>(stream));
         if (s != DET_GEMM_OK) return s;
     }
     return DET_GEMM_OK;

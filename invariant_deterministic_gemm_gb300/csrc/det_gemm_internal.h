@@ -35,6 +35,7 @@ enum Variant {
     kBf16MNMN,      // db, db_transposed: both MN-major
     kF32KMN,        // fwd_fp32
     kF32KK,         // fwd_fp32 with a [N,K] weight
+    kBf16KMNGrouped,   // fwd_grouped: several problems per launch, optional row reduction
     kVariantCount
 };
 
@@ -121,6 +122,7 @@ VariantOps ops_bf16_kk();
 VariantOps ops_bf16_mnmn();
 VariantOps ops_f32_kmn();
 VariantOps ops_f32_kk();
+VariantOps ops_bf16_kmn_grouped();
 
 // det_gemm_fwd with a caller-provided scratch buffer: nothing is allocated,
 // device or host. Returns a det_gemm_status.

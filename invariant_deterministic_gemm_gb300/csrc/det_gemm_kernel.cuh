@@ -609,7 +609,7 @@ struct Smem {
 // barrier phase pair; the turn order guarantees that for the accumulator
 // barriers, and slot ownership for the ring barriers. The warp runs the loop
 // and the waits; one elected lane issues copies, MMAs and commits.
-template <int A_MAJOR, int B_MAJOR, bool F32>
+template <int A_MAJOR, int B_MAJOR, bool F32, bool GROUPED>
 __device__ __forceinline__ void stage_role(const Params &p, const Smem<F32> &S, int j)
 {
     using C = Cfg<F32>;
@@ -650,7 +650,7 @@ __device__ __forceinline__ void stage_role(const Params &p, const Smem<F32> &S, 
         const int tl = g / KS;                        // unit of this CTA
         const int ks = g - tl * KS;
         const int u = blockIdx.x + tl * gridDim.x;
-        const Problem &pb = p.prob[problem_of(p, u)];
+        const Problem &pb = p.prob[GROUPED ? problem_of(p, u) : 0];
         const int ul = u - pb.first_unit;
         const int t = ul / p.parts;
         const int part = ul - t * p.parts;
@@ -744,7 +744,7 @@ __device__ __forceinline__ void stage_role(const Params &p, const Smem<F32> &S, 
 // entry names and parked (one TMEM or scratch access) or written out as the
 // root. The code stays small so that the loop, rare branches included,
 // lives in the instruction cache.
-template <bool F32>
+template <bool F32, bool GROUPED>
 __device__ __forceinline__ void epilogue_role(const Params &p, const Smem<F32> &S, int warp, int lane)
 {
     using C = Cfg<F32>;
@@ -792,7 +792,7 @@ __device__ __forceinline__ void epilogue_role(const Params &p, const Smem<F32> &
     };
 
     for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
-        const Problem &pb = p.prob[problem_of(p, u)];
+        const Problem &pb = p.prob[GROUPED ? problem_of(p, u) : 0];
         const int ul = u - pb.first_unit;
         const int t = ul / p.parts;
         const int part = ul - t * p.parts;
@@ -836,7 +836,7 @@ __device__ __forceinline__ void epilogue_role(const Params &p, const Smem<F32> &
             const int st = static_cast<int>(e >> 12);
             if (st == kSlotRoot) {
                 store_out<F32>(A, p, c);
-                if constexpr (!F32) {
+                if constexpr (GROUPED && !F32) {
                     if (pb.rd_part != nullptr) row_partial(A, p, pb, c, nt, cq);
                 }
             } else {
@@ -846,7 +846,7 @@ __device__ __forceinline__ void epilogue_role(const Params &p, const Smem<F32> &
     }
 }
 
-template <int A_MAJOR, int B_MAJOR, bool F32>
+template <int A_MAJOR, int B_MAJOR, bool F32, bool GROUPED>
 __global__ void __launch_bounds__(kThreads, 1) det_gemm_kernel(const __grid_constant__ Params p)
 {
     using C = Cfg<F32>;
@@ -885,7 +885,7 @@ __global__ void __launch_bounds__(kThreads, 1) det_gemm_kernel(const __grid_cons
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == kFirstStageWarp && lane == 0) {
-        for (int pi = 0; pi < p.num_problems; ++pi) {
+        for (int pi = 0; pi < (GROUPED ? p.num_problems : 1); ++pi) {
             tmap_prefetch(&p.prob[pi].tmap_a);
             tmap_prefetch(&p.prob[pi].tmap_b);
         }
@@ -910,10 +910,10 @@ __global__ void __launch_bounds__(kThreads, 1) det_gemm_kernel(const __grid_cons
     static_assert(kProdRegs * 128 + kEpiRegs * 32 * kEpiWarps <= kLaunchRegs * kThreads, "register split");
     if (warp < kEpiWarps) {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kEpiRegs));
-        epilogue_role<F32>(p, S, warp, lane);
+        epilogue_role<F32, GROUPED>(p, S, warp, lane);
     } else {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kProdRegs));
-        stage_role<A_MAJOR, B_MAJOR, F32>(p, S, warp - kFirstStageWarp);
+        stage_role<A_MAJOR, B_MAJOR, F32, GROUPED>(p, S, warp - kFirstStageWarp);
     }
 
     // ---- teardown
@@ -929,11 +929,11 @@ __global__ void __launch_bounds__(kThreads, 1) det_gemm_kernel(const __grid_cons
 
 // --------------------------------------------------------- host launcher
 
-template <int A_MAJOR, int B_MAJOR, bool F32>
+template <int A_MAJOR, int B_MAJOR, bool F32, bool GROUPED = false>
 struct Launcher {
     static cudaError_t prepare(int *num_regs)
     {
-        auto fn = det_gemm_kernel<A_MAJOR, B_MAJOR, F32>;
+        auto fn = det_gemm_kernel<A_MAJOR, B_MAJOR, F32, GROUPED>;
         cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              Cfg<F32>::SMEM_BYTES);
         if (e != cudaSuccess) return e;
@@ -945,7 +945,7 @@ struct Launcher {
     }
     static cudaError_t launch(const Params &p, int grid, cudaStream_t stream)
     {
-        det_gemm_kernel<A_MAJOR, B_MAJOR, F32><<<grid, kThreads, Cfg<F32>::SMEM_BYTES, stream>>>(p);
+        det_gemm_kernel<A_MAJOR, B_MAJOR, F32, GROUPED><<<grid, kThreads, Cfg<F32>::SMEM_BYTES, stream>>>(p);
         return cudaGetLastError();
     }
     static VariantOps ops()
