@@ -18,6 +18,11 @@
  *   it. When L is even, a contiguous half-K product is one child of the root,
  *   so bf16(first_half + second_half) equals the full product bit for bit.
  *
+ *   How an output is tiled is an implementation choice that never shows in
+ *   the bits: BF16 launches with at most 64 output rows (fwd,
+ *   fwd_rhs_transposed, da) run a transposed tile whose MMA lanes carry the
+ *   output columns, and produce the same bits as the plain tile.
+ *
  *   Within a leaf the FP32 sum is formed by the tensor core; its internal
  *   summation order differs from a sequential loop, so a leaf can differ from
  *   a sequential FP32 leaf by one BF16 unit when it lies next to a rounding

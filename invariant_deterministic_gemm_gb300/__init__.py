@@ -66,6 +66,8 @@ class DetGemmError(RuntimeError):
 def lib() -> ctypes.CDLL:
     """The loaded C library (raises if it was not built)."""
     global _lib
+    if _lib is not None:
+        return _lib
     with _lock:
         if _lib is not None:
             return _lib
@@ -110,9 +112,20 @@ def status_string(status: int) -> str:
     return lib().det_gemm_status_string(int(status)).decode()
 
 
+# The current stream's raw handle without building a torch.cuda.Stream object
+# (a measurable part of a decode-sized call); the public route otherwise.
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
 def _stream_handle(stream) -> int:
-    s = torch.cuda.current_stream() if stream is None else stream
-    return int(s.cuda_stream)
+    if stream is not None:
+        return int(stream.cuda_stream)
+    if _raw_stream is not None:
+        return int(_raw_stream(torch.cuda.current_device()))
+    return int(torch.cuda.current_stream().cuda_stream)
+
+
+_ELEM_SIZE = {torch.bfloat16: 2, torch.float32: 4}
 
 
 def _mat(t: torch.Tensor, name: str, dtype=torch.bfloat16):
@@ -122,7 +135,7 @@ def _mat(t: torch.Tensor, name: str, dtype=torch.bfloat16):
         raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
     if t.dim() != 2:
         raise ValueError("%s must be 2-D, got shape %s" % (name, tuple(t.shape)))
-    if t.device.type != "cuda":
+    if not t.is_cuda:
         raise ValueError("%s must be a CUDA tensor" % name)
     if t.shape[1] > 1 and t.stride(1) != 1:
         raise ValueError("%s must be row-major with unit column stride" % name)
@@ -132,7 +145,7 @@ def _mat(t: torch.Tensor, name: str, dtype=torch.bfloat16):
         # One row: the leading dimension is never used to address anything,
         # so any value that meets the library's 16-byte pitch rule will do.
         ld = max(t.shape[1], t.stride(0))
-        per16 = 16 // t.element_size()
+        per16 = 16 // _ELEM_SIZE[dtype]
         ld = (ld + per16 - 1) // per16 * per16
     return t.data_ptr(), int(ld)
 
@@ -141,16 +154,24 @@ def _out(out, rows, cols, dtype, like: torch.Tensor):
     if out is None:
         # Pad the row pitch to 16 bytes (the library's rule) and hand back
         # the [rows, cols] view.
-        per16 = 16 // torch.empty((), dtype=dtype).element_size()
+        per16 = 16 // _ELEM_SIZE[dtype]
         ld = max(per16, (cols + per16 - 1) // per16 * per16)
+        if ld == cols:
+            return torch.empty((rows, cols), dtype=dtype, device=like.device)
         return torch.empty((rows, ld), dtype=dtype, device=like.device)[:, :cols]
     if tuple(out.shape) != (rows, cols):
         raise ValueError("out must have shape %s, got %s" % ((rows, cols), tuple(out.shape)))
     return out
 
 
+_fns = {}
+
+
 def _call(name: str, x_ptr, y_ptr, out_ptr, M, N, K, ldx, ldy, ldo, stream):
-    st = getattr(lib(), name)(x_ptr, y_ptr, out_ptr, M, N, K, ldx, ldy, ldo, _stream_handle(stream))
+    fn = _fns.get(name)
+    if fn is None:
+        fn = _fns[name] = getattr(lib(), name)
+    st = fn(x_ptr, y_ptr, out_ptr, M, N, K, ldx, ldy, ldo, _stream_handle(stream))
     if st != OK:
         raise DetGemmError(st, name)
 

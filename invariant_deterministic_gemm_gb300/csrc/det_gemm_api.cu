@@ -72,6 +72,8 @@ VariantOps variant_ops(Variant v)
     case kF32KMN: return ops_f32_kmn();
     case kF32KK: return ops_f32_kk();
     case kBf16KMNGrouped: return ops_bf16_kmn_grouped();
+    case kBf16SwapMNK: return ops_bf16_swap_mnk();
+    case kBf16SwapKK: return ops_bf16_swap_kk();
     default: return VariantOps{};
     }
 }
@@ -260,12 +262,12 @@ det_gemm_status prepare_variant(DeviceState *st, Variant v)
         cudaError_t e = ops.prepare ? ops.prepare(&regs) : cudaErrorInvalidDeviceFunction;
         if (e != cudaSuccess) {
             st->prepare_status[v] = fail_cuda(DET_GEMM_ERR_LAUNCH, e, "kernel attributes");
-        } else if (regs != kLaunchRegs) {
+        } else if (ops.split_regs != 0 && regs != ops.split_regs) {
             // setmaxnreg redistributes exactly the registers the CTA is
             // launched with; any other launch allocation would make the
             // epilogue's request unsatisfiable or waste registers.
             std::snprintf(g_detail, sizeof g_detail, "kernel compiled for %d registers per thread, expected %d",
-                          regs, kLaunchRegs);
+                          regs, ops.split_regs);
             st->prepare_status[v] = DET_GEMM_ERR_LAUNCH;
         }
     }
@@ -469,15 +471,19 @@ det_gemm_status run_problems(Variant v, bool a_kmajor, bool b_kmajor, const Prob
         // of A, and those rows are never stored.
         const int a_box_rows =
             (a_kmajor && q.rows < kBM) ? static_cast<int>(std::max<int64_t>(16, (q.rows + 7) / 8 * 8)) : kBM;
+        // The same for a K-major B operand with fewer columns than a tile
+        // (the transposed tile's few output rows).
+        const int b_box_rows =
+            (b_kmajor && cols < ops.bn) ? static_cast<int>(std::max<int64_t>(16, (cols + 7) / 8 * 8)) : ops.bn;
         bool ok;
         if (a_kmajor) ok = encode(&pb.tmap_a, q.a.ptr, kc, q.rows, q.a.ld, 64, static_cast<uint32_t>(a_box_rows));
         else ok = encode(&pb.tmap_a, q.a.ptr, q.rows, kc, q.a.ld, 64, 64);
         if (ok) {
-            if (b_kmajor) ok = encode(&pb.tmap_b, q.b.ptr, kc, cols, q.b.ld, 64, ops.bn);
+            if (b_kmajor) ok = encode(&pb.tmap_b, q.b.ptr, kc, cols, q.b.ld, 64, static_cast<uint32_t>(b_box_rows));
             else ok = encode(&pb.tmap_b, q.b.ptr, cols, kc, q.b.ld, 64, 64);
         }
         if (!ok) return DET_GEMM_ERR_LAUNCH;
-        pb.stage_tx = a_box_rows * kBK * 2 + ops.bn * kBK * 2;
+        pb.stage_tx = a_box_rows * kBK * 2 + b_box_rows * kBK * 2;
         pb.out = const_cast<void *>(q.out.ptr);
         pb.ldo = q.out.ld;
         choose_tile_order(pb, q.rows, cols, kc, ops.bn, p.n_tiles);
@@ -489,11 +495,14 @@ det_gemm_status run_problems(Variant v, bool a_kmajor, bool b_kmajor, const Prob
     }
     if (units > (int64_t{1} << 31) - 1) return DET_GEMM_ERR_INVALID_ARG;
     p.units = static_cast<int>(units);
-    // A split launch's part slabs: rows x part_ld each, the row pitch a
-    // multiple of 8 elements (16 bytes).
-    const int64_t part_ld = (cols + 7) / 8 * 8;
+    // A split launch's part slabs: laid out like the output (out_rows x
+    // part_ld each, the row pitch a multiple of 8 elements, 16 bytes). The
+    // transposed tile's kernel rows are the output's columns.
+    const int64_t out_rows = ops.swap ? cols : pa[0].rows;
+    const int64_t out_cols = ops.swap ? pa[0].rows : cols;
+    const int64_t part_ld = (out_cols + 7) / 8 * 8;
     const size_t part_bytes =
-        parts > 1 ? align256(static_cast<size_t>(parts) * pa[0].rows * part_ld * pa[0].out.esize) : 0;
+        parts > 1 ? align256(static_cast<size_t>(parts) * out_rows * part_ld * pa[0].out.esize) : 0;
     if (fixed_scratch) {
         p.scratch = fixed_scratch;
     } else {
@@ -517,7 +526,7 @@ det_gemm_status run_problems(Variant v, bool a_kmajor, bool b_kmajor, const Prob
     }
     p.parts = parts;
     p.part_ld = part_ld;
-    p.part_stride = pa[0].rows * part_ld;
+    p.part_stride = out_rows * part_ld;
     p.status = st->status_ptr;
     p.timeout_ns = timeout_ns();
     p.cols = static_cast<int>(cols);
@@ -544,9 +553,9 @@ det_gemm_status run_problems(Variant v, bool a_kmajor, bool b_kmajor, const Prob
     const cudaError_t le = ops.launch(p, grid, stream);
     if (le != cudaSuccess) return fail_cuda(DET_GEMM_ERR_LAUNCH, le, "kernel launch");
     if (parts > 1) {
-        const cudaError_t me = launch_merge_parts(pa[0].out.esize == 4, p.part_out, parts, p.prob[0].rows, p.cols,
-                                                  part_ld, p.part_stride, const_cast<void *>(pa[0].out.ptr),
-                                                  pa[0].out.ld, stream);
+        const cudaError_t me = launch_merge_parts(pa[0].out.esize == 4, p.part_out, parts, static_cast<int>(out_rows),
+                                                  static_cast<int>(out_cols), part_ld, p.part_stride,
+                                                  const_cast<void *>(pa[0].out.ptr), pa[0].out.ld, stream);
         if (me != cudaSuccess) return fail_cuda(DET_GEMM_ERR_LAUNCH, me, "merge launch");
     }
     for (int i = 0; i < g; ++i) {
@@ -562,6 +571,15 @@ det_gemm_status run(Variant v, Mat a, bool a_kmajor, Mat b, bool b_kmajor, Mat o
                     int64_t kc, cudaStream_t stream, void *fixed_scratch = nullptr, size_t fixed_bytes = 0)
 {
     if (rows < 0 || cols < 0 || kc < 0) return DET_GEMM_ERR_INVALID_ARG;
+    // A BF16 launch with a K-major A and few output rows takes the
+    // transposed tile: the kernel's A operand is b (its rows are the
+    // output's columns), its B operand is a, and the kernel stores
+    // transposed. Same leaves, same tree, same bits as the plain tile.
+    if ((v == kBf16KMN || v == kBf16KK) && a_kmajor && rows >= 1 && rows <= kSwapMaxRows && cols > 0 && kc > 0) {
+        const ProblemArgs sw{b, a, out, cols, nullptr, 0, nullptr};
+        return run_problems(b_kmajor ? kBf16SwapKK : kBf16SwapMNK, b_kmajor, true, &sw, 1, rows, kc, stream,
+                            fixed_scratch, fixed_bytes);
+    }
     const ProblemArgs pa{a, b, out, rows, nullptr, 0, nullptr};
     return run_problems(v, a_kmajor, b_kmajor, &pa, 1, cols, kc, stream, fixed_scratch, fixed_bytes);
 }

@@ -16,12 +16,8 @@ constexpr int kSlotRoot = 15;             // schedule "store" value for the root
 constexpr int kMaxSlots = 10;             // ceil(log2(kMaxLeaves)) pending partials
 constexpr int kBM = 128;                  // output rows per tile (one TMEM lane per row)
 constexpr int kBK = 64;                   // contraction elements per shared-memory stage (two leaves)
-constexpr int kEpiWarps = 16;             // four per scheduler, one TMEM lane quadrant each
-constexpr int kFirstStageWarp = 16;       // warps 16..19: TMA copies and MMAs of the K-stages
-constexpr int kStageWarps = 4;            // one per SM sub-partition
-constexpr int kTmemWarp = 17;             // allocates and frees TMEM
-constexpr int kThreads = 32 * (kEpiWarps + kStageWarps);
-constexpr int kLaunchRegs = 96;           // registers per thread at launch (65536 / 640, rounded down to 8)
+constexpr int kStageWarps = 4;            // TMA copies and MMAs of the K-stages: one per SM sub-partition
+constexpr int kLaunchRegs = 96;           // registers per thread at launch of the plain tile's 640 threads
 constexpr int kProdRegs = 40;             // stage warpgroup after setmaxnreg
 constexpr int kEpiRegs = 104;             // epilogue warpgroups after setmaxnreg
 
@@ -36,6 +32,8 @@ enum Variant {
     kF32KMN,        // fwd_fp32
     kF32KK,         // fwd_fp32 with a [N,K] weight
     kBf16KMNGrouped,   // fwd_grouped: several problems per launch, optional row reduction
+    kBf16SwapMNK,   // fwd with at most kSwapMaxRows rows: transposed tile, A = B[K,N] (MN-major), B = A[M,K]
+    kBf16SwapKK,    // fwd_rhs_transposed, da with few rows: transposed tile, both K-major
     kVariantCount
 };
 
@@ -86,7 +84,12 @@ struct VariantOps {
     int bn;                       // output columns per tile
     int smem_bytes;
     int scratch_cta_bytes;        // global scratch each CTA needs for its deep slots
+    int split_regs;               // registers per thread the kernel must be built with (0: no register split)
+    bool swap;                    // transposed tile: the kernel's rows are the output's columns
 };
+
+// Output rows up to which a BF16 launch uses the transposed tile.
+constexpr int kSwapMaxRows = 64;
 
 // Merges the `parts` partial results of a split launch into the output with
 // the top levels of the merge tree (parts is a power of two; part p is leaf
@@ -123,6 +126,8 @@ VariantOps ops_bf16_mnmn();
 VariantOps ops_f32_kmn();
 VariantOps ops_f32_kk();
 VariantOps ops_bf16_kmn_grouped();
+VariantOps ops_bf16_swap_mnk();
+VariantOps ops_bf16_swap_kk();
 
 // det_gemm_fwd with a caller-provided scratch buffer: nothing is allocated,
 // device or host. Returns a det_gemm_status.

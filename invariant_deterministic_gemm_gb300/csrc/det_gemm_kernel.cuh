@@ -23,6 +23,14 @@
 //              stage's MMAs; MMA issue is handed from warp to warp in stage
 //              order (turn barriers). Warp 17 also allocates and frees TMEM.
 //
+// Transposed tile (launches with at most 64 output rows, BF16 out): the
+// MMA's A operand is the weight, so its 128 TMEM lanes are 128 output
+// columns, and its N side (64) holds the rows. 384 threads: warps 0-7
+// epilogue, two per scheduler, each owning one output column per lane and
+// 32 rows; warps 8-11 stage warps. The accumulators and all eight pending
+// slots fit in TMEM, and the stage warps also prefetch the weight tiles of
+// later stages into L2.
+//
 // Per tile: 64-wide K stages (two leaves) of the A and B operand tiles go
 // through a ring of four swizzled shared-memory slots. For leaf l the stage
 // warp issues two K=16 MMAs into accumulator buffer l % NACC (the first one
@@ -53,31 +61,52 @@
 namespace detg {
 
 constexpr int kStatusTimeout = 6;   // DET_GEMM_ERR_TIMEOUT
+constexpr int kPrefetchRounds = 2;  // transposed tile: L2 prefetch distance, in rounds of the stage ring
 
 
 // ------------------------------------------------------------------ config
 
-template <bool F32>
+// SWAP: the transposed tile for launches with few output rows (at most
+// BN of them). The MMA's 128 lanes then carry 128 output columns and its N
+// side the rows, so the epilogue's work follows the rows that exist instead
+// of a 128-row tile that is mostly padding. Every output element still comes
+// out of the same leaves and the same tree: the tensor core forms the same
+// products and FP32 leaf sums whichever operand is A (the bits are checked
+// against the plain tile on the GPU).
+template <bool F32, bool SWAP = false>
 struct Cfg {
-    static constexpr int BN = F32 ? 64 : 128;           // output columns per tile
-    static constexpr int NACC = F32 ? 4 : 3;            // TMEM accumulator buffers
+    static constexpr int EPI_WARPS = SWAP ? 8 : 16;     // epilogue warps
+    static constexpr int GROUPS = EPI_WARPS / 4;        // epilogue warps per TMEM lane quadrant
+    static constexpr int BN = SWAP ? 64 : (F32 ? 64 : 128);   // output columns per tile (rows when SWAP)
+    static constexpr int NACC = SWAP ? 4 : (F32 ? 4 : 3);     // TMEM accumulator buffers
     static constexpr int STAGES = kStageWarps;          // shared-memory ring depth: one slot per stage warp
     static constexpr int A_STAGE = kBM * kBK * 2;       // bytes of one A stage
     static constexpr int B_STAGE = BN * kBK * 2;        // bytes of one B stage
-    static constexpr int STAGE_TX = A_STAGE + B_STAGE;  // TMA bytes per stage with a full A box
-    static constexpr int COLS = BN / 4;                 // output columns per epilogue thread
+    static constexpr int STAGE_TX = A_STAGE + B_STAGE;  // TMA bytes per stage with full boxes
+    static constexpr int COLS = BN / GROUPS;            // accumulator columns per epilogue thread
     static constexpr int WORDS = F32 ? COLS : COLS / 2; // 32-bit words per value per thread (16)
     static constexpr int TMEM_COLS = 512;
     static constexpr int TMEM_SLOT_BASE = NACC * BN;    // after the accumulators
+    static constexpr int TMEM_SLOT_STRIDE = WORDS * GROUPS;   // TMEM columns of one slot
     static constexpr int TMEM_FIRST = 2;                // slots 0-1 never leave a block's registers
-    static constexpr int TMEM_SLOTS = (TMEM_COLS - TMEM_SLOT_BASE) / 64;
+    static constexpr int TMEM_SLOTS_FIT = (TMEM_COLS - TMEM_SLOT_BASE) / TMEM_SLOT_STRIDE;
+    static constexpr int TMEM_SLOTS =
+        TMEM_SLOTS_FIT < kMaxSlots - TMEM_FIRST ? TMEM_SLOTS_FIT : kMaxSlots - TMEM_FIRST;
     static constexpr int SMEM_FIRST = TMEM_FIRST + TMEM_SLOTS;
-    static constexpr int SMEM_SLOTS = F32 ? 2 : 3;
+    static constexpr int SMEM_SLOTS = SWAP ? 0 : (F32 ? 2 : 3);
     static constexpr int GLOBAL_FIRST = SMEM_FIRST + SMEM_SLOTS;
     static constexpr int GLOBAL_SLOTS = kMaxSlots - GLOBAL_FIRST;
     static constexpr int LINE = WORDS * 4;              // bytes of one value of one thread (64)
-    static constexpr int SLOT_BYTES = kEpiWarps * 32 * LINE;   // one slot for the whole CTA
+    static constexpr int SLOT_BYTES = EPI_WARPS * 32 * LINE;   // one slot for the whole CTA
     static constexpr int SCRATCH_CTA_BYTES = GLOBAL_SLOTS * SLOT_BYTES;
+
+    // Warp roles: epilogue warps first, then the stage warps.
+    static constexpr int FIRST_STAGE_WARP = EPI_WARPS;
+    static constexpr int TMEM_WARP = EPI_WARPS + 1;     // allocates and frees TMEM
+    static constexpr int THREADS = 32 * (EPI_WARPS + kStageWarps);
+    // Registers per thread at launch: the register split below redistributes
+    // exactly these (plain tile); the transposed tile needs no split.
+    static constexpr int LAUNCH_REGS = SWAP ? 0 : kLaunchRegs;
 
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + STAGES * A_STAGE;
@@ -90,7 +119,8 @@ struct Cfg {
     static constexpr int BYTES = OFF_MISC + 16;
     static constexpr int SMEM_BYTES = BYTES + 1024;     // slack to align the base to 1024 B
 
-    static_assert(GLOBAL_SLOTS >= 1, "slot storage");
+    static_assert(SWAP ? GLOBAL_SLOTS == 0 : GLOBAL_SLOTS >= 1, "slot storage");
+    static_assert(!SWAP || !F32, "the transposed tile has a BF16 output only");
     static_assert(SCRATCH_CTA_BYTES <= kMaxScratchCtaBytes, "scratch");
     static_assert(SMEM_BYTES <= 232448, "shared memory");
     static_assert(A_STAGE % 1024 == 0 && B_STAGE % 1024 == 0, "swizzle atoms");
@@ -211,6 +241,16 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
         " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y)
         : "memory");
+}
+
+// Prefetch of one tile of a tensor map into L2 (no shared memory, no
+// completion); same coordinate rules as tma_load_2d.
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap *map, int x, int y)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y)
+                 : "memory");
 }
 
 __device__ __forceinline__ void tmap_prefetch(const CUtensorMap *map)
@@ -419,12 +459,27 @@ __device__ __forceinline__ uint32_t smem_chunk(uint32_t line, int lane, int k)
 // matrix. A row the matrix clips goes element by element through the
 // thread's scratch line, which is free once the root is formed (every
 // pending partial has been merged into it).
-template <bool F32>
+//
+// Transposed tile (SWAP): the thread's TMEM lane is output column c.row and
+// its 32 values are output rows c.col .. c.col+31 of that column; each goes
+// to out[(c.col + j) * ldo + c.row]. The 32 lanes of a warp hold 32
+// consecutive columns, so every store of the warp writes 64 contiguous bytes.
+template <bool F32, bool SWAP>
 __device__ __forceinline__ void store_out(const Val &v, const Params &p, const EpiCtx &c)
 {
-    using C = Cfg<F32>;
+    using C = Cfg<F32, SWAP>;
     constexpr int ES = F32 ? 4 : 2;
     if (c.row >= c.rows) return;
+    if constexpr (SWAP) {
+        const int nrows = p.cols - c.col;
+        uint16_t *dst = reinterpret_cast<uint16_t *>(c.out) + static_cast<long long>(c.col) * c.ldo + c.row;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            if (2 * i < nrows) dst[(2 * i) * c.ldo] = static_cast<uint16_t>(v[i] & 0xFFFFu);
+            if (2 * i + 1 < nrows) dst[(2 * i + 1) * c.ldo] = static_cast<uint16_t>(v[i] >> 16);
+        }
+        return;
+    }
     const int ncols = p.cols - c.col;
     if (ncols <= 0) return;
     const bool full = ncols >= C::COLS;
@@ -494,12 +549,12 @@ __device__ __forceinline__ void row_partial(const Val &v, const Params &p, const
 }
 
 // Slot s >= 2 (TMEM, shared memory or global scratch) -> t.
-template <bool F32>
+template <bool F32, bool SWAP>
 __device__ __forceinline__ void load_slot(int s, Val &t, const EpiCtx &c)
 {
-    using C = Cfg<F32>;
+    using C = Cfg<F32, SWAP>;
     if (s < C::SMEM_FIRST) {
-        tmem_ld16(c.tmem_slot + static_cast<uint32_t>((s - C::TMEM_FIRST) * 64), t);
+        tmem_ld16(c.tmem_slot + static_cast<uint32_t>((s - C::TMEM_FIRST) * C::TMEM_SLOT_STRIDE), t);
         tmem_wait_ld();
         reg_fence16(t);
     } else if (s < C::GLOBAL_FIRST) {
@@ -522,12 +577,12 @@ __device__ __forceinline__ void load_slot(int s, Val &t, const EpiCtx &c)
 }
 
 // v -> slot s >= 2 (TMEM, shared memory or global scratch).
-template <bool F32>
+template <bool F32, bool SWAP>
 __device__ __forceinline__ void store_slot(int s, const Val &v, const EpiCtx &c)
 {
-    using C = Cfg<F32>;
+    using C = Cfg<F32, SWAP>;
     if (s < C::SMEM_FIRST) {
-        tmem_st16(c.tmem_slot + static_cast<uint32_t>((s - C::TMEM_FIRST) * 64), v);
+        tmem_st16(c.tmem_slot + static_cast<uint32_t>((s - C::TMEM_FIRST) * C::TMEM_SLOT_STRIDE), v);
         tmem_wait_st();
     } else if (s < C::GLOBAL_FIRST) {
         const uint32_t line = c.smem_slot + static_cast<uint32_t>((s - C::SMEM_FIRST) * C::SLOT_BYTES);
@@ -580,15 +635,16 @@ __device__ __forceinline__ void stage_convert(const uint32_t (&stg)[32], Val &F)
 // ----------------------------------------------------------------- kernel
 
 // Shared-memory and TMEM addresses of one CTA.
-template <bool F32>
+template <bool F32, bool SWAP>
 struct Smem {
     uint32_t sA, sB, sSlots, bar0, tmem;
     volatile int *abort_flag;
     __device__ uint32_t full(int s) const { return bar0 + 8u * s; }
-    __device__ uint32_t empty(int s) const { return bar0 + 8u * (Cfg<F32>::STAGES + s); }
-    __device__ uint32_t accf(int b) const { return bar0 + 8u * (2 * Cfg<F32>::STAGES + b); }
-    __device__ uint32_t acce(int b) const { return bar0 + 8u * (2 * Cfg<F32>::STAGES + Cfg<F32>::NACC + b); }
-    __device__ uint32_t never() const { return bar0 + 8u * (2 * Cfg<F32>::STAGES + 2 * Cfg<F32>::NACC); }
+    using C = Cfg<F32, SWAP>;
+    __device__ uint32_t empty(int s) const { return bar0 + 8u * (C::STAGES + s); }
+    __device__ uint32_t accf(int b) const { return bar0 + 8u * (2 * C::STAGES + b); }
+    __device__ uint32_t acce(int b) const { return bar0 + 8u * (2 * C::STAGES + C::NACC + b); }
+    __device__ uint32_t never() const { return bar0 + 8u * (2 * C::STAGES + 2 * C::NACC); }
     __device__ uint32_t drain(int j) const { return never() + 8u * (1 + j); }
     __device__ uint32_t turn(int j) const { return never() + 8u * (1 + kStageWarps + j); }
 };
@@ -609,10 +665,10 @@ struct Smem {
 // barrier phase pair; the turn order guarantees that for the accumulator
 // barriers, and slot ownership for the ring barriers. The warp runs the loop
 // and the waits; one elected lane issues copies, MMAs and commits.
-template <int A_MAJOR, int B_MAJOR, bool F32, bool GROUPED>
-__device__ __forceinline__ void stage_role(const Params &p, const Smem<F32> &S, int j)
+template <int A_MAJOR, int B_MAJOR, bool F32, bool GROUPED, bool SWAP>
+__device__ __forceinline__ void stage_role(const Params &p, const Smem<F32, SWAP> &S, int j)
 {
-    using C = Cfg<F32>;
+    using C = Cfg<F32, SWAP>;
     static_assert(C::STAGES == kStageWarps, "one ring slot per stage warp");
     constexpr uint32_t IDESC = idesc_bf16(kBM, C::BN, A_MAJOR, B_MAJOR);
     // Byte offset of K step k (16 contraction elements) inside a stage:
@@ -676,6 +732,32 @@ __device__ __forceinline__ void stage_role(const Params &p, const Smem<F32> &S, 
             } else {
 #pragma unroll
                 for (int b = 0; b < C::BN / 64; ++b) tma_load_2d(b_dst + 8192 * b, &pb.tmap_b, full, n0 + 64 * b, k0);
+            }
+            if constexpr (SWAP) {
+                // Transposed tile (few output rows): the launch streams the
+                // A operand from DRAM with little arithmetic per byte, so
+                // four slots in flight leave each SM waiting on DRAM
+                // latency. The A tile this warp will copy kPrefetchRounds
+                // rounds from now is fetched into L2 already.
+                const int gp = g + kPrefetchRounds * kStageWarps;
+                if (gp < total) {
+                    const int tlp = gp / KS;
+                    const int ksp = gp - tlp * KS;
+                    const int up = blockIdx.x + tlp * gridDim.x;
+                    const Problem &pbp = p.prob[GROUPED ? problem_of(p, up) : 0];
+                    const int ulp = up - pbp.first_unit;
+                    const int tp = ulp / p.parts;
+                    const int partp = ulp - tp * p.parts;
+                    int mtp, ntp;
+                    tile_coords(tp, pbp, p.n_tiles, mtp, ntp);
+                    const int kp = partp * L * kLeaf + ksp * kBK, mp = mtp * kBM;
+                    if constexpr (A_MAJOR == kKMajor) {
+                        tma_prefetch_2d(&pbp.tmap_a, kp, mp);
+                    } else {
+                        tma_prefetch_2d(&pbp.tmap_a, mp, kp);
+                        if (mp + 64 < pbp.rows) tma_prefetch_2d(&pbp.tmap_a, mp + 64, kp);
+                    }
+                }
             }
         }
         __syncwarp();
@@ -744,16 +826,16 @@ __device__ __forceinline__ void stage_role(const Params &p, const Smem<F32> &S, 
 // entry names and parked (one TMEM or scratch access) or written out as the
 // root. The code stays small so that the loop, rare branches included,
 // lives in the instruction cache.
-template <bool F32, bool GROUPED>
-__device__ __forceinline__ void epilogue_role(const Params &p, const Smem<F32> &S, int warp, int lane)
+template <bool F32, bool GROUPED, bool SWAP>
+__device__ __forceinline__ void epilogue_role(const Params &p, const Smem<F32, SWAP> &S, int warp, int lane)
 {
-    using C = Cfg<F32>;
+    using C = Cfg<F32, SWAP>;
     const int q = warp & 3;               // TMEM lane quadrant (rows 32q .. 32q+31)
-    const int cq = warp >> 2;             // column quarter of the tile
+    const int cq = warp >> 2;             // column group of the tile (a quarter, or a half when SWAP)
     const uint32_t lane_bits = static_cast<uint32_t>(q * 32) << 16;
     const uint32_t acc0 = S.tmem + lane_bits + static_cast<uint32_t>(cq * C::COLS);
     EpiCtx c;
-    c.tmem_slot = S.tmem + lane_bits + static_cast<uint32_t>(C::TMEM_SLOT_BASE + cq * 16);
+    c.tmem_slot = S.tmem + lane_bits + static_cast<uint32_t>(C::TMEM_SLOT_BASE + cq * C::WORDS);
     c.smem_slot = S.sSlots + static_cast<uint32_t>((warp * 32 + lane) * C::LINE);
     c.scratch = static_cast<uint8_t *>(p.scratch) + static_cast<long long>(blockIdx.x) * C::SCRATCH_CTA_BYTES +
                 (warp * 32 + lane) * C::LINE;
@@ -829,27 +911,27 @@ __device__ __forceinline__ void epilogue_role(const Params &p, const Smem<F32> &
 #pragma unroll 1
             for (uint32_t m = (e & 0x3FFu) >> C::TMEM_FIRST, s = C::TMEM_FIRST; m != 0; m >>= 1, ++s) {
                 if (!(m & 1u)) continue;
-                load_slot<F32>(static_cast<int>(s), B, c);   // B is free once the block is merged
+                load_slot<F32, SWAP>(static_cast<int>(s), B, c);   // B is free once the block is merged
 #pragma unroll
                 for (int i = 0; i < 16; ++i) A[i] = merge<F32>(B[i], A[i]);
             }
             const int st = static_cast<int>(e >> 12);
             if (st == kSlotRoot) {
-                store_out<F32>(A, p, c);
+                store_out<F32, SWAP>(A, p, c);
                 if constexpr (GROUPED && !F32) {
                     if (pb.rd_part != nullptr) row_partial(A, p, pb, c, nt, cq);
                 }
             } else {
-                store_slot<F32>(st, A, c);
+                store_slot<F32, SWAP>(st, A, c);
             }
         }
     }
 }
 
-template <int A_MAJOR, int B_MAJOR, bool F32, bool GROUPED>
-__global__ void __launch_bounds__(kThreads, 1) det_gemm_kernel(const __grid_constant__ Params p)
+template <int A_MAJOR, int B_MAJOR, bool F32, bool GROUPED, bool SWAP>
+__global__ void __launch_bounds__(Cfg<F32, SWAP>::THREADS, 1) det_gemm_kernel(const __grid_constant__ Params p)
 {
-    using C = Cfg<F32>;
+    using C = Cfg<F32, SWAP>;
     extern __shared__ uint8_t smem_raw[];
     // 128-byte swizzle atoms need 1024-byte aligned buffers.
     const uint32_t raw = smem_u32(smem_raw);
@@ -858,7 +940,7 @@ __global__ void __launch_bounds__(kThreads, 1) det_gemm_kernel(const __grid_cons
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
 
-    Smem<F32> S;
+    Smem<F32, SWAP> S;
     S.sA = base + C::OFF_A;
     S.sB = base + C::OFF_B;
     S.sSlots = base + C::OFF_SLOTS;
@@ -875,7 +957,7 @@ __global__ void __launch_bounds__(kThreads, 1) det_gemm_kernel(const __grid_cons
         }
         for (int b = 0; b < C::NACC; ++b) {
             mbar_init(S.accf(b), 1);
-            mbar_init(S.acce(b), kEpiWarps);
+            mbar_init(S.acce(b), C::EPI_WARPS);
         }
         mbar_init(S.never(), 1);
         for (int j = 0; j < kStageWarps; ++j) {
@@ -884,13 +966,13 @@ __global__ void __launch_bounds__(kThreads, 1) det_gemm_kernel(const __grid_cons
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    if (warp == kFirstStageWarp && lane == 0) {
+    if (warp == C::FIRST_STAGE_WARP && lane == 0) {
         for (int pi = 0; pi < (GROUPED ? p.num_problems : 1); ++pi) {
             tmap_prefetch(&p.prob[pi].tmap_a);
             tmap_prefetch(&p.prob[pi].tmap_b);
         }
     }
-    if (warp == kTmemWarp) {
+    if (warp == C::TMEM_WARP) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                          smem_u32(tmem_base_smem)),
                      "r"(C::TMEM_COLS)
@@ -902,18 +984,24 @@ __global__ void __launch_bounds__(kThreads, 1) det_gemm_kernel(const __grid_cons
     tc_fence_after();
     S.tmem = *tmem_base_smem;
 
-    // Register split: the stage warpgroup gives up registers and the four
-    // epilogue warpgroups take them (kProdRegs*128 + kEpiRegs*512 fits in
-    // the kLaunchRegs*640 the CTA is launched with). Each role's code sits
-    // inside its own branch so that the compiler allocates it under the
-    // matching limit.
-    static_assert(kProdRegs * 128 + kEpiRegs * 32 * kEpiWarps <= kLaunchRegs * kThreads, "register split");
-    if (warp < kEpiWarps) {
-        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kEpiRegs));
-        epilogue_role<F32, GROUPED>(p, S, warp, lane);
+    if constexpr (!SWAP) {
+        // Register split: the stage warpgroup gives up registers and the four
+        // epilogue warpgroups take them (kProdRegs*128 + kEpiRegs*512 fits in
+        // the kLaunchRegs*640 the CTA is launched with). Each role's code sits
+        // inside its own branch so that the compiler allocates it under the
+        // matching limit.
+        static_assert(kProdRegs * 128 + kEpiRegs * 32 * C::EPI_WARPS <= kLaunchRegs * C::THREADS, "register split");
+        if (warp < C::EPI_WARPS) {
+            asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kEpiRegs));
+            epilogue_role<F32, GROUPED, SWAP>(p, S, warp, lane);
+        } else {
+            asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kProdRegs));
+            stage_role<A_MAJOR, B_MAJOR, F32, GROUPED, SWAP>(p, S, warp - C::FIRST_STAGE_WARP);
+        }
     } else {
-        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kProdRegs));
-        stage_role<A_MAJOR, B_MAJOR, F32, GROUPED>(p, S, warp - kFirstStageWarp);
+        // 384 threads: every warp has the registers it needs without a split.
+        if (warp < C::EPI_WARPS) epilogue_role<F32, GROUPED, SWAP>(p, S, warp, lane);
+        else stage_role<A_MAJOR, B_MAJOR, F32, GROUPED, SWAP>(p, S, warp - C::FIRST_STAGE_WARP);
     }
 
     // ---- teardown
@@ -921,7 +1009,7 @@ __global__ void __launch_bounds__(kThreads, 1) det_gemm_kernel(const __grid_cons
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == kTmemWarp) {
+    if (warp == C::TMEM_WARP) {
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(S.tmem), "r"(C::TMEM_COLS)
                      : "memory");
     }
@@ -929,13 +1017,13 @@ __global__ void __launch_bounds__(kThreads, 1) det_gemm_kernel(const __grid_cons
 
 // --------------------------------------------------------- host launcher
 
-template <int A_MAJOR, int B_MAJOR, bool F32, bool GROUPED = false>
+template <int A_MAJOR, int B_MAJOR, bool F32, bool GROUPED = false, bool SWAP = false>
 struct Launcher {
+    using C = Cfg<F32, SWAP>;
     static cudaError_t prepare(int *num_regs)
     {
-        auto fn = det_gemm_kernel<A_MAJOR, B_MAJOR, F32, GROUPED>;
-        cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             Cfg<F32>::SMEM_BYTES);
+        auto fn = det_gemm_kernel<A_MAJOR, B_MAJOR, F32, GROUPED, SWAP>;
+        cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
         if (e != cudaSuccess) return e;
         cudaFuncAttributes at;
         e = cudaFuncGetAttributes(&at, fn);
@@ -945,7 +1033,7 @@ struct Launcher {
     }
     static cudaError_t launch(const Params &p, int grid, cudaStream_t stream)
     {
-        det_gemm_kernel<A_MAJOR, B_MAJOR, F32, GROUPED><<<grid, kThreads, Cfg<F32>::SMEM_BYTES, stream>>>(p);
+        det_gemm_kernel<A_MAJOR, B_MAJOR, F32, GROUPED, SWAP><<<grid, C::THREADS, C::SMEM_BYTES, stream>>>(p);
         return cudaGetLastError();
     }
     static VariantOps ops()
@@ -953,9 +1041,11 @@ struct Launcher {
         VariantOps o;
         o.prepare = &prepare;
         o.launch = &launch;
-        o.bn = Cfg<F32>::BN;
-        o.smem_bytes = Cfg<F32>::SMEM_BYTES;
-        o.scratch_cta_bytes = Cfg<F32>::SCRATCH_CTA_BYTES;
+        o.bn = C::BN;
+        o.smem_bytes = C::SMEM_BYTES;
+        o.scratch_cta_bytes = C::SCRATCH_CTA_BYTES;
+        o.split_regs = C::LAUNCH_REGS;
+        o.swap = SWAP;
         return o;
     }
 };

@@ -1,0 +1,107 @@
+"""Launches with at most 64 output rows take the transposed tile: the MMA's
+128 lanes carry output columns and its N side the few rows, so the
+epilogue's work follows the rows that exist. The page promises that a row's
+bits do not depend on how many rows are computed with it (RL-Kernel,
+"Batch-Invariant Deterministic GEMM (det_gemm)", sections "Why" and
+"Guarantees"), so every case here checks the transposed launch against the
+same rows computed by the plain tile (more than 64 rows), bit for bit, and
+against the oracle on exact inputs and within the derived tolerance on
+normal ones."""
+import numpy as np
+import pytest
+import torch
+
+import invariant_deterministic_gemm_gb300 as dg
+import oracle
+import workloads as W
+from gpu_util import assert_bf16_close, check, dev, exact_equal
+
+pytestmark = pytest.mark.gpu
+
+ROWS = (1, 2, 7, 16, 17, 33, 63, 64)
+
+
+def bits_equal(x, y):
+    return torch.equal(x.contiguous().view(torch.int16), y.contiguous().view(torch.int16))
+
+
+@pytest.mark.parametrize("K,N", [(4096, 1024), (100, 200), (14336, 256), (32, 8)])
+def test_forward_rows_equal_the_plain_tile(K, N):
+    A = dev(W.randn_bf16((256, K), 1.0, 8100 + K))
+    B = dev(W.randn_bf16((K, N), 0.02, 8200 + K))
+    full = dg.det_gemm_fwd(A, B)                    # 256 rows: plain tile
+    for M in ROWS:
+        assert bits_equal(dg.det_gemm_fwd(A[:M], B), full[:M]), (K, N, M)
+    # rows taken from the middle of the batch
+    assert bits_equal(dg.det_gemm_fwd(A[100:137], B), full[100:137])
+    check()
+
+
+@pytest.mark.parametrize("K,N", [(4096, 1024), (744, 136)])   # 744: a partial last leaf
+def test_rhs_transposed_and_da_rows_equal_the_plain_tile(K, N):
+    A = dev(W.randn_bf16((256, K), 1.0, 8301 + K))
+    Wt = dev(W.randn_bf16((N, K), 0.02, 8302 + K))          # [N, K]
+    dC = dev(W.randn_bf16((256, N), 1e-3, 8303 + K))
+    Bw = dev(W.randn_bf16((K, N), 0.02, 8304 + K))          # [K, N]
+    full = dg.det_gemm_fwd_rhs_transposed(A, Wt)
+    full_da = dg.det_gemm_da(dC, Bw)                         # [256, K], contraction N
+    for M in ROWS:
+        assert bits_equal(dg.det_gemm_fwd_rhs_transposed(A[:M], Wt), full[:M]), (K, N, M)
+        assert bits_equal(dg.det_gemm_da(dC[:M], Bw), full_da[:M]), (K, N, M)
+    check()
+
+
+def test_split_contraction_rows_equal_the_plain_tile():
+    # Few column tiles and a long contraction: the transposed launch also
+    # splits its contraction into subtrees (MLP down-projection of 4 tokens).
+    K, N = 14336, 512
+    A = dev(W.randn_bf16((128, K), 1.0, 8401))
+    B = dev(W.randn_bf16((K, N), 0.02, 8402))
+    full = dg.det_gemm_fwd(A, B)
+    for M in (1, 4, 64):
+        assert bits_equal(dg.det_gemm_fwd(A[:M], B), full[:M]), M
+    check()
+
+
+def test_padded_pitches_and_the_allocation_free_entry_point():
+    K, N = 512, 384
+    A = W.randn_bf16((128, K), 1.0, 8501)
+    B = W.randn_bf16((K, N), 0.02, 8502)
+    Ab = torch.zeros((128, K + 24), dtype=torch.bfloat16, device="cuda")
+    Ab[:, :K] = A.cuda()
+    Bb = torch.zeros((K, N + 40), dtype=torch.bfloat16, device="cuda")
+    Bb[:, :N] = B.cuda()
+    full = dg.det_gemm_fwd(Ab[:, :K], Bb[:, :N])
+    for M in (5, 64):
+        Cb = torch.full((M, N + 56), 7.0, dtype=torch.bfloat16, device="cuda")   # padded output pitch
+        dg.det_gemm_fwd(Ab[:M, :K], Bb[:, :N], out=Cb[:, :N])
+        assert bits_equal(Cb[:, :N], full[:M]), M
+        assert bool((Cb[:, N:] == 7.0).all()), "columns past N were written"
+        C2 = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        dg.det_gemm_fwd_noalloc(Ab[:M, :K], Bb[:, :N], C2)
+        assert bits_equal(C2, full[:M]), M
+    check()
+
+
+@pytest.mark.parametrize("M,K,N", [(1, 96, 136), (13, 4096, 256), (64, 2000, 128)])
+def test_integer_inputs_match_oracle_bit_for_bit(M, K, N):
+    A = W.randint_bf16((M, K), -8, 9, 8600 + M)
+    B = W.randint_bf16((K, N), -8, 9, 8700 + M)
+    got = W.bits(dg.det_gemm_fwd(dev(A), dev(B)))
+    check()
+    want = oracle.gemm(W.bits(A), W.bits(B))
+    assert exact_equal(got, want)
+
+
+def test_normal_inputs_within_tolerance_of_oracle():
+    M, K, N = 3, 4096, 640
+    A = W.randn_bf16((M, K), 1.0, 8801)
+    B = W.randn_bf16((K, N), 0.02, 8802)
+    got = W.bits(dg.det_gemm_fwd(dev(A), dev(B)))
+    Wt = W.randn_bf16((N, K), 0.02, 8803)
+    got_t = W.bits(dg.det_gemm_fwd_rhs_transposed(dev(A), dev(Wt)))
+    check()
+    want, nodemax = oracle.gemm(W.bits(A), W.bits(B), with_node_max=True)
+    assert_bf16_close(got, want, nodemax, K // 32, "fwd, 3 rows")
+    want_t, nodemax_t = oracle.gemm(W.bits(A), np.ascontiguousarray(W.bits(Wt).T), with_node_max=True)
+    assert_bf16_close(got_t, want_t, nodemax_t, K // 32, "rhs_transposed, 3 rows")
