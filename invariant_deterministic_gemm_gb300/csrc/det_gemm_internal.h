@@ -17,9 +17,14 @@ constexpr int kMaxSlots = 10;             // ceil(log2(kMaxLeaves)) pending part
 constexpr int kBM = 128;                  // output rows per tile (one TMEM lane per row)
 constexpr int kBK = 64;                   // contraction elements per shared-memory stage (two leaves)
 constexpr int kStageWarps = 4;            // TMA copies and MMAs of the K-stages: one per SM sub-partition
-constexpr int kLaunchRegs = 96;           // registers per thread at launch of the plain tile's 640 threads
-constexpr int kProdRegs = 40;             // stage warpgroup after setmaxnreg
-constexpr int kEpiRegs = 104;             // epilogue warpgroups after setmaxnreg
+constexpr int kEpiWarps = 8;              // epilogue warps of the plain tile (a multiple of 4)
+// Registers per thread at launch: the most a CTA of the plain tile's
+// threads can have at one CTA per SM, and the register split between the
+// stage warpgroup and the epilogue warps (setmaxnreg), which redistributes
+// exactly the launch's registers.
+constexpr int kLaunchRegs = (65536 / (32 * (kEpiWarps + kStageWarps))) & ~7;
+constexpr int kProdRegs = kEpiWarps == 8 ? 72 : 40;
+constexpr int kEpiRegs = (kLaunchRegs * 32 * (kEpiWarps + kStageWarps) - kProdRegs * 32 * kStageWarps) / (32 * kEpiWarps) & ~7;
 
 // Operand major-ness as seen by the MMA: K-major = contraction contiguous.
 enum Major { kKMajor = 0, kMNMajor = 1 };

@@ -12,17 +12,21 @@
 // invariance bullet). One tile shape per variant, whatever M is: choosing a
 // kernel by problem shape is what breaks batch invariance (section "Why").
 //
-// CTA layout (640 threads, one CTA per SM, persistent over output tiles):
-//   warps 0-15 epilogue: warp w reads TMEM lanes 32*(w%4).. (rows) and the
-//              column quarter w/4 of the tile; each thread owns one row and
-//              BN/4 columns, and keeps the tree's pending partials for them.
-//              Four epilogue warps per scheduler hide each other's waits.
-//   warps 16-19 stage warps, one per scheduler: warp 16+j owns ring slot j
+// CTA layout (384 threads, one CTA per SM, persistent over output tiles):
+//   warps 0-7  epilogue: warp w reads TMEM lanes 32*(w%4).. (rows) and the
+//              column half w/4 of the tile; each thread owns one row and
+//              BN/2 columns, and keeps the tree's pending partials for them.
+//              Two epilogue warps per scheduler; each overlaps the TMEM load
+//              of its next leaf with the merges of the current one.
+//   warps 8-11 stage warps, one per scheduler: warp 8+j owns ring slot j
 //              and the K-stages g = j (mod 4) of the CTA's tile sequence. It
 //              copies the stage's A and B tiles in with TMA, then issues the
 //              stage's MMAs; MMA issue is handed from warp to warp in stage
-//              order (turn barriers). Warp 17 also allocates and frees TMEM.
-//
+//              order (turn barriers). Warp 9 also allocates and frees TMEM.
+//   The stage warpgroup runs on 72 registers per thread and the epilogue
+//   warps on 216 (setmaxnreg), which holds a leaf in flight, three values
+//   of 32 words and the merge operands without spilling.
+
 // Transposed tile (launches with at most 64 output rows, BF16 out): the
 // MMA's A operand is the weight, so its 128 TMEM lanes are 128 output
 // columns, and its N side (64) holds the rows. 384 threads: warps 0-7
@@ -47,7 +51,7 @@
 // entirely in registers, so only slots 2 and up ever hold a value: the
 // next slots are TMEM columns past the accumulators, then shared memory,
 // and the last three (touched at most once per 256 leaves) a per-CTA
-// global-memory scratch line of 128 bytes per thread.
+// global-memory scratch line per thread.
 //
 // Every mbarrier wait is bounded (Params::timeout_ns of %globaltimer). On
 // expiry the waiter records DET_GEMM_ERR_TIMEOUT in the status word and sets
@@ -55,6 +59,8 @@
 // loads and MMAs are drained with bounded waits, TMEM is released and the
 // CTA exits.
 #pragma once
+
+#include <type_traits>
 
 #include "det_gemm_internal.h"
 
@@ -75,7 +81,7 @@ constexpr int kPrefetchRounds = 2;  // transposed tile: L2 prefetch distance, in
 // against the plain tile on the GPU).
 template <bool F32, bool SWAP = false>
 struct Cfg {
-    static constexpr int EPI_WARPS = SWAP ? 8 : 16;     // epilogue warps
+    static constexpr int EPI_WARPS = SWAP ? 8 : kEpiWarps;   // epilogue warps
     static constexpr int GROUPS = EPI_WARPS / 4;        // epilogue warps per TMEM lane quadrant
     static constexpr int BN = SWAP ? 64 : (F32 ? 64 : 128);   // output columns per tile (rows when SWAP)
     static constexpr int NACC = SWAP ? 4 : (F32 ? 4 : 3);     // TMEM accumulator buffers
@@ -84,7 +90,7 @@ struct Cfg {
     static constexpr int B_STAGE = BN * kBK * 2;        // bytes of one B stage
     static constexpr int STAGE_TX = A_STAGE + B_STAGE;  // TMA bytes per stage with full boxes
     static constexpr int COLS = BN / GROUPS;            // accumulator columns per epilogue thread
-    static constexpr int WORDS = F32 ? COLS : COLS / 2; // 32-bit words per value per thread (16)
+    static constexpr int WORDS = F32 ? COLS : COLS / 2; // 32-bit words per value per thread
     static constexpr int TMEM_COLS = 512;
     static constexpr int TMEM_SLOT_BASE = NACC * BN;    // after the accumulators
     static constexpr int TMEM_SLOT_STRIDE = WORDS * GROUPS;   // TMEM columns of one slot
@@ -96,7 +102,8 @@ struct Cfg {
     static constexpr int SMEM_SLOTS = SWAP ? 0 : (F32 ? 2 : 3);
     static constexpr int GLOBAL_FIRST = SMEM_FIRST + SMEM_SLOTS;
     static constexpr int GLOBAL_SLOTS = kMaxSlots - GLOBAL_FIRST;
-    static constexpr int LINE = WORDS * 4;              // bytes of one value of one thread (64)
+    static constexpr int LINE = WORDS * 4;              // bytes of one value of one thread
+    static constexpr int CHUNKS = LINE / 16;            // 16-byte chunks of a line
     static constexpr int SLOT_BYTES = EPI_WARPS * 32 * LINE;   // one slot for the whole CTA
     static constexpr int SCRATCH_CTA_BYTES = GLOBAL_SLOTS * SLOT_BYTES;
 
@@ -104,8 +111,9 @@ struct Cfg {
     static constexpr int FIRST_STAGE_WARP = EPI_WARPS;
     static constexpr int TMEM_WARP = EPI_WARPS + 1;     // allocates and frees TMEM
     static constexpr int THREADS = 32 * (EPI_WARPS + kStageWarps);
-    // Registers per thread at launch: the register split below redistributes
-    // exactly these (plain tile); the transposed tile needs no split.
+    // Registers per thread at launch (the most 384 threads of one CTA per SM
+    // can have); the plain tile's register split redistributes exactly
+    // these, the transposed tile needs no split.
     static constexpr int LAUNCH_REGS = SWAP ? 0 : kLaunchRegs;
 
     static constexpr int OFF_A = 0;
@@ -124,7 +132,8 @@ struct Cfg {
     static_assert(SCRATCH_CTA_BYTES <= kMaxScratchCtaBytes, "scratch");
     static_assert(SMEM_BYTES <= 232448, "shared memory");
     static_assert(A_STAGE % 1024 == 0 && B_STAGE % 1024 == 0, "swizzle atoms");
-    static_assert(WORDS == 16, "epilogue values are 16 words per thread");
+    static_assert(WORDS == 16 || WORDS == 32, "epilogue values are 16 or 32 words per thread");
+    static_assert(THREADS * kLaunchRegs <= 65536, "one CTA per SM at the launch register count");
 };
 
 // ----------------------------------------------------------- PTX helpers
@@ -431,29 +440,22 @@ __device__ __forceinline__ int problem_of(const Params &p, int u)
 
 // ------------------------------------------------------------- epilogue
 
-// Every epilogue value (a rounded leaf, a partial, the root) is 16 words per
-// thread: 32 BF16 columns packed in pairs, or 16 FP32 columns.
-using Val = uint32_t[16];
+// Every epilogue value (a rounded leaf, a partial, the root) is W words per
+// thread: 2W BF16 columns packed in pairs, or W FP32 columns.
+template <int W>
+using ValW = uint32_t[W];
 
 // What one epilogue thread needs to reach its storage.
 struct EpiCtx {
     uint32_t tmem_slot;   // TMEM address of this thread's first TMEM slot
-    uint32_t smem_slot;   // shared-memory address of this thread's line in the first shared slot
-    uint8_t *scratch;     // this thread's 64-byte line in the first global slot
+    uint8_t *smem_line;   // generic address of this thread's line in the first shared slot
+    uint8_t *scratch;     // this thread's line in the first global slot
     int lane;
     int row, col;         // first output element owned by this thread
     int rows;             // rows of the output (the problem's)
     uint8_t *out;         // matrix the roots go to (the output, or this unit's part slab)
     long long ldo;        // its leading dimension, elements
 };
-
-// 16-byte chunk k (0..3) of a thread's 64-byte shared-memory line. Lines of
-// consecutive lanes are 64 bytes apart; swizzling the chunk by lane/2 puts
-// the eight lanes of a quarter-warp access on eight distinct bank groups.
-__device__ __forceinline__ uint32_t smem_chunk(uint32_t line, int lane, int k)
-{
-    return line + static_cast<uint32_t>((k ^ ((lane >> 1) & 3)) * 16);
-}
 
 // Writes this thread's value of the root to the output, clipped to the
 // matrix. A row the matrix clips goes element by element through the
@@ -464,8 +466,8 @@ __device__ __forceinline__ uint32_t smem_chunk(uint32_t line, int lane, int k)
 // its 32 values are output rows c.col .. c.col+31 of that column; each goes
 // to out[(c.col + j) * ldo + c.row]. The 32 lanes of a warp hold 32
 // consecutive columns, so every store of the warp writes 64 contiguous bytes.
-template <bool F32, bool SWAP>
-__device__ __forceinline__ void store_out(const Val &v, const Params &p, const EpiCtx &c)
+template <bool F32, bool SWAP, int W>
+__device__ __forceinline__ void store_out(const ValW<W> &v, const Params &p, const EpiCtx &c)
 {
     using C = Cfg<F32, SWAP>;
     constexpr int ES = F32 ? 4 : 2;
@@ -474,7 +476,7 @@ __device__ __forceinline__ void store_out(const Val &v, const Params &p, const E
         const int nrows = p.cols - c.col;
         uint16_t *dst = reinterpret_cast<uint16_t *>(c.out) + static_cast<long long>(c.col) * c.ldo + c.row;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
+        for (int i = 0; i < W; ++i) {
             if (2 * i < nrows) dst[(2 * i) * c.ldo] = static_cast<uint16_t>(v[i] & 0xFFFFu);
             if (2 * i + 1 < nrows) dst[(2 * i + 1) * c.ldo] = static_cast<uint16_t>(v[i] >> 16);
         }
@@ -486,7 +488,7 @@ __device__ __forceinline__ void store_out(const Val &v, const Params &p, const E
     uint8_t *dst = c.out + (static_cast<long long>(c.row) * c.ldo + c.col) * ES;
     uint8_t *vec = full ? dst : c.scratch;
 #pragma unroll
-    for (int k = 0; k < 4; ++k)
+    for (int k = 0; k < W / 4; ++k)
         asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(vec + 16 * k), "r"(v[4 * k]),
                      "r"(v[4 * k + 1]), "r"(v[4 * k + 2]), "r"(v[4 * k + 3])
                      : "memory");
@@ -506,129 +508,191 @@ __device__ __forceinline__ void store_out(const Val &v, const Params &p, const E
 }
 
 // Row reduction of a grouped launch (bf16 variant): this thread's share of
-// rowdot[row] = sum over columns n of C[row, n] * D[row, n], for its 32
-// columns of column tile nt and quarter cq: the FP32 sum of the products
-// (exact: BF16 x BF16) in ascending column order, from +0 (+0 for a quarter
-// entirely past the last column). It goes to its own slot; no other thread
+// rowdot[row] = sum over columns n of C[row, n] * D[row, n]. The tile's
+// columns are cut into four quarters of 32; for each quarter it holds, the
+// thread forms the FP32 sum of the products (exact: BF16 x BF16) in
+// ascending column order, from +0 (+0 for a quarter entirely past the last
+// column), and writes it to that quarter's own slot; no other thread
 // writes there, and the slots are combined later in a fixed order.
-__device__ __forceinline__ void row_partial(const Val &v, const Params &p, const Problem &pb, const EpiCtx &c,
+template <int W>
+__device__ __forceinline__ void row_partial(const ValW<W> &v, const Params &p, const Problem &pb, const EpiCtx &c,
                                             int nt, int cq)
 {
     if (c.row >= c.rows) return;
-    const int ncols = p.cols - c.col;
-    float s = 0.0f;
-    if (ncols > 0) {
-        const uint16_t *d = pb.rd_d + static_cast<long long>(c.row) * pb.rd_ldd + c.col;
-        uint32_t dw[16];
-        if (ncols >= 32) {
+    constexpr int QUARTERS = W / 16;      // 32-column quarters this thread holds
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const uint4 x = *reinterpret_cast<const uint4 *>(d + 8 * k);
-                dw[4 * k] = x.x;
-                dw[4 * k + 1] = x.y;
-                dw[4 * k + 2] = x.z;
-                dw[4 * k + 3] = x.w;
+    for (int h = 0; h < QUARTERS; ++h) {
+        const int col = c.col + 32 * h;
+        const int ncols = p.cols - col;
+        float s = 0.0f;
+        if (ncols > 0) {
+            const uint16_t *d = pb.rd_d + static_cast<long long>(c.row) * pb.rd_ldd + col;
+            uint32_t dw[16];
+            if (ncols >= 32) {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const uint4 x = *reinterpret_cast<const uint4 *>(d + 8 * k);
+                    dw[4 * k] = x.x;
+                    dw[4 * k + 1] = x.y;
+                    dw[4 * k + 2] = x.z;
+                    dw[4 * k + 3] = x.w;
+                }
+            } else {
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {
+                    const uint32_t lo = 2 * k < ncols ? d[2 * k] : 0u;
+                    const uint32_t hi = 2 * k + 1 < ncols ? d[2 * k + 1] : 0u;
+                    dw[k] = lo | (hi << 16);
+                }
             }
-        } else {
 #pragma unroll
             for (int k = 0; k < 16; ++k) {
-                const uint32_t lo = 2 * k < ncols ? d[2 * k] : 0u;
-                const uint32_t hi = 2 * k + 1 < ncols ? d[2 * k + 1] : 0u;
-                dw[k] = lo | (hi << 16);
+                const uint32_t x = v[16 * h + k];
+                if (2 * k < ncols)
+                    s = __fadd_rn(s, __fmul_rn(__uint_as_float(x << 16), __uint_as_float(dw[k] << 16)));
+                if (2 * k + 1 < ncols)
+                    s = __fadd_rn(s, __fmul_rn(__uint_as_float(x & 0xFFFF0000u), __uint_as_float(dw[k] & 0xFFFF0000u)));
             }
         }
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {
-            if (2 * k < ncols)
-                s = __fadd_rn(s, __fmul_rn(__uint_as_float(v[k] << 16), __uint_as_float(dw[k] << 16)));
-            if (2 * k + 1 < ncols)
-                s = __fadd_rn(s, __fmul_rn(__uint_as_float(v[k] & 0xFFFF0000u), __uint_as_float(dw[k] & 0xFFFF0000u)));
-        }
+        pb.rd_part[static_cast<long long>(nt * 4 + cq * QUARTERS + h) * pb.rows + c.row] = s;
     }
-    pb.rd_part[static_cast<long long>(nt * 4 + cq) * pb.rows + c.row] = s;
 }
 
-// Slot s >= 2 (TMEM, shared memory or global scratch) -> t.
-template <bool F32, bool SWAP>
-__device__ __forceinline__ void load_slot(int s, Val &t, const EpiCtx &c)
+// TMEM <-> registers for one value of W words.
+template <int W>
+__device__ __forceinline__ void tmem_ld_val(uint32_t taddr, ValW<W> &t)
 {
-    using C = Cfg<F32, SWAP>;
-    if (s < C::SMEM_FIRST) {
-        tmem_ld16(c.tmem_slot + static_cast<uint32_t>((s - C::TMEM_FIRST) * C::TMEM_SLOT_STRIDE), t);
-        tmem_wait_ld();
-        reg_fence16(t);
-    } else if (s < C::GLOBAL_FIRST) {
-        const uint32_t line = c.smem_slot + static_cast<uint32_t>((s - C::SMEM_FIRST) * C::SLOT_BYTES);
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-                         : "=r"(t[4 * k]), "=r"(t[4 * k + 1]), "=r"(t[4 * k + 2]), "=r"(t[4 * k + 3])
-                         : "r"(smem_chunk(line, c.lane, k))
-                         : "memory");
+    if constexpr (W == 16) {
+        tmem_ld16(taddr, t);
     } else {
-        const uint8_t *src = c.scratch + (s - C::GLOBAL_FIRST) * C::SLOT_BYTES;
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-            asm volatile("ld.global.v4.b32 {%0, %1, %2, %3}, [%4];"
-                         : "=r"(t[4 * k]), "=r"(t[4 * k + 1]), "=r"(t[4 * k + 2]), "=r"(t[4 * k + 3])
-                         : "l"(src + 16 * k)
-                         : "memory");
+        tmem_ld32(taddr, t);
     }
 }
 
-// v -> slot s >= 2 (TMEM, shared memory or global scratch).
+template <int W>
+__device__ __forceinline__ void tmem_st_val(uint32_t taddr, const ValW<W> &v)
+{
+    if constexpr (W == 16) {
+        tmem_st16(taddr, v);
+    } else {
+        tmem_st32(taddr, v);
+    }
+}
+
+template <int W>
+__device__ __forceinline__ void reg_fence_val(ValW<W> &t)
+{
+    if constexpr (W == 16) {
+        reg_fence16(t);
+    } else {
+        reg_fence(t);
+    }
+}
+
+// Where slot s >= 2 lives when it is not in TMEM: a generic address of
+// this thread's line, in the shared-memory slots or the global scratch.
 template <bool F32, bool SWAP>
-__device__ __forceinline__ void store_slot(int s, const Val &v, const EpiCtx &c)
+__device__ __forceinline__ uint8_t *slot_line(int s, const EpiCtx &c)
+{
+    using C = Cfg<F32, SWAP>;
+    return s < C::GLOBAL_FIRST ? c.smem_line + (s - C::SMEM_FIRST) * C::SLOT_BYTES
+                               : c.scratch + (s - C::GLOBAL_FIRST) * C::SLOT_BYTES;
+}
+
+// 16-byte chunk k of a thread's line of CHUNKS chunks. Lines of
+// consecutive lanes are 16*CHUNKS bytes apart; permuting the chunks by lane
+// puts the eight lanes of a quarter-warp shared-memory access on eight
+// distinct 16-byte bank groups. Shared and global lines use the same
+// permutation.
+template <int CHUNKS>
+__device__ __forceinline__ uint8_t *line_chunk(uint8_t *line, int lane, int k)
+{
+    if constexpr (CHUNKS == 8) return line + (k ^ (lane & 7)) * 16;
+    else return line + (k ^ ((lane >> 1) & 3)) * 16;
+}
+
+// A = slot s (s >= 2) merged with A: A = merge(slot, A).
+template <bool F32, bool SWAP, int W>
+__device__ __forceinline__ void merge_slot(int s, ValW<W> &A, ValW<W> &T, const EpiCtx &c)
 {
     using C = Cfg<F32, SWAP>;
     if (s < C::SMEM_FIRST) {
-        tmem_st16(c.tmem_slot + static_cast<uint32_t>((s - C::TMEM_FIRST) * C::TMEM_SLOT_STRIDE), v);
-        tmem_wait_st();
-    } else if (s < C::GLOBAL_FIRST) {
-        const uint32_t line = c.smem_slot + static_cast<uint32_t>((s - C::SMEM_FIRST) * C::SLOT_BYTES);
+        tmem_ld_val<W>(c.tmem_slot + static_cast<uint32_t>((s - C::TMEM_FIRST) * C::TMEM_SLOT_STRIDE), T);
+        tmem_wait_ld();
+        reg_fence_val<W>(T);
+    } else {
+        uint8_t *line = slot_line<F32, SWAP>(s, c);
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(smem_chunk(line, c.lane, k)),
+        for (int k = 0; k < C::CHUNKS; ++k)
+            asm volatile("ld.v4.b32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(T[4 * k]), "=r"(T[4 * k + 1]), "=r"(T[4 * k + 2]), "=r"(T[4 * k + 3])
+                         : "l"(line_chunk<C::CHUNKS>(line, c.lane, k))
+                         : "memory");
+    }
+#pragma unroll
+    for (int i = 0; i < W; ++i) A[i] = merge<F32>(T[i], A[i]);
+}
+
+// v -> slot s >= 2.
+template <bool F32, bool SWAP, int W>
+__device__ __forceinline__ void store_slot(int s, const ValW<W> &v, const EpiCtx &c)
+{
+    using C = Cfg<F32, SWAP>;
+    if (s < C::SMEM_FIRST) {
+        tmem_st_val<W>(c.tmem_slot + static_cast<uint32_t>((s - C::TMEM_FIRST) * C::TMEM_SLOT_STRIDE), v);
+        tmem_wait_st();
+    } else {
+        uint8_t *line = slot_line<F32, SWAP>(s, c);
+#pragma unroll
+        for (int k = 0; k < C::CHUNKS; ++k)
+            asm volatile("st.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(line_chunk<C::CHUNKS>(line, c.lane, k)),
                          "r"(v[4 * k]), "r"(v[4 * k + 1]), "r"(v[4 * k + 2]), "r"(v[4 * k + 3])
                          : "memory");
-    } else {
-        uint8_t *dst = c.scratch + (s - C::GLOBAL_FIRST) * C::SLOT_BYTES;
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-            asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(dst + 16 * k), "r"(v[4 * k]),
-                         "r"(v[4 * k + 1]), "r"(v[4 * k + 2]), "r"(v[4 * k + 3])
-                         : "memory");
     }
 }
 
-// Loads this thread's BN/4 accumulator columns (32 FP32 for the bf16
-// variant, 16 for the fp32 one) into the staging registers and waits.
-template <bool F32>
-__device__ __forceinline__ void stage_load(uint32_t acc_taddr, uint32_t (&stg)[32])
+// Starts loading this thread's N accumulator columns of one leaf (FP32)
+// into the staging registers. The registers are not valid until
+// stage_land().
+template <int N>
+__device__ __forceinline__ void stage_issue(uint32_t acc_taddr, uint32_t (&stg)[N])
 {
-    if constexpr (F32) {
-        uint32_t(&lo)[16] = *reinterpret_cast<uint32_t(*)[16]>(&stg[0]);
-        tmem_ld16(acc_taddr, lo);
-        tmem_wait_ld();
-        reg_fence16(lo);
+    static_assert(N == 16 || N % 32 == 0, "staging in loads of 16 or 32 columns");
+    if constexpr (N == 16) {
+        tmem_ld16(acc_taddr, stg);
     } else {
-        tmem_ld32(acc_taddr, stg);
-        tmem_wait_ld();
-        reg_fence(stg);
+#pragma unroll
+        for (int h = 0; h < N / 32; ++h)
+            tmem_ld32(acc_taddr + 32u * h, *reinterpret_cast<uint32_t(*)[32]>(&stg[32 * h]));
+    }
+}
+
+// Waits for the staging load and ties the registers to a point after the
+// wait, so that no use of them is scheduled before it.
+template <int N>
+__device__ __forceinline__ void stage_land(uint32_t (&stg)[N])
+{
+    tmem_wait_ld();
+    if constexpr (N == 16) {
+        reg_fence16(stg);
+    } else {
+#pragma unroll
+        for (int h = 0; h < N / 32; ++h) reg_fence(*reinterpret_cast<uint32_t(*)[32]>(&stg[32 * h]));
     }
 }
 
 // The staged leaf -> F: rounded once to BF16 (RNE), two columns per word,
 // for the bf16 variant; as is for the fp32 variant.
-template <bool F32>
-__device__ __forceinline__ void stage_convert(const uint32_t (&stg)[32], Val &F)
+template <bool F32, int W, int N>
+__device__ __forceinline__ void stage_convert(const uint32_t (&stg)[N], ValW<W> &F)
 {
+    static_assert(N == (F32 ? W : 2 * W), "staging width");
     if constexpr (F32) {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) F[i] = stg[i];
+        for (int i = 0; i < W; ++i) F[i] = stg[i];
     } else {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) F[i] = cvt_bf16x2(stg[2 * i], stg[2 * i + 1]);
+        for (int i = 0; i < W; ++i) F[i] = cvt_bf16x2(stg[2 * i], stg[2 * i + 1]);
     }
 }
 
@@ -637,7 +701,8 @@ __device__ __forceinline__ void stage_convert(const uint32_t (&stg)[32], Val &F)
 // Shared-memory and TMEM addresses of one CTA.
 template <bool F32, bool SWAP>
 struct Smem {
-    uint32_t sA, sB, sSlots, bar0, tmem;
+    uint32_t sA, sB, bar0, tmem;
+    uint8_t *slots;       // generic address of the shared-memory slots
     volatile int *abort_flag;
     __device__ uint32_t full(int s) const { return bar0 + 8u * s; }
     using C = Cfg<F32, SWAP>;
@@ -817,48 +882,65 @@ __device__ __forceinline__ void stage_role(const Params &p, const Smem<F32, SWAP
     }
 }
 
-// Epilogue warp: leaf rounding and the merge tree for one row and BN/2
+// Epilogue warp: leaf rounding and the merge tree for one row and BN/GROUPS
 // columns of every tile.
 //
 // The tree is walked block by block (det_gemm_block_schedule): a block's
-// two to four leaves are rounded and merged in registers in straight-line
+// one to four leaves are rounded and merged in registers in straight-line
 // code, then the block's value is merged with the pending partials its
-// entry names and parked (one TMEM or scratch access) or written out as the
-// root. The code stays small so that the loop, rare branches included,
-// lives in the instruction cache.
+// entry names and parked (one TMEM, shared or scratch access) or written
+// out as the root.
+//
+// Leaves stream through one set of staging registers: taking a leaf waits
+// for its TMEM load, hands the accumulator back to the MMA, rounds the leaf
+// and at once starts the wait and the load of the next leaf, so that the
+// load runs under the merges that follow. The load in flight is landed
+// before the loop goes on to the next block.
 template <bool F32, bool GROUPED, bool SWAP>
 __device__ __forceinline__ void epilogue_role(const Params &p, const Smem<F32, SWAP> &S, int warp, int lane)
 {
     using C = Cfg<F32, SWAP>;
+    constexpr int W = C::WORDS;
+    using Val = ValW<W>;
     const int q = warp & 3;               // TMEM lane quadrant (rows 32q .. 32q+31)
-    const int cq = warp >> 2;             // column group of the tile (a quarter, or a half when SWAP)
+    const int cq = warp >> 2;             // column group of the tile
     const uint32_t lane_bits = static_cast<uint32_t>(q * 32) << 16;
     const uint32_t acc0 = S.tmem + lane_bits + static_cast<uint32_t>(cq * C::COLS);
     EpiCtx c;
     c.tmem_slot = S.tmem + lane_bits + static_cast<uint32_t>(C::TMEM_SLOT_BASE + cq * C::WORDS);
-    c.smem_slot = S.sSlots + static_cast<uint32_t>((warp * 32 + lane) * C::LINE);
+    c.smem_line = S.slots + (warp * 32 + lane) * C::LINE;
     c.scratch = static_cast<uint8_t *>(p.scratch) + static_cast<long long>(blockIdx.x) * C::SCRATCH_CTA_BYTES +
                 (warp * 32 + lane) * C::LINE;
     c.lane = lane;
     const int units = p.units;
     const int NB = p.num_blocks;
+    const int my_units = blockIdx.x < units ? (units - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+    int to_load = my_units * p.num_leaves;   // leaves of this CTA whose load is not yet started
 
     Val A, B, Cc;
-    uint32_t stg[32];
-    int acc = 0;                          // accumulator of the next leaf
+    uint32_t stg[C::COLS];                // the leaf in flight, FP32
+    int acc = 0;                          // its accumulator
     uint32_t acc_phase = 0;
     bool ok = true;
-    // Waits for the next leaf's accumulator, loads it, hands it back to the
-    // MMA (which may then fill it with the leaf NACC ahead) and rounds the
-    // leaf into dst.
-    auto take = [&](Val &dst) {
-        const bool got = wait_bounded(S.accf(acc), acc_phase, S.abort_flag, p.status, p.timeout_ns, true);
-        if (!__all_sync(0xFFFFFFFFu, got)) {
-            ok = false;
-            return;
+    // Waits for the accumulator of the next leaf and starts loading it. The
+    // load itself is issued unconditionally, so that the staging registers
+    // have a single definition on every path: past the stream's last leaf
+    // (or once the CTA is aborting) it reads an accumulator that is never
+    // used.
+    auto issue = [&]() {
+        if (ok && to_load > 0) {
+            const bool got = wait_bounded(S.accf(acc), acc_phase, S.abort_flag, p.status, p.timeout_ns, true);
+            ok = __all_sync(0xFFFFFFFFu, got);
         }
+        --to_load;
         tc_fence_after();
-        stage_load<F32>(acc0 + static_cast<uint32_t>(acc * C::BN), stg);
+        stage_issue<C::COLS>(acc0 + static_cast<uint32_t>(acc * C::BN), stg);
+    };
+    // The leaf in flight -> dst, rounded; its accumulator goes back to the
+    // MMA (which may then fill it with the leaf NACC ahead) and the next
+    // leaf's load starts.
+    auto take = [&](Val &dst) {
+        stage_land<C::COLS>(stg);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(S.acce(acc));
@@ -866,13 +948,37 @@ __device__ __forceinline__ void epilogue_role(const Params &p, const Smem<F32, S
             acc = 0;
             acc_phase ^= 1u;
         }
-        stage_convert<F32>(stg, dst);
+        stage_convert<F32, W>(stg, dst);
+        issue();
     };
     auto add = [](Val &left, const Val &right) {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) left[i] = merge<F32>(left[i], right[i]);
+        for (int i = 0; i < W; ++i) left[i] = merge<F32>(left[i], right[i]);
     };
 
+    // The leaves of one block merged in registers in straight-line code,
+    // one copy per block size. What follows the block (the pending
+    // partials its entry names, then parking or storing) is shared by all
+    // sizes: four copies of it overflow the registers of the transposed
+    // tile.
+    auto block = [&](auto nc) {
+        constexpr int N = decltype(nc)::value;
+        // N = 1: A = l0          N = 2: A = l0 + l1
+        // N = 3: A = l0 + (l1 + l2)     N = 4: A = (l0 + l1) + (l2 + l3)
+        take(A);
+        if constexpr (N >= 2) take(B);
+        if constexpr (N == 4) {
+            add(A, B);
+            take(B);
+        }
+        if constexpr (N >= 3) {
+            take(Cc);
+            add(B, Cc);
+        }
+        if constexpr (N >= 2) add(A, B);
+    };
+
+    issue();
     for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
         const Problem &pb = p.prob[GROUPED ? problem_of(p, u) : 0];
         const int ul = u - pb.first_unit;
@@ -890,42 +996,33 @@ __device__ __forceinline__ void epilogue_role(const Params &p, const Smem<F32, S
             c.out = static_cast<uint8_t *>(pb.out);
             c.ldo = pb.ldo;
         }
-        for (int b = 0; b < NB; ++b) {
+        for (int b = 0; ok && b < NB; ++b) {
             const uint32_t e = p.blocks[b];
-            const int n = static_cast<int>((e >> 10) & 3u) + 1;   // leaves in the block
-            // n = 1: A = l0          n = 2: A = l0 + l1
-            // n = 3: A = l0 + (l1 + l2)     n = 4: A = (l0 + l1) + (l2 + l3)
-            take(A);
-            if (n >= 2) take(B);
-            if (n == 4) {
-                add(A, B);
-                take(B);
+            switch ((e >> 10) & 3u) {   // leaves in the block, minus one
+            case 0: block(std::integral_constant<int, 1>{}); break;
+            case 1: block(std::integral_constant<int, 2>{}); break;
+            case 2: block(std::integral_constant<int, 3>{}); break;
+            default: block(std::integral_constant<int, 4>{}); break;
             }
-            if (n >= 3) {
-                take(Cc);
-                add(B, Cc);
-            }
-            if (!ok) return;
-            if (n >= 2) add(A, B);
+            if (!ok) break;
             // merge with the pending left siblings above the block, lowest first
 #pragma unroll 1
-            for (uint32_t m = (e & 0x3FFu) >> C::TMEM_FIRST, s = C::TMEM_FIRST; m != 0; m >>= 1, ++s) {
-                if (!(m & 1u)) continue;
-                load_slot<F32, SWAP>(static_cast<int>(s), B, c);   // B is free once the block is merged
-#pragma unroll
-                for (int i = 0; i < 16; ++i) A[i] = merge<F32>(B[i], A[i]);
-            }
+            for (uint32_t m = (e & 0x3FFu) >> C::TMEM_FIRST, s = C::TMEM_FIRST; m != 0; m >>= 1, ++s)
+                if (m & 1u) merge_slot<F32, SWAP, W>(static_cast<int>(s), A, B, c);
             const int st = static_cast<int>(e >> 12);
             if (st == kSlotRoot) {
-                store_out<F32, SWAP>(A, p, c);
+                store_out<F32, SWAP, W>(A, p, c);
                 if constexpr (GROUPED && !F32) {
-                    if (pb.rd_part != nullptr) row_partial(A, p, pb, c, nt, cq);
+                    if (pb.rd_part != nullptr) row_partial<W>(A, p, pb, c, nt, cq);
                 }
             } else {
-                store_slot<F32, SWAP>(st, A, c);
+                store_slot<F32, SWAP, W>(st, A, c);
             }
+            // the next leaf's load lands before the loop goes round
+            stage_land<C::COLS>(stg);
         }
     }
+    tmem_wait_ld();   // nothing of this thread's may still be loading when TMEM is freed
 }
 
 template <int A_MAJOR, int B_MAJOR, bool F32, bool GROUPED, bool SWAP>
@@ -943,7 +1040,7 @@ __global__ void __launch_bounds__(Cfg<F32, SWAP>::THREADS, 1) det_gemm_kernel(co
     Smem<F32, SWAP> S;
     S.sA = base + C::OFF_A;
     S.sB = base + C::OFF_B;
-    S.sSlots = base + C::OFF_SLOTS;
+    S.slots = smem + C::OFF_SLOTS;
     S.bar0 = base + C::OFF_BAR;
     uint32_t *tmem_base_smem = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
     S.abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
@@ -985,9 +1082,9 @@ __global__ void __launch_bounds__(Cfg<F32, SWAP>::THREADS, 1) det_gemm_kernel(co
     S.tmem = *tmem_base_smem;
 
     if constexpr (!SWAP) {
-        // Register split: the stage warpgroup gives up registers and the four
-        // epilogue warpgroups take them (kProdRegs*128 + kEpiRegs*512 fits in
-        // the kLaunchRegs*640 the CTA is launched with). Each role's code sits
+        // Register split: the stage warpgroup gives up registers and the two
+        // epilogue warpgroups take them (kProdRegs*128 + kEpiRegs*256 fits in
+        // the kLaunchRegs*384 the CTA is launched with). Each role's code sits
         // inside its own branch so that the compiler allocates it under the
         // matching limit.
         static_assert(kProdRegs * 128 + kEpiRegs * 32 * C::EPI_WARPS <= kLaunchRegs * C::THREADS, "register split");
