@@ -51,7 +51,7 @@ struct Problem {
     CUtensorMap tmap_b;           // "B operand": contraction x output columns
     void *out;                    // row-major output, rows x cols
     long long ldo;                // output leading dimension, elements
-    float *rd_part;               // row reduction: per (column tile, quarter) partials [4 n_tiles][rows], or null
+    float *rd_part;               // row reduction: per 32-column group partials [groups][rows], or null
     const uint16_t *rd_d;         // row reduction: the BF16 [rows, cols] operand D, row pitch rd_ldd
     long long rd_ldd;
     int rows;                     // output rows
@@ -68,7 +68,8 @@ struct Params {
     Problem prob[kMaxProblems];
     int num_problems;
     int units;                    // work units of the launch (all problems)
-    void *scratch;                // deep-slot scratch: grid x VariantOps::scratch_cta_bytes
+    void *scratch;                // deep-slot scratch: grid x scratch_cta_bytes
+    long long scratch_cta_bytes;  // one CTA's part of it: the global slots this launch's tree reaches
     int *status;                  // device status word (first int = code)
     unsigned long long timeout_ns;
     int cols, kc;
@@ -88,7 +89,8 @@ struct VariantOps {
     cudaError_t (*launch)(const Params &p, int grid, cudaStream_t stream);
     int bn;                       // output columns per tile
     int smem_bytes;
-    int scratch_cta_bytes;        // global scratch each CTA needs for its deep slots
+    int slot_bytes;               // bytes of one pending-partial slot of a whole CTA
+    int global_first;             // first slot kept in global scratch (lower slots: TMEM, shared memory)
     int split_regs;               // registers per thread the kernel must be built with (0: no register split)
     bool swap;                    // transposed tile: the kernel's rows are the output's columns
 };
@@ -107,8 +109,10 @@ cudaError_t launch_merge_list(bool f32, const void *const *parts, int n, int row
                               long long ldo, cudaStream_t stream);
 
 // Row reduction of a grouped launch: rowdot[i] = the partials of row i
-// (four per column tile, written by the kernel) combined in a fixed order.
-cudaError_t launch_rowdot_reduce(const float *part, int rows, int n_tiles, float *rowdot, cudaStream_t stream);
+// (one per 32-column group, n_groups of them, written by the kernel)
+// combined in a fixed order over n_tiles 128-column tiles.
+cudaError_t launch_rowdot_reduce(const float *part, int rows, int n_tiles, int n_groups, float *rowdot,
+                                 cudaStream_t stream);
 
 // Batch-invariant RMSNorm (det_rmsnorm): one warp per row.
 struct RmsParams {
@@ -122,8 +126,18 @@ struct RmsParams {
 constexpr int kRmsWarps = 8;      // rows per CTA
 cudaError_t launch_rmsnorm(const RmsParams &p, cudaStream_t stream);
 
-// Largest scratch_cta_bytes over all variants (bf16: 3 slots x 32 KiB).
-constexpr int kMaxScratchCtaBytes = 3 * 32768;
+// Global scratch one CTA needs: the slots at or above ops.global_first that
+// a block schedule of `count` entries parks a partial in.
+inline size_t scratch_cta_bytes(const VariantOps &ops, const uint16_t *blocks, long long count)
+{
+    int top = -1;   // highest slot written
+    for (long long i = 0; i < count; ++i) {
+        const int dst = blocks[i] >> 12;
+        if (dst != kSlotRoot && dst > top) top = dst;
+    }
+    const int n = top >= ops.global_first ? top + 1 - ops.global_first : 0;
+    return static_cast<size_t>(n) * static_cast<size_t>(ops.slot_bytes);
+}
 
 VariantOps ops_bf16_kmn();
 VariantOps ops_bf16_kk();
