@@ -25,11 +25,12 @@
 //   The stage warpgroup runs on 72 registers per thread and the epilogue
 //   warps on 216 (setmaxnreg).
 //
-// Tile: 128 x 128 outputs. Wider tiles (192 or 256 columns) give each MMA
-// more work for the same issue cost, but leave TMEM too little room for
-// three accumulators and the tree's pending partials, and the epilogue
-// then spends more time moving partials through shared and global memory
-// than the MMAs save; measured on GB300, 128 columns were faster.
+// Tile: 128 x 128 outputs (128 x 64 for FP32 output). Wider tiles (192 or
+// 256 columns) give each MMA more work for the same issue cost, but leave
+// TMEM too little room for three accumulators and the tree's pending
+// partials, and the epilogue then spends more time moving partials through
+// shared and global memory than the MMAs save; measured on GB300, these
+// widths were faster.
 //
 // Transposed tile (launches with at most 64 output rows, BF16 out): the
 // MMA's A operand is the weight, so its 128 TMEM lanes are 128 output
@@ -89,10 +90,14 @@ template <bool F32, bool SWAP = false>
 struct Cfg {
     static constexpr int EPI_WARPS = SWAP ? 8 : kEpiWarps;   // epilogue warps
     static constexpr int GROUPS = EPI_WARPS / 4;        // epilogue warps per TMEM lane quadrant
-    static constexpr int BN = SWAP ? 64 : 128;          // output columns per tile (rows when SWAP)
-    static constexpr int NACC = SWAP ? 4 : (F32 ? 2 : 3);     // TMEM accumulator buffers
+    // Output columns per tile (rows when SWAP). The fp32 tile is half as
+    // wide as the bf16 one: its values take twice the bytes, and at 128
+    // columns moving its pending partials cost more than the wider MMAs
+    // saved.
+    static constexpr int BN = (SWAP || F32) ? 64 : 128;
+    static constexpr int NACC = (SWAP || F32) ? 4 : 3;  // TMEM accumulator buffers
     // Shared-memory ring depth, one ring slot per active stage warp.
-    static constexpr int STAGES = SWAP ? 4 : (F32 ? 3 : 4);
+    static constexpr int STAGES = 4;
     static constexpr int A_STAGE = kBM * kBK * 2;       // bytes of one A stage
     static constexpr int B_STAGE = BN * kBK * 2;        // bytes of one B stage
     static constexpr int STAGE_TX = A_STAGE + B_STAGE;  // TMA bytes per stage with full boxes
@@ -109,7 +114,7 @@ struct Cfg {
     static constexpr int TMEM_SLOTS =
         TMEM_SLOTS_FIT < kMaxSlots - TMEM_FIRST ? TMEM_SLOTS_FIT : kMaxSlots - TMEM_FIRST;
     static constexpr int SMEM_FIRST = TMEM_FIRST + TMEM_SLOTS;
-    static constexpr int SMEM_SLOTS = SWAP ? 0 : (F32 ? 2 : 3);
+    static constexpr int SMEM_SLOTS = SWAP ? 0 : 3;
     static constexpr int GLOBAL_FIRST = SMEM_FIRST + SMEM_SLOTS;
     static constexpr int GLOBAL_SLOTS = kMaxSlots - GLOBAL_FIRST;
     static constexpr int LINE = WORDS * 4;              // bytes of one value of one thread
