@@ -265,10 +265,8 @@ det_gemm_status det_rmsnorm(const det_gemm_bf16 *x, const det_gemm_bf16 *w, det_
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress) and initialises the library's state for that
  *     device; make that first call before any stream capture.
- *   - The array holds scratch for 160 CTAs (one per SM up to 160 SMs) at
- *     the longest contraction. A launch whose CTAs would need more runs on
- *     as many CTAs as the array holds (same bits, fewer SMs); one that
- *     cannot fit even one CTA is rejected with DET_GEMM_ERR_INVALID_ARG
+ *   - The array holds scratch for 160 CTAs (one per SM up to 160 SMs). A
+ *     launch that would need more is rejected with DET_GEMM_ERR_INVALID_ARG
  *     before anything is enqueued (det_gemm_last_error_detail says why).
  *   - Every call shares the array and nothing in it needs to start at zero
  *     (each pending partial is written before it is read). Calls that

@@ -490,7 +490,7 @@ det_gemm_status run_problems(Variant v, bool a_kmajor, bool b_kmajor, const Prob
         if (q.rowdot) {
             pb.rd_d = static_cast<const uint16_t *>(q.d);
             pb.rd_ldd = q.ldd;
-            rd_bytes += align256(sizeof(float) * (ops.bn / 32) * n_tiles * q.rows);
+            rd_bytes += align256(sizeof(float) * 4 * n_tiles * q.rows);
         }
     }
     if (units > (int64_t{1} << 31) - 1) return DET_GEMM_ERR_INVALID_ARG;
@@ -503,53 +503,25 @@ det_gemm_status run_problems(Variant v, bool a_kmajor, bool b_kmajor, const Prob
     const int64_t part_ld = (out_cols + 7) / 8 * 8;
     const size_t part_bytes =
         parts > 1 ? align256(static_cast<size_t>(parts) * out_rows * part_ld * pa[0].out.esize) : 0;
-    if (blocks) {
-        p.num_blocks = static_cast<int>(blocks->count);
-        std::memcpy(p.blocks, blocks->entries, sizeof(uint16_t) * blocks->count);
-    } else {
-        int64_t nb = 0;
-        build_blocks(Lp, p.blocks, &nb);
-        p.num_blocks = static_cast<int>(nb);
-    }
-    // One CTA's deep slots: only those the tree of Lp leaves reaches.
-    const size_t cta_bytes = scratch_cta_bytes(ops, p.blocks, p.num_blocks);
-    p.scratch_cta_bytes = static_cast<long long>(cta_bytes);
-    int grid = static_cast<int>(units < st->sm_count ? units : st->sm_count);
     if (fixed_scratch) {
-        // The fixed array holds the deep slots of this many CTAs at most;
-        // the persistent kernel then runs on fewer SMs (same bits: which
-        // CTA computes a tile changes only the timing).
-        if (cta_bytes > 0) {
-            const size_t fit = fixed_bytes / cta_bytes;
-            if (fit == 0) {
-                std::snprintf(g_detail, sizeof g_detail,
-                              "one CTA needs %zu bytes of scratch; the fixed scratch holds %zu", cta_bytes,
-                              fixed_bytes);
-                return DET_GEMM_ERR_INVALID_ARG;
-            }
-            if (static_cast<size_t>(grid) > fit) grid = static_cast<int>(fit);
-        }
         p.scratch = fixed_scratch;
     } else {
         int dev = 0;
         cudaGetDevice(&dev);
-        // The deep-slot part (one CTA's slots per SM), then the part slabs
-        // of a split launch and the row-reduction partials. The buffer only
-        // grows, so launches on this stream mostly reuse it.
-        const size_t slot_bytes = align256(static_cast<size_t>(st->sm_count) * cta_bytes);
-        const size_t total = slot_bytes + part_bytes + rd_bytes;   // 0: the launch needs no scratch
-        uint8_t *base = nullptr;
-        if (total > 0) {
-            base = static_cast<uint8_t *>(scratch_for(dev, stream, total));
-            if (!base) return DET_GEMM_ERR_LAUNCH;
-        }
+        // The deep-slot part is sized for the largest variant and a grid of
+        // one CTA per SM, so every launch on this stream can reuse it; the
+        // part slabs of a split launch and the row-reduction partials
+        // follow it.
+        const size_t slot_bytes = static_cast<size_t>(st->sm_count) * kMaxScratchCtaBytes;
+        uint8_t *base = static_cast<uint8_t *>(scratch_for(dev, stream, slot_bytes + part_bytes + rd_bytes));
+        if (!base) return DET_GEMM_ERR_LAUNCH;
         p.scratch = base;
         p.part_out = parts > 1 ? base + slot_bytes : nullptr;
         uint8_t *rd = base + slot_bytes + part_bytes;
         for (int i = 0; i < g; ++i) {
             if (!pa[i].rowdot || pa[i].rows == 0) continue;
             p.prob[i].rd_part = reinterpret_cast<float *>(rd);
-            rd += align256(sizeof(float) * (ops.bn / 32) * n_tiles * pa[i].rows);
+            rd += align256(sizeof(float) * 4 * n_tiles * pa[i].rows);
         }
     }
     p.parts = parts;
@@ -561,7 +533,23 @@ det_gemm_status run_problems(Variant v, bool a_kmajor, bool b_kmajor, const Prob
     p.kc = static_cast<int>(kc);
     p.num_leaves = static_cast<int>(Lp);
     p.force_timeout = g_force_timeout;
+    if (blocks) {
+        p.num_blocks = static_cast<int>(blocks->count);
+        std::memcpy(p.blocks, blocks->entries, sizeof(uint16_t) * blocks->count);
+    } else {
+        int64_t nb = 0;
+        build_blocks(Lp, p.blocks, &nb);
+        p.num_blocks = static_cast<int>(nb);
+    }
 
+    const int grid = static_cast<int>(units < st->sm_count ? units : st->sm_count);
+    if (fixed_scratch && static_cast<size_t>(grid) * static_cast<size_t>(ops.scratch_cta_bytes) > fixed_bytes) {
+        std::snprintf(g_detail, sizeof g_detail,
+                      "this launch needs %zu bytes of scratch (%d CTAs x %d); the fixed scratch holds %zu",
+                      static_cast<size_t>(grid) * static_cast<size_t>(ops.scratch_cta_bytes), grid,
+                      ops.scratch_cta_bytes, fixed_bytes);
+        return DET_GEMM_ERR_INVALID_ARG;
+    }
     const cudaError_t le = ops.launch(p, grid, stream);
     if (le != cudaSuccess) return fail_cuda(DET_GEMM_ERR_LAUNCH, le, "kernel launch");
     if (parts > 1) {
@@ -572,9 +560,7 @@ det_gemm_status run_problems(Variant v, bool a_kmajor, bool b_kmajor, const Prob
     }
     for (int i = 0; i < g; ++i) {
         if (!pa[i].rowdot || pa[i].rows == 0) continue;
-        const cudaError_t re =
-            launch_rowdot_reduce(p.prob[i].rd_part, p.prob[i].rows, static_cast<int>((cols + 127) / 128),
-                                 static_cast<int>((cols + 31) / 32), pa[i].rowdot, stream);
+        const cudaError_t re = launch_rowdot_reduce(p.prob[i].rd_part, p.prob[i].rows, p.n_tiles, pa[i].rowdot, stream);
         if (re != cudaSuccess) return fail_cuda(DET_GEMM_ERR_LAUNCH, re, "row reduction launch");
     }
     return DET_GEMM_OK;

@@ -17,14 +17,9 @@ constexpr int kMaxSlots = 10;             // ceil(log2(kMaxLeaves)) pending part
 constexpr int kBM = 128;                  // output rows per tile (one TMEM lane per row)
 constexpr int kBK = 64;                   // contraction elements per shared-memory stage (two leaves)
 constexpr int kStageWarps = 4;            // TMA copies and MMAs of the K-stages: one per SM sub-partition
-constexpr int kEpiWarps = 8;              // epilogue warps of the plain tile (a multiple of 4)
-// Registers per thread at launch: the most a CTA of the plain tile's
-// threads can have at one CTA per SM, and the register split between the
-// stage warpgroup and the epilogue warps (setmaxnreg), which redistributes
-// exactly the launch's registers.
-constexpr int kLaunchRegs = (65536 / (32 * (kEpiWarps + kStageWarps))) & ~7;
-constexpr int kProdRegs = kEpiWarps == 8 ? 72 : 40;
-constexpr int kEpiRegs = (kLaunchRegs * 32 * (kEpiWarps + kStageWarps) - kProdRegs * 32 * kStageWarps) / (32 * kEpiWarps) & ~7;
+constexpr int kLaunchRegs = 96;           // registers per thread at launch of the plain tile's 640 threads
+constexpr int kProdRegs = 40;             // stage warpgroup after setmaxnreg
+constexpr int kEpiRegs = 104;             // epilogue warpgroups after setmaxnreg
 
 // Operand major-ness as seen by the MMA: K-major = contraction contiguous.
 enum Major { kKMajor = 0, kMNMajor = 1 };
@@ -51,7 +46,7 @@ struct Problem {
     CUtensorMap tmap_b;           // "B operand": contraction x output columns
     void *out;                    // row-major output, rows x cols
     long long ldo;                // output leading dimension, elements
-    float *rd_part;               // row reduction: per 32-column group partials [groups][rows], or null
+    float *rd_part;               // row reduction: per (column tile, quarter) partials [4 n_tiles][rows], or null
     const uint16_t *rd_d;         // row reduction: the BF16 [rows, cols] operand D, row pitch rd_ldd
     long long rd_ldd;
     int rows;                     // output rows
@@ -68,8 +63,7 @@ struct Params {
     Problem prob[kMaxProblems];
     int num_problems;
     int units;                    // work units of the launch (all problems)
-    void *scratch;                // deep-slot scratch: grid x scratch_cta_bytes
-    long long scratch_cta_bytes;  // one CTA's part of it: the global slots this launch's tree reaches
+    void *scratch;                // deep-slot scratch: grid x VariantOps::scratch_cta_bytes
     int *status;                  // device status word (first int = code)
     unsigned long long timeout_ns;
     int cols, kc;
@@ -89,8 +83,7 @@ struct VariantOps {
     cudaError_t (*launch)(const Params &p, int grid, cudaStream_t stream);
     int bn;                       // output columns per tile
     int smem_bytes;
-    int slot_bytes;               // bytes of one pending-partial slot of a whole CTA
-    int global_first;             // first slot kept in global scratch (lower slots: TMEM, shared memory)
+    int scratch_cta_bytes;        // global scratch each CTA needs for its deep slots
     int split_regs;               // registers per thread the kernel must be built with (0: no register split)
     bool swap;                    // transposed tile: the kernel's rows are the output's columns
 };
@@ -109,10 +102,8 @@ cudaError_t launch_merge_list(bool f32, const void *const *parts, int n, int row
                               long long ldo, cudaStream_t stream);
 
 // Row reduction of a grouped launch: rowdot[i] = the partials of row i
-// (one per 32-column group, n_groups of them, written by the kernel)
-// combined in a fixed order over n_tiles 128-column tiles.
-cudaError_t launch_rowdot_reduce(const float *part, int rows, int n_tiles, int n_groups, float *rowdot,
-                                 cudaStream_t stream);
+// (four per column tile, written by the kernel) combined in a fixed order.
+cudaError_t launch_rowdot_reduce(const float *part, int rows, int n_tiles, float *rowdot, cudaStream_t stream);
 
 // Batch-invariant RMSNorm (det_rmsnorm): one warp per row.
 struct RmsParams {
@@ -126,18 +117,8 @@ struct RmsParams {
 constexpr int kRmsWarps = 8;      // rows per CTA
 cudaError_t launch_rmsnorm(const RmsParams &p, cudaStream_t stream);
 
-// Global scratch one CTA needs: the slots at or above ops.global_first that
-// a block schedule of `count` entries parks a partial in.
-inline size_t scratch_cta_bytes(const VariantOps &ops, const uint16_t *blocks, long long count)
-{
-    int top = -1;   // highest slot written
-    for (long long i = 0; i < count; ++i) {
-        const int dst = blocks[i] >> 12;
-        if (dst != kSlotRoot && dst > top) top = dst;
-    }
-    const int n = top >= ops.global_first ? top + 1 - ops.global_first : 0;
-    return static_cast<size_t>(n) * static_cast<size_t>(ops.slot_bytes);
-}
+// Largest scratch_cta_bytes over all variants (bf16: 3 slots x 32 KiB).
+constexpr int kMaxScratchCtaBytes = 3 * 32768;
 
 VariantOps ops_bf16_kmn();
 VariantOps ops_bf16_kk();

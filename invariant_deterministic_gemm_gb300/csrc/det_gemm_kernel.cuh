@@ -12,25 +12,16 @@
 // invariance bullet). One tile shape per variant, whatever M is: choosing a
 // kernel by problem shape is what breaks batch invariance (section "Why").
 //
-// CTA layout (384 threads, one CTA per SM, persistent over output tiles):
-//   warps 0-7  epilogue: warp w reads TMEM lanes 32*(w%4).. (rows) and the
-//              column half w/4 of the tile; each thread owns one row and
-//              BN/2 columns, and keeps the tree's pending partials for them.
-//   warps 8-11 stage warps, one per scheduler: warp 8+j (j < STAGES) owns
-//              ring slot j and the K-stages g = j (mod STAGES) of the CTA's
-//              tile sequence. It copies the stage's A and B tiles in with
-//              TMA, then issues the stage's MMAs; MMA issue is handed from
-//              warp to warp in stage order (turn barriers). Warp 9 also
-//              allocates and frees TMEM.
-//   The stage warpgroup runs on 72 registers per thread and the epilogue
-//   warps on 216 (setmaxnreg).
-//
-// Tile: 128 x 128 outputs (128 x 64 for FP32 output). Wider tiles (192 or
-// 256 columns) give each MMA more work for the same issue cost, but leave
-// TMEM too little room for three accumulators and the tree's pending
-// partials, and the epilogue then spends more time moving partials through
-// shared and global memory than the MMAs save; measured on GB300, these
-// widths were faster.
+// CTA layout (640 threads, one CTA per SM, persistent over output tiles):
+//   warps 0-15 epilogue: warp w reads TMEM lanes 32*(w%4).. (rows) and the
+//              column quarter w/4 of the tile; each thread owns one row and
+//              BN/4 columns, and keeps the tree's pending partials for them.
+//              Four epilogue warps per scheduler hide each other's waits.
+//   warps 16-19 stage warps, one per scheduler: warp 16+j owns ring slot j
+//              and the K-stages g = j (mod 4) of the CTA's tile sequence. It
+//              copies the stage's A and B tiles in with TMA, then issues the
+//              stage's MMAs; MMA issue is handed from warp to warp in stage
+//              order (turn barriers). Warp 17 also allocates and frees TMEM.
 //
 // Transposed tile (launches with at most 64 output rows, BF16 out): the
 // MMA's A operand is the weight, so its 128 TMEM lanes are 128 output
@@ -41,24 +32,22 @@
 // later stages into L2.
 //
 // Per tile: 64-wide K stages (two leaves) of the A and B operand tiles go
-// through a ring of STAGES swizzled shared-memory slots. For leaf l the
-// stage warp issues two K=16 MMAs into accumulator buffer l % NACC (the
-// first one overwrites, so each leaf starts from zero) and commits to that
-// buffer's "full" barrier. The epilogue loads the leaf in chunks of 16
-// columns, frees the buffer as soon as the last chunk has landed (so the
-// MMAs can run NACC-1 leaves ahead), rounds it (bf16 variant) and merges
-// it into its pending partials following the block schedule, and writes
-// the root after the last leaf.
+// through a ring of four swizzled shared-memory slots. For leaf l the stage
+// warp issues two K=16 MMAs into accumulator buffer l % NACC (the first one
+// overwrites, so each leaf starts from zero) and commits to that buffer's
+// "full" barrier. The epilogue loads the leaf, frees the buffer at once (so
+// the MMAs can run NACC-1 leaves ahead), rounds it (bf16 variant) and merges
+// it into its pending partials following the block schedule, and writes the
+// root after the last leaf.
 //
 // Pending partials ("slots"): slot s holds the finished left child of a tree
 // node of height s + 1, so at most ceil(log2 L) <= 10 are live, and slot s
 // is written at most once per 2^(s+1) leaves. The epilogue evaluates the
 // tree's maximal subtrees of at most four leaves ("blocks", height <= 2)
 // entirely in registers, so only slots 2 and up ever hold a value: the
-// next slots are TMEM columns past the accumulators, then shared-memory
-// slots, and the rest (touched at most once per 64 leaves) a per-CTA
-// global-memory scratch line per thread, sized on the host for the slots
-// the launch's tree reaches.
+// next slots are TMEM columns past the accumulators, then shared memory,
+// and the last three (touched at most once per 256 leaves) a per-CTA
+// global-memory scratch line of 128 bytes per thread.
 //
 // Every mbarrier wait is bounded (Params::timeout_ns of %globaltimer). On
 // expiry the waiter records DET_GEMM_ERR_TIMEOUT in the status word and sets
@@ -66,8 +55,6 @@
 // loads and MMAs are drained with bounded waits, TMEM is released and the
 // CTA exits.
 #pragma once
-
-#include <type_traits>
 
 #include "det_gemm_internal.h"
 
@@ -88,24 +75,16 @@ constexpr int kPrefetchRounds = 2;  // transposed tile: L2 prefetch distance, in
 // against the plain tile on the GPU).
 template <bool F32, bool SWAP = false>
 struct Cfg {
-    static constexpr int EPI_WARPS = SWAP ? 8 : kEpiWarps;   // epilogue warps
+    static constexpr int EPI_WARPS = SWAP ? 8 : 16;     // epilogue warps
     static constexpr int GROUPS = EPI_WARPS / 4;        // epilogue warps per TMEM lane quadrant
-    // Output columns per tile (rows when SWAP). The fp32 tile is half as
-    // wide as the bf16 one: its values take twice the bytes, and at 128
-    // columns moving its pending partials cost more than the wider MMAs
-    // saved.
-    static constexpr int BN = (SWAP || F32) ? 64 : 128;
-    static constexpr int NACC = (SWAP || F32) ? 4 : 3;  // TMEM accumulator buffers
-    // Shared-memory ring depth, one ring slot per active stage warp.
-    static constexpr int STAGES = 4;
+    static constexpr int BN = SWAP ? 64 : (F32 ? 64 : 128);   // output columns per tile (rows when SWAP)
+    static constexpr int NACC = SWAP ? 4 : (F32 ? 4 : 3);     // TMEM accumulator buffers
+    static constexpr int STAGES = kStageWarps;          // shared-memory ring depth: one slot per stage warp
     static constexpr int A_STAGE = kBM * kBK * 2;       // bytes of one A stage
     static constexpr int B_STAGE = BN * kBK * 2;        // bytes of one B stage
     static constexpr int STAGE_TX = A_STAGE + B_STAGE;  // TMA bytes per stage with full boxes
     static constexpr int COLS = BN / GROUPS;            // accumulator columns per epilogue thread
-    static constexpr int WORDS = F32 ? COLS : COLS / 2; // 32-bit words per value per thread
-    static constexpr int CHUNK = 16;                    // accumulator columns per TMEM load
-    static constexpr int NCH = COLS / CHUNK;            // TMEM loads per leaf and thread
-    static constexpr int CHUNK_WORDS = F32 ? CHUNK : CHUNK / 2;   // words one load yields
+    static constexpr int WORDS = F32 ? COLS : COLS / 2; // 32-bit words per value per thread (16)
     static constexpr int TMEM_COLS = 512;
     static constexpr int TMEM_SLOT_BASE = NACC * BN;    // after the accumulators
     static constexpr int TMEM_SLOT_STRIDE = WORDS * GROUPS;   // TMEM columns of one slot
@@ -114,20 +93,19 @@ struct Cfg {
     static constexpr int TMEM_SLOTS =
         TMEM_SLOTS_FIT < kMaxSlots - TMEM_FIRST ? TMEM_SLOTS_FIT : kMaxSlots - TMEM_FIRST;
     static constexpr int SMEM_FIRST = TMEM_FIRST + TMEM_SLOTS;
-    static constexpr int SMEM_SLOTS = SWAP ? 0 : 3;
+    static constexpr int SMEM_SLOTS = SWAP ? 0 : (F32 ? 2 : 3);
     static constexpr int GLOBAL_FIRST = SMEM_FIRST + SMEM_SLOTS;
     static constexpr int GLOBAL_SLOTS = kMaxSlots - GLOBAL_FIRST;
-    static constexpr int LINE = WORDS * 4;              // bytes of one value of one thread
-    static constexpr int CHUNKS = LINE / 16;            // 16-byte chunks of a line
+    static constexpr int LINE = WORDS * 4;              // bytes of one value of one thread (64)
     static constexpr int SLOT_BYTES = EPI_WARPS * 32 * LINE;   // one slot for the whole CTA
+    static constexpr int SCRATCH_CTA_BYTES = GLOBAL_SLOTS * SLOT_BYTES;
 
     // Warp roles: epilogue warps first, then the stage warps.
     static constexpr int FIRST_STAGE_WARP = EPI_WARPS;
     static constexpr int TMEM_WARP = EPI_WARPS + 1;     // allocates and frees TMEM
     static constexpr int THREADS = 32 * (EPI_WARPS + kStageWarps);
-    // Registers per thread at launch (the most 384 threads of one CTA per SM
-    // can have); the plain tile's register split redistributes exactly
-    // these, the transposed tile needs no split.
+    // Registers per thread at launch: the register split below redistributes
+    // exactly these (plain tile); the transposed tile needs no split.
     static constexpr int LAUNCH_REGS = SWAP ? 0 : kLaunchRegs;
 
     static constexpr int OFF_A = 0;
@@ -143,12 +121,10 @@ struct Cfg {
 
     static_assert(SWAP ? GLOBAL_SLOTS == 0 : GLOBAL_SLOTS >= 1, "slot storage");
     static_assert(!SWAP || !F32, "the transposed tile has a BF16 output only");
-    static_assert(STAGES <= kStageWarps, "one ring slot per active stage warp");
-    static_assert(NCH % 2 == 0, "the leaf's loads alternate between two staging buffers");
+    static_assert(SCRATCH_CTA_BYTES <= kMaxScratchCtaBytes, "scratch");
     static_assert(SMEM_BYTES <= 232448, "shared memory");
     static_assert(A_STAGE % 1024 == 0 && B_STAGE % 1024 == 0, "swizzle atoms");
-    static_assert(WORDS % 16 == 0 && WORDS <= 64, "epilogue values are whole 16-word pieces");
-    static_assert(THREADS * kLaunchRegs <= 65536, "one CTA per SM at the launch register count");
+    static_assert(WORDS == 16, "epilogue values are 16 words per thread");
 };
 
 // ----------------------------------------------------------- PTX helpers
@@ -455,16 +431,15 @@ __device__ __forceinline__ int problem_of(const Params &p, int u)
 
 // ------------------------------------------------------------- epilogue
 
-// Every epilogue value (a rounded leaf, a partial, the root) is W words per
-// thread: 2W BF16 columns packed in pairs, or W FP32 columns.
-template <int W>
-using ValW = uint32_t[W];
+// Every epilogue value (a rounded leaf, a partial, the root) is 16 words per
+// thread: 32 BF16 columns packed in pairs, or 16 FP32 columns.
+using Val = uint32_t[16];
 
 // What one epilogue thread needs to reach its storage.
 struct EpiCtx {
     uint32_t tmem_slot;   // TMEM address of this thread's first TMEM slot
-    uint8_t *smem_line;   // generic address of this thread's line in the first shared slot
-    uint8_t *scratch;     // this thread's line in the first global slot
+    uint32_t smem_slot;   // shared-memory address of this thread's line in the first shared slot
+    uint8_t *scratch;     // this thread's 64-byte line in the first global slot
     int lane;
     int row, col;         // first output element owned by this thread
     int rows;             // rows of the output (the problem's)
@@ -472,17 +447,25 @@ struct EpiCtx {
     long long ldo;        // its leading dimension, elements
 };
 
+// 16-byte chunk k (0..3) of a thread's 64-byte shared-memory line. Lines of
+// consecutive lanes are 64 bytes apart; swizzling the chunk by lane/2 puts
+// the eight lanes of a quarter-warp access on eight distinct bank groups.
+__device__ __forceinline__ uint32_t smem_chunk(uint32_t line, int lane, int k)
+{
+    return line + static_cast<uint32_t>((k ^ ((lane >> 1) & 3)) * 16);
+}
+
 // Writes this thread's value of the root to the output, clipped to the
 // matrix. A row the matrix clips goes element by element through the
-// thread's line of the shared-memory slot, which is free once the root is
-// formed (every pending partial has been merged into it).
+// thread's scratch line, which is free once the root is formed (every
+// pending partial has been merged into it).
 //
 // Transposed tile (SWAP): the thread's TMEM lane is output column c.row and
 // its 32 values are output rows c.col .. c.col+31 of that column; each goes
 // to out[(c.col + j) * ldo + c.row]. The 32 lanes of a warp hold 32
 // consecutive columns, so every store of the warp writes 64 contiguous bytes.
-template <bool F32, bool SWAP, int W>
-__device__ __forceinline__ void store_out(const ValW<W> &v, const Params &p, const EpiCtx &c)
+template <bool F32, bool SWAP>
+__device__ __forceinline__ void store_out(const Val &v, const Params &p, const EpiCtx &c)
 {
     using C = Cfg<F32, SWAP>;
     constexpr int ES = F32 ? 4 : 2;
@@ -491,7 +474,7 @@ __device__ __forceinline__ void store_out(const ValW<W> &v, const Params &p, con
         const int nrows = p.cols - c.col;
         uint16_t *dst = reinterpret_cast<uint16_t *>(c.out) + static_cast<long long>(c.col) * c.ldo + c.row;
 #pragma unroll
-        for (int i = 0; i < W; ++i) {
+        for (int i = 0; i < 16; ++i) {
             if (2 * i < nrows) dst[(2 * i) * c.ldo] = static_cast<uint16_t>(v[i] & 0xFFFFu);
             if (2 * i + 1 < nrows) dst[(2 * i + 1) * c.ldo] = static_cast<uint16_t>(v[i] >> 16);
         }
@@ -501,221 +484,151 @@ __device__ __forceinline__ void store_out(const ValW<W> &v, const Params &p, con
     if (ncols <= 0) return;
     const bool full = ncols >= C::COLS;
     uint8_t *dst = c.out + (static_cast<long long>(c.row) * c.ldo + c.col) * ES;
-    static_assert(SWAP || C::SMEM_SLOTS >= 1, "the clipped row goes through a shared-memory line");
-    if (full) {
+    uint8_t *vec = full ? dst : c.scratch;
 #pragma unroll
-        for (int k = 0; k < W / 4; ++k)
-            asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(dst + 16 * k), "r"(v[4 * k]),
-                         "r"(v[4 * k + 1]), "r"(v[4 * k + 2]), "r"(v[4 * k + 3])
-                         : "memory");
-        return;
-    }
-    uint8_t *line = c.smem_line;
-#pragma unroll
-    for (int k = 0; k < W / 4; ++k)
-        asm volatile("st.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(line + 16 * k), "r"(v[4 * k]), "r"(v[4 * k + 1]),
-                     "r"(v[4 * k + 2]), "r"(v[4 * k + 3])
+    for (int k = 0; k < 4; ++k)
+        asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(vec + 16 * k), "r"(v[4 * k]),
+                     "r"(v[4 * k + 1]), "r"(v[4 * k + 2]), "r"(v[4 * k + 3])
                      : "memory");
+    if (full) return;
 #pragma unroll 1
     for (int j = 0; j < ncols; ++j) {
         if constexpr (F32) {
             uint32_t w;
-            asm volatile("ld.b32 %0, [%1];" : "=r"(w) : "l"(line + 4 * j) : "memory");
+            asm volatile("ld.global.b32 %0, [%1];" : "=r"(w) : "l"(c.scratch + 4 * j) : "memory");
             asm volatile("st.global.b32 [%0], %1;" ::"l"(dst + 4 * j), "r"(w) : "memory");
         } else {
             uint16_t w;
-            asm volatile("ld.u16 %0, [%1];" : "=h"(w) : "l"(line + 2 * j) : "memory");
+            asm volatile("ld.global.u16 %0, [%1];" : "=h"(w) : "l"(c.scratch + 2 * j) : "memory");
             asm volatile("st.global.u16 [%0], %1;" ::"l"(dst + 2 * j), "h"(w) : "memory");
         }
     }
 }
 
 // Row reduction of a grouped launch (bf16 variant): this thread's share of
-// rowdot[row] = sum over columns n of C[row, n] * D[row, n]. The columns
-// are cut into groups of 32; for each group it holds, the thread forms the
-// FP32 sum of the products (exact: BF16 x BF16) in ascending column order,
-// from +0 (+0 for a group entirely past the last column), and writes it to
-// that group's own slot (group g = column / 32); no other thread writes
-// there, and the slots are combined later in a fixed order.
-template <int W>
-__device__ __forceinline__ void row_partial(const ValW<W> &v, const Params &p, const Problem &pb, const EpiCtx &c)
+// rowdot[row] = sum over columns n of C[row, n] * D[row, n], for its 32
+// columns of column tile nt and quarter cq: the FP32 sum of the products
+// (exact: BF16 x BF16) in ascending column order, from +0 (+0 for a quarter
+// entirely past the last column). It goes to its own slot; no other thread
+// writes there, and the slots are combined later in a fixed order.
+__device__ __forceinline__ void row_partial(const Val &v, const Params &p, const Problem &pb, const EpiCtx &c,
+                                            int nt, int cq)
 {
     if (c.row >= c.rows) return;
-    constexpr int GROUPS32 = W / 16;      // 32-column groups this thread holds
+    const int ncols = p.cols - c.col;
+    float s = 0.0f;
+    if (ncols > 0) {
+        const uint16_t *d = pb.rd_d + static_cast<long long>(c.row) * pb.rd_ldd + c.col;
+        uint32_t dw[16];
+        if (ncols >= 32) {
 #pragma unroll
-    for (int h = 0; h < GROUPS32; ++h) {
-        const int col = c.col + 32 * h;
-        const int ncols = p.cols - col;
-        float s = 0.0f;
-        if (ncols > 0) {
-            const uint16_t *d = pb.rd_d + static_cast<long long>(c.row) * pb.rd_ldd + col;
-            uint32_t dw[16];
-            if (ncols >= 32) {
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const uint4 x = *reinterpret_cast<const uint4 *>(d + 8 * k);
-                    dw[4 * k] = x.x;
-                    dw[4 * k + 1] = x.y;
-                    dw[4 * k + 2] = x.z;
-                    dw[4 * k + 3] = x.w;
-                }
-            } else {
-#pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                    const uint32_t lo = 2 * k < ncols ? d[2 * k] : 0u;
-                    const uint32_t hi = 2 * k + 1 < ncols ? d[2 * k + 1] : 0u;
-                    dw[k] = lo | (hi << 16);
-                }
+            for (int k = 0; k < 4; ++k) {
+                const uint4 x = *reinterpret_cast<const uint4 *>(d + 8 * k);
+                dw[4 * k] = x.x;
+                dw[4 * k + 1] = x.y;
+                dw[4 * k + 2] = x.z;
+                dw[4 * k + 3] = x.w;
             }
+        } else {
 #pragma unroll
             for (int k = 0; k < 16; ++k) {
-                const uint32_t x = v[16 * h + k];
-                if (2 * k < ncols)
-                    s = __fadd_rn(s, __fmul_rn(__uint_as_float(x << 16), __uint_as_float(dw[k] << 16)));
-                if (2 * k + 1 < ncols)
-                    s = __fadd_rn(s, __fmul_rn(__uint_as_float(x & 0xFFFF0000u), __uint_as_float(dw[k] & 0xFFFF0000u)));
+                const uint32_t lo = 2 * k < ncols ? d[2 * k] : 0u;
+                const uint32_t hi = 2 * k + 1 < ncols ? d[2 * k + 1] : 0u;
+                dw[k] = lo | (hi << 16);
             }
         }
-        pb.rd_part[static_cast<long long>(col / 32) * pb.rows + c.row] = s;
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            if (2 * k < ncols)
+                s = __fadd_rn(s, __fmul_rn(__uint_as_float(v[k] << 16), __uint_as_float(dw[k] << 16)));
+            if (2 * k + 1 < ncols)
+                s = __fadd_rn(s, __fmul_rn(__uint_as_float(v[k] & 0xFFFF0000u), __uint_as_float(dw[k] & 0xFFFF0000u)));
+        }
     }
+    pb.rd_part[static_cast<long long>(nt * 4 + cq) * pb.rows + c.row] = s;
 }
 
-// TMEM <-> registers for one value of W words.
-// A value of W words moves as W / 32 pieces of 32 words and, if W is an
-// odd multiple of 16, one piece of 16 at the end.
-template <int W>
-__device__ __forceinline__ void tmem_ld_val(uint32_t taddr, ValW<W> &t)
-{
-#pragma unroll
-    for (int h = 0; h < W / 32; ++h) tmem_ld32(taddr + 32u * h, *reinterpret_cast<uint32_t(*)[32]>(&t[32 * h]));
-    if constexpr (W % 32 != 0)
-        tmem_ld16(taddr + static_cast<uint32_t>(W - 16), *reinterpret_cast<uint32_t(*)[16]>(&t[W - 16]));
-}
-
-template <int W>
-__device__ __forceinline__ void tmem_st_val(uint32_t taddr, const ValW<W> &v)
-{
-#pragma unroll
-    for (int h = 0; h < W / 32; ++h)
-        tmem_st32(taddr + 32u * h, *reinterpret_cast<const uint32_t(*)[32]>(&v[32 * h]));
-    if constexpr (W % 32 != 0)
-        tmem_st16(taddr + static_cast<uint32_t>(W - 16), *reinterpret_cast<const uint32_t(*)[16]>(&v[W - 16]));
-}
-
-template <int W>
-__device__ __forceinline__ void reg_fence_val(ValW<W> &t)
-{
-#pragma unroll
-    for (int h = 0; h < W / 32; ++h) reg_fence(*reinterpret_cast<uint32_t(*)[32]>(&t[32 * h]));
-    if constexpr (W % 32 != 0) reg_fence16(*reinterpret_cast<uint32_t(*)[16]>(&t[W - 16]));
-}
-
-// Where slot s >= 2 lives when it is not in TMEM: a generic address of
-// this thread's line, in the shared-memory slots or the global scratch.
+// Slot s >= 2 (TMEM, shared memory or global scratch) -> t.
 template <bool F32, bool SWAP>
-__device__ __forceinline__ uint8_t *slot_line(int s, const EpiCtx &c)
-{
-    using C = Cfg<F32, SWAP>;
-    return s < C::GLOBAL_FIRST ? c.smem_line + (s - C::SMEM_FIRST) * C::SLOT_BYTES
-                               : c.scratch + (s - C::GLOBAL_FIRST) * C::SLOT_BYTES;
-}
-
-// 16-byte chunk k of a thread's line of CHUNKS chunks. Lines of
-// consecutive lanes are 16*CHUNKS bytes apart; permuting the chunks by lane
-// puts the eight lanes of a quarter-warp shared-memory access on eight
-// distinct 16-byte bank groups (bank group of lane i: 12 i + k' mod 8 for a
-// line of 12 chunks, so k' = k + i/2 mod 12 makes them 4 i + i/2 + k, all
-// distinct). Shared and global lines use the same permutation.
-template <int CHUNKS>
-__device__ __forceinline__ uint8_t *line_chunk(uint8_t *line, int lane, int k)
-{
-    static_assert(CHUNKS == 4 || CHUNKS == 12 || CHUNKS % 8 == 0, "line of 4, 12 or a multiple of 8 chunks");
-    if constexpr (CHUNKS == 12) {
-        const int kk = k + ((lane >> 1) & 3);
-        return line + (kk < 12 ? kk : kk - 12) * 16;
-    } else if constexpr (CHUNKS >= 8) {
-        return line + (k ^ (lane & 7)) * 16;
-    } else {
-        return line + (k ^ ((lane >> 1) & 3)) * 16;
-    }
-}
-
-// Starts loading slot s (s >= 2) into T. A TMEM slot is valid after the
-// thread's next tcgen05.wait::ld (and reg_fence_val); a shared or global
-// one when its registers are first used.
-template <bool F32, bool SWAP, int W>
-__device__ __forceinline__ void load_slot(int s, ValW<W> &T, const EpiCtx &c)
+__device__ __forceinline__ void load_slot(int s, Val &t, const EpiCtx &c)
 {
     using C = Cfg<F32, SWAP>;
     if (s < C::SMEM_FIRST) {
-        tmem_ld_val<W>(c.tmem_slot + static_cast<uint32_t>((s - C::TMEM_FIRST) * C::TMEM_SLOT_STRIDE), T);
-    } else {
-        uint8_t *line = slot_line<F32, SWAP>(s, c);
+        tmem_ld16(c.tmem_slot + static_cast<uint32_t>((s - C::TMEM_FIRST) * C::TMEM_SLOT_STRIDE), t);
+        tmem_wait_ld();
+        reg_fence16(t);
+    } else if (s < C::GLOBAL_FIRST) {
+        const uint32_t line = c.smem_slot + static_cast<uint32_t>((s - C::SMEM_FIRST) * C::SLOT_BYTES);
 #pragma unroll
-        for (int k = 0; k < C::CHUNKS; ++k)
-            asm volatile("ld.v4.b32 {%0, %1, %2, %3}, [%4];"
-                         : "=r"(T[4 * k]), "=r"(T[4 * k + 1]), "=r"(T[4 * k + 2]), "=r"(T[4 * k + 3])
-                         : "l"(line_chunk<C::CHUNKS>(line, c.lane, k))
+        for (int k = 0; k < 4; ++k)
+            asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(t[4 * k]), "=r"(t[4 * k + 1]), "=r"(t[4 * k + 2]), "=r"(t[4 * k + 3])
+                         : "r"(smem_chunk(line, c.lane, k))
+                         : "memory");
+    } else {
+        const uint8_t *src = c.scratch + (s - C::GLOBAL_FIRST) * C::SLOT_BYTES;
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            asm volatile("ld.global.v4.b32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(t[4 * k]), "=r"(t[4 * k + 1]), "=r"(t[4 * k + 2]), "=r"(t[4 * k + 3])
+                         : "l"(src + 16 * k)
                          : "memory");
     }
 }
 
-// A = T merged with A (T left), T holding slot s loaded by load_slot, a
-// tcgen05.wait::ld having followed the load if s is a TMEM slot.
-template <bool F32, bool SWAP, int W>
-__device__ __forceinline__ void merge_loaded(int s, ValW<W> &A, ValW<W> &T)
-{
-    using C = Cfg<F32, SWAP>;
-    if (s < C::SMEM_FIRST) reg_fence_val<W>(T);
-#pragma unroll
-    for (int i = 0; i < W; ++i) A[i] = merge<F32>(T[i], A[i]);
-}
-
-// A = slot s (s >= 2) merged with A: A = merge(slot, A).
-template <bool F32, bool SWAP, int W>
-__device__ __forceinline__ void merge_slot(int s, ValW<W> &A, ValW<W> &T, const EpiCtx &c)
-{
-    using C = Cfg<F32, SWAP>;
-    load_slot<F32, SWAP, W>(s, T, c);
-    if (s < C::SMEM_FIRST) tmem_wait_ld();
-    merge_loaded<F32, SWAP, W>(s, A, T);
-}
-
-// v -> slot s >= 2.
-template <bool F32, bool SWAP, int W>
-__device__ __forceinline__ void store_slot(int s, const ValW<W> &v, const EpiCtx &c)
+// v -> slot s >= 2 (TMEM, shared memory or global scratch).
+template <bool F32, bool SWAP>
+__device__ __forceinline__ void store_slot(int s, const Val &v, const EpiCtx &c)
 {
     using C = Cfg<F32, SWAP>;
     if (s < C::SMEM_FIRST) {
-        tmem_st_val<W>(c.tmem_slot + static_cast<uint32_t>((s - C::TMEM_FIRST) * C::TMEM_SLOT_STRIDE), v);
+        tmem_st16(c.tmem_slot + static_cast<uint32_t>((s - C::TMEM_FIRST) * C::TMEM_SLOT_STRIDE), v);
         tmem_wait_st();
-    } else {
-        uint8_t *line = slot_line<F32, SWAP>(s, c);
+    } else if (s < C::GLOBAL_FIRST) {
+        const uint32_t line = c.smem_slot + static_cast<uint32_t>((s - C::SMEM_FIRST) * C::SLOT_BYTES);
 #pragma unroll
-        for (int k = 0; k < C::CHUNKS; ++k)
-            asm volatile("st.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(line_chunk<C::CHUNKS>(line, c.lane, k)),
+        for (int k = 0; k < 4; ++k)
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(smem_chunk(line, c.lane, k)),
                          "r"(v[4 * k]), "r"(v[4 * k + 1]), "r"(v[4 * k + 2]), "r"(v[4 * k + 3])
                          : "memory");
+    } else {
+        uint8_t *dst = c.scratch + (s - C::GLOBAL_FIRST) * C::SLOT_BYTES;
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(dst + 16 * k), "r"(v[4 * k]),
+                         "r"(v[4 * k + 1]), "r"(v[4 * k + 2]), "r"(v[4 * k + 3])
+                         : "memory");
     }
 }
 
-// Chunk K of a leaf (CHUNK FP32 accumulator columns, staged in registers)
-// -> words [K * CW, (K + 1) * CW) of dst: rounded once to BF16 (RNE), two
-// columns per word, for the bf16 variant; as is for the fp32 variant. With
-// ADD the chunk is merged into what dst holds there (dst + chunk, the
-// left operand first); otherwise it replaces it.
-template <bool F32, bool ADD, int K, int W>
-__device__ __forceinline__ void put_chunk(const uint32_t (&stg)[16], ValW<W> &dst)
+// Loads this thread's BN/4 accumulator columns (32 FP32 for the bf16
+// variant, 16 for the fp32 one) into the staging registers and waits.
+template <bool F32>
+__device__ __forceinline__ void stage_load(uint32_t acc_taddr, uint32_t (&stg)[32])
 {
-    constexpr int CW = F32 ? 16 : 8;
-    static_assert((K + 1) * CW <= W, "chunk inside the value");
+    if constexpr (F32) {
+        uint32_t(&lo)[16] = *reinterpret_cast<uint32_t(*)[16]>(&stg[0]);
+        tmem_ld16(acc_taddr, lo);
+        tmem_wait_ld();
+        reg_fence16(lo);
+    } else {
+        tmem_ld32(acc_taddr, stg);
+        tmem_wait_ld();
+        reg_fence(stg);
+    }
+}
+
+// The staged leaf -> F: rounded once to BF16 (RNE), two columns per word,
+// for the bf16 variant; as is for the fp32 variant.
+template <bool F32>
+__device__ __forceinline__ void stage_convert(const uint32_t (&stg)[32], Val &F)
+{
+    if constexpr (F32) {
 #pragma unroll
-    for (int i = 0; i < CW; ++i) {
-        uint32_t x;
-        if constexpr (F32) x = stg[i];
-        else x = cvt_bf16x2(stg[2 * i], stg[2 * i + 1]);
-        if constexpr (ADD) dst[K * CW + i] = merge<F32>(dst[K * CW + i], x);
-        else dst[K * CW + i] = x;
+        for (int i = 0; i < 16; ++i) F[i] = stg[i];
+    } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) F[i] = cvt_bf16x2(stg[2 * i], stg[2 * i + 1]);
     }
 }
 
@@ -724,8 +637,7 @@ __device__ __forceinline__ void put_chunk(const uint32_t (&stg)[16], ValW<W> &ds
 // Shared-memory and TMEM addresses of one CTA.
 template <bool F32, bool SWAP>
 struct Smem {
-    uint32_t sA, sB, bar0, tmem;
-    uint8_t *slots;       // generic address of the shared-memory slots
+    uint32_t sA, sB, sSlots, bar0, tmem;
     volatile int *abort_flag;
     __device__ uint32_t full(int s) const { return bar0 + 8u * s; }
     using C = Cfg<F32, SWAP>;
@@ -737,16 +649,15 @@ struct Smem {
     __device__ uint32_t turn(int j) const { return never() + 8u * (1 + kStageWarps + j); }
 };
 
-// Stage warps: one per SM sub-partition; the first STAGES of them are
-// active (the rest of the warpgroup idles). Warp j owns ring slot j and the
-// K-stages g with g % STAGES == j: it issues the stage's TMA copies into
-// its slot, waits for them, then issues the stage's MMAs (two K=16 MMAs per
-// leaf into a fresh accumulator) and the commits that hand the
-// accumulators to the epilogue and the slot back for the stage STAGES
-// later. Issuing an MMA holds up the sub-partition that issues it until the
-// tensor core accepts it; rotating the stages over the sub-partitions
-// spreads that cost over the epilogue warps, which run on all four,
-// instead of slowing the quarter of them that share one.
+// Stage warps: kStageWarps warps, one per SM sub-partition. Warp j owns
+// ring slot j and the K-stages g with g % kStageWarps == j: it issues the
+// stage's TMA copies into its slot, waits for them, then issues the stage's
+// MMAs (two K=16 MMAs per leaf into a fresh accumulator) and the commits that
+// hand the accumulators to the epilogue and the slot back for the stage
+// kStageWarps later. Issuing an MMA holds up the sub-partition that issues
+// it until the tensor core accepts it; rotating the stages over the four
+// sub-partitions spreads that cost over the epilogue warps, which run on all
+// four, instead of slowing the quarter of them that share one.
 //
 // MMAs are still issued in leaf order: warp j issues stage g's MMAs only
 // after warp j-1 has issued stage g-1's (the turn barriers). The barrier
@@ -758,7 +669,7 @@ template <int A_MAJOR, int B_MAJOR, bool F32, bool GROUPED, bool SWAP>
 __device__ __forceinline__ void stage_role(const Params &p, const Smem<F32, SWAP> &S, int j)
 {
     using C = Cfg<F32, SWAP>;
-    if (j >= C::STAGES) return;                       // no ring slot: idle
+    static_assert(C::STAGES == kStageWarps, "one ring slot per stage warp");
     constexpr uint32_t IDESC = idesc_bf16(kBM, C::BN, A_MAJOR, B_MAJOR);
     // Byte offset of K step k (16 contraction elements) inside a stage:
     // K-major rows hold the stage's 64 contraction elements (128 B), so a
@@ -772,7 +683,7 @@ __device__ __forceinline__ void stage_role(const Params &p, const Smem<F32, SWAP
     const bool leader = elect_one();
     const int s = j;                                  // this warp's ring slot
     const uint32_t full = S.full(s), empty = S.empty(s);
-    const uint32_t my_turn = S.turn(j), next_turn = S.turn((j + 1) % C::STAGES);
+    const uint32_t my_turn = S.turn(j), next_turn = S.turn((j + 1) % kStageWarps);
     const uint32_t a_dst = S.sA + s * C::A_STAGE;
     const uint32_t b_dst = S.sB + s * C::B_STAGE;
     const uint64_t a_st = sdesc(a_dst, A_LBO, 1024u);
@@ -790,8 +701,8 @@ __device__ __forceinline__ void stage_role(const Params &p, const Smem<F32, SWAP
         // Test hook: a wait that nothing will end.
         ok = __all_sync(0xFFFFFFFFu, wait_bounded(S.never(), 0, S.abort_flag, p.status, p.timeout_ns, true));
     }
-    for (int g = j; ok && g < total; g += C::STAGES) {
-        const uint32_t round = static_cast<uint32_t>(g / C::STAGES) & 1u;
+    for (int g = j; ok && g < total; g += kStageWarps) {
+        const uint32_t round = static_cast<uint32_t>(g / kStageWarps) & 1u;
         const int tl = g / KS;                        // unit of this CTA
         const int ks = g - tl * KS;
         const int u = blockIdx.x + tl * gridDim.x;
@@ -828,7 +739,7 @@ __device__ __forceinline__ void stage_role(const Params &p, const Smem<F32, SWAP
                 // four slots in flight leave each SM waiting on DRAM
                 // latency. The A tile this warp will copy kPrefetchRounds
                 // rounds from now is fetched into L2 already.
-                const int gp = g + kPrefetchRounds * C::STAGES;
+                const int gp = g + kPrefetchRounds * kStageWarps;
                 if (gp < total) {
                     const int tlp = gp / KS;
                     const int ksp = gp - tlp * KS;
@@ -855,7 +766,7 @@ __device__ __forceinline__ void stage_role(const Params &p, const Smem<F32, SWAP
         // ---- wait for the data and for this stage's turn to issue MMAs
         got = wait_bounded(full, round, S.abort_flag, p.status, p.timeout_ns, true);
         if (got && g > 0)
-            got = wait_bounded(my_turn, static_cast<uint32_t>((g - 1) / C::STAGES) & 1u, S.abort_flag, p.status,
+            got = wait_bounded(my_turn, static_cast<uint32_t>((g - 1) / kStageWarps) & 1u, S.abort_flag, p.status,
                                p.timeout_ns, true);
         if (!__all_sync(0xFFFFFFFFu, got)) {
             ok = false;
@@ -906,131 +817,63 @@ __device__ __forceinline__ void stage_role(const Params &p, const Smem<F32, SWAP
     }
 }
 
-template <bool F32, bool GROUPED, bool SWAP>
-struct Epilogue {
-    using C = Cfg<F32, SWAP>;
-    static constexpr int W = C::WORDS;
-    static constexpr int NCH = C::NCH;
-    using Val = ValW<W>;
-
-    const Params &p;
-    const Smem<F32, SWAP> &S;
-    uint32_t acc0;                        // TMEM address of this thread's first column of accumulator 0
-    int lane;
-    int to_load;                          // leaves of this CTA whose load is not yet started
-    int acc = 0;                          // accumulator of the leaf in flight
-    uint32_t acc_phase = 0;
-    bool ok = true;
-    Val A, B;
-    uint32_t stg[2][C::CHUNK];            // chunk k of a leaf is staged in stg[k % 2]
-
-    __device__ __forceinline__ Epilogue(const Params &p_, const Smem<F32, SWAP> &S_, uint32_t acc0_, int lane_,
-                                        int leaves)
-        : p(p_), S(S_), acc0(acc0_), lane(lane_), to_load(leaves)
-    {
-    }
-
-    // Waits for the accumulator of the next leaf and starts loading its
-    // chunk 0. The load itself is issued unconditionally, so that the
-    // staging registers have a single definition on every path: past the
-    // stream's last leaf (or once the CTA is aborting) it reads an
-    // accumulator that is never used.
-    __device__ __forceinline__ void start_leaf()
-    {
-        if (ok && to_load > 0) {
-            const bool got = wait_bounded(S.accf(acc), acc_phase, S.abort_flag, p.status, p.timeout_ns, true);
-            ok = __all_sync(0xFFFFFFFFu, got);
-        }
-        --to_load;
-        tc_fence_after();
-        tmem_ld16(acc0 + static_cast<uint32_t>(acc * C::BN), stg[0]);
-    }
-
-    // Chunk K of the leaf in flight -> dst (placed, or added with ADD), then
-    // the chunks after it.
-    template <bool ADD, int K>
-    __device__ __forceinline__ void chunk(Val &dst)
-    {
-        tmem_wait_ld();
-        reg_fence16(stg[K % 2]);
-        if constexpr (K + 1 < NCH) {
-            tmem_ld16(acc0 + static_cast<uint32_t>(acc * C::BN + C::CHUNK * (K + 1)), stg[(K + 1) % 2]);
-        } else {
-            // the whole leaf is in registers: its accumulator goes back to
-            // the MMA, and the next leaf starts (into stg[0]: NCH is even)
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(S.acce(acc));
-            if (++acc == C::NACC) {
-                acc = 0;
-                acc_phase ^= 1u;
-            }
-            start_leaf();
-        }
-        put_chunk<F32, ADD, K, W>(stg[K % 2], dst);
-        if constexpr (K + 1 < NCH) chunk<ADD, K + 1>(dst);
-    }
-
-    static __device__ __forceinline__ void add(Val &left, const Val &right)
-    {
-#pragma unroll
-        for (int i = 0; i < W; ++i) left[i] = merge<F32>(left[i], right[i]);
-    }
-
-    // The N leaves of one block merged in registers in straight-line code:
-    //   N = 1: A = l0                N = 2: A = l0 + l1
-    //   N = 3: A = l0 + (l1 + l2)    N = 4: A = (l0 + l1) + (l2 + l3)
-    template <int N>
-    __device__ __forceinline__ void block()
-    {
-        chunk<false, 0>(A);
-        if constexpr (N == 2 || N == 4) chunk<true, 0>(A);
-        if constexpr (N >= 3) {
-            chunk<false, 0>(B);
-            chunk<true, 0>(B);
-            add(A, B);
-        }
-    }
-};
-
-// Epilogue warp: leaf rounding and the merge tree for one row and BN/GROUPS
+// Epilogue warp: leaf rounding and the merge tree for one row and BN/2
 // columns of every tile.
 //
 // The tree is walked block by block (det_gemm_block_schedule): a block's
-// one to four leaves are rounded and merged in registers in straight-line
+// two to four leaves are rounded and merged in registers in straight-line
 // code, then the block's value is merged with the pending partials its
-// entry names and parked (one TMEM, shared or scratch access) or written
-// out as the root.
-//
-// A leaf streams through two staging buffers of CHUNK columns: while one
-// chunk is rounded and merged into its destination (A or B), the TMEM load
-// of the next one is in flight. The last chunk's load starts the next leaf
-// (after its accumulator is full), and the accumulator goes back to the
-// MMA as soon as its last chunk has landed. Rounding and the first merge
-// are fused: a leaf is either placed or added into a value, so a block
-// needs two values, not one per leaf.
+// entry names and parked (one TMEM or scratch access) or written out as the
+// root. The code stays small so that the loop, rare branches included,
+// lives in the instruction cache.
 template <bool F32, bool GROUPED, bool SWAP>
 __device__ __forceinline__ void epilogue_role(const Params &p, const Smem<F32, SWAP> &S, int warp, int lane)
 {
     using C = Cfg<F32, SWAP>;
-    constexpr int W = C::WORDS;
     const int q = warp & 3;               // TMEM lane quadrant (rows 32q .. 32q+31)
-    const int cq = warp >> 2;             // column group of the tile
+    const int cq = warp >> 2;             // column group of the tile (a quarter, or a half when SWAP)
     const uint32_t lane_bits = static_cast<uint32_t>(q * 32) << 16;
+    const uint32_t acc0 = S.tmem + lane_bits + static_cast<uint32_t>(cq * C::COLS);
     EpiCtx c;
     c.tmem_slot = S.tmem + lane_bits + static_cast<uint32_t>(C::TMEM_SLOT_BASE + cq * C::WORDS);
-    c.smem_line = S.slots + (warp * 32 + lane) * C::LINE;
-    c.scratch = static_cast<uint8_t *>(p.scratch) + static_cast<long long>(blockIdx.x) * p.scratch_cta_bytes +
+    c.smem_slot = S.sSlots + static_cast<uint32_t>((warp * 32 + lane) * C::LINE);
+    c.scratch = static_cast<uint8_t *>(p.scratch) + static_cast<long long>(blockIdx.x) * C::SCRATCH_CTA_BYTES +
                 (warp * 32 + lane) * C::LINE;
     c.lane = lane;
     const int units = p.units;
     const int NB = p.num_blocks;
-    const int my_units = blockIdx.x < units ? (units - 1 - blockIdx.x) / gridDim.x + 1 : 0;
-    Epilogue<F32, GROUPED, SWAP> E(p, S, S.tmem + lane_bits + static_cast<uint32_t>(cq * C::COLS), lane,
-                                   my_units * p.num_leaves);
 
-    E.start_leaf();
-    for (int u = blockIdx.x; E.ok && u < units; u += gridDim.x) {
+    Val A, B, Cc;
+    uint32_t stg[32];
+    int acc = 0;                          // accumulator of the next leaf
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    // Waits for the next leaf's accumulator, loads it, hands it back to the
+    // MMA (which may then fill it with the leaf NACC ahead) and rounds the
+    // leaf into dst.
+    auto take = [&](Val &dst) {
+        const bool got = wait_bounded(S.accf(acc), acc_phase, S.abort_flag, p.status, p.timeout_ns, true);
+        if (!__all_sync(0xFFFFFFFFu, got)) {
+            ok = false;
+            return;
+        }
+        tc_fence_after();
+        stage_load<F32>(acc0 + static_cast<uint32_t>(acc * C::BN), stg);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(S.acce(acc));
+        if (++acc == C::NACC) {
+            acc = 0;
+            acc_phase ^= 1u;
+        }
+        stage_convert<F32>(stg, dst);
+    };
+    auto add = [](Val &left, const Val &right) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) left[i] = merge<F32>(left[i], right[i]);
+    };
+
+    for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
         const Problem &pb = p.prob[GROUPED ? problem_of(p, u) : 0];
         const int ul = u - pb.first_unit;
         const int t = ul / p.parts;
@@ -1047,32 +890,42 @@ __device__ __forceinline__ void epilogue_role(const Params &p, const Smem<F32, S
             c.out = static_cast<uint8_t *>(pb.out);
             c.ldo = pb.ldo;
         }
-        for (int b = 0; E.ok && b < NB; ++b) {
+        for (int b = 0; b < NB; ++b) {
             const uint32_t e = p.blocks[b];
-            switch ((e >> 10) & 3u) {   // leaves in the block, minus one
-            case 0: E.template block<1>(); break;
-            case 1: E.template block<2>(); break;
-            case 2: E.template block<3>(); break;
-            default: E.template block<4>(); break;
+            const int n = static_cast<int>((e >> 10) & 3u) + 1;   // leaves in the block
+            // n = 1: A = l0          n = 2: A = l0 + l1
+            // n = 3: A = l0 + (l1 + l2)     n = 4: A = (l0 + l1) + (l2 + l3)
+            take(A);
+            if (n >= 2) take(B);
+            if (n == 4) {
+                add(A, B);
+                take(B);
             }
-            if (!E.ok) break;
-            // merge with the pending left siblings above the block, lowest
-            // first (B is free once the block is merged)
+            if (n >= 3) {
+                take(Cc);
+                add(B, Cc);
+            }
+            if (!ok) return;
+            if (n >= 2) add(A, B);
+            // merge with the pending left siblings above the block, lowest first
 #pragma unroll 1
-            for (uint32_t m = (e & 0x3FFu) >> C::TMEM_FIRST, s = C::TMEM_FIRST; m != 0; m >>= 1, ++s)
-                if (m & 1u) merge_slot<F32, SWAP, W>(static_cast<int>(s), E.A, E.B, c);
+            for (uint32_t m = (e & 0x3FFu) >> C::TMEM_FIRST, s = C::TMEM_FIRST; m != 0; m >>= 1, ++s) {
+                if (!(m & 1u)) continue;
+                load_slot<F32, SWAP>(static_cast<int>(s), B, c);   // B is free once the block is merged
+#pragma unroll
+                for (int i = 0; i < 16; ++i) A[i] = merge<F32>(B[i], A[i]);
+            }
             const int st = static_cast<int>(e >> 12);
             if (st == kSlotRoot) {
-                store_out<F32, SWAP, W>(E.A, p, c);
+                store_out<F32, SWAP>(A, p, c);
                 if constexpr (GROUPED && !F32) {
-                    if (pb.rd_part != nullptr) row_partial<W>(E.A, p, pb, c);
+                    if (pb.rd_part != nullptr) row_partial(A, p, pb, c, nt, cq);
                 }
             } else {
-                store_slot<F32, SWAP, W>(st, E.A, c);
+                store_slot<F32, SWAP>(st, A, c);
             }
         }
     }
-    tmem_wait_ld();   // nothing of this thread's may still be loading when TMEM is freed
 }
 
 template <int A_MAJOR, int B_MAJOR, bool F32, bool GROUPED, bool SWAP>
@@ -1090,7 +943,7 @@ __global__ void __launch_bounds__(Cfg<F32, SWAP>::THREADS, 1) det_gemm_kernel(co
     Smem<F32, SWAP> S;
     S.sA = base + C::OFF_A;
     S.sB = base + C::OFF_B;
-    S.slots = smem + C::OFF_SLOTS;
+    S.sSlots = base + C::OFF_SLOTS;
     S.bar0 = base + C::OFF_BAR;
     uint32_t *tmem_base_smem = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
     S.abort_flag = reinterpret_cast<volatile int *>(smem + C::OFF_MISC + 4);
@@ -1132,9 +985,9 @@ __global__ void __launch_bounds__(Cfg<F32, SWAP>::THREADS, 1) det_gemm_kernel(co
     S.tmem = *tmem_base_smem;
 
     if constexpr (!SWAP) {
-        // Register split: the stage warpgroup gives up registers and the two
-        // epilogue warpgroups take them (kProdRegs*128 + kEpiRegs*256 fits in
-        // the kLaunchRegs*384 the CTA is launched with). Each role's code sits
+        // Register split: the stage warpgroup gives up registers and the four
+        // epilogue warpgroups take them (kProdRegs*128 + kEpiRegs*512 fits in
+        // the kLaunchRegs*640 the CTA is launched with). Each role's code sits
         // inside its own branch so that the compiler allocates it under the
         // matching limit.
         static_assert(kProdRegs * 128 + kEpiRegs * 32 * C::EPI_WARPS <= kLaunchRegs * C::THREADS, "register split");
@@ -1190,8 +1043,7 @@ struct Launcher {
         o.launch = &launch;
         o.bn = C::BN;
         o.smem_bytes = C::SMEM_BYTES;
-        o.slot_bytes = C::SLOT_BYTES;
-        o.global_first = C::GLOBAL_FIRST;
+        o.scratch_cta_bytes = C::SCRATCH_CTA_BYTES;
         o.split_regs = C::LAUNCH_REGS;
         o.swap = SWAP;
         return o;

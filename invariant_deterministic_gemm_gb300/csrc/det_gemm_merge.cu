@@ -78,10 +78,9 @@ cudaError_t launch_merge(bool f32, const PartPtrs &at, int parts, int rows, int 
 }
 
 // Row reduction of a grouped launch. The kernel leaves, for every row i,
-// one FP32 partial per 32-column group g < n_groups: part[g rows + i].
-// rowdot[i] combines them in a fixed order: the groups of each 128-column
-// tile t (g = 4 t + q, +0 past the last group) as ((q0 + q1) + (q2 + q3)),
-// then the tiles by the same mid-split tree of FP32
+// one FP32 partial per (column tile t, quarter q): part[(4 t + q) rows + i].
+// rowdot[i] combines them in a fixed order: each tile's four quarters as
+// ((q0 + q1) + (q2 + q3)), then the tiles by the same mid-split tree of FP32
 // adds the contraction uses, walked with its per-leaf schedule (pending left
 // children in slots). No atomics: the same bits every run, whichever CTA
 // wrote which partial first (Megatron Core notes, "Kernel redesign: the
@@ -89,7 +88,7 @@ cudaError_t launch_merge(bool f32, const PartPtrs &at, int parts, int rows, int 
 struct RowdotParams {
     const float *part;
     float *rowdot;
-    int rows, n_tiles, n_groups;
+    int rows, n_tiles;
     uint16_t sched[kMaxLeaves];
 };
 
@@ -101,11 +100,8 @@ __global__ void rowdot_reduce_kernel(const __grid_constant__ RowdotParams p)
     float root = 0.0f;
     const long long stride = p.rows;
     for (int t = 0; t < p.n_tiles; ++t) {
-        float g[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-            g[k] = 4 * t + k < p.n_groups ? p.part[static_cast<long long>(4 * t + k) * stride + i] : 0.0f;
-        float v = __fadd_rn(__fadd_rn(g[0], g[1]), __fadd_rn(g[2], g[3]));
+        const float *q = p.part + static_cast<long long>(4 * t) * stride + i;
+        float v = __fadd_rn(__fadd_rn(q[0], q[stride]), __fadd_rn(q[2 * stride], q[3 * stride]));
         const uint32_t e = p.sched[t];
 #pragma unroll
         for (int s = 0; s < kMaxSlots; ++s)
@@ -139,17 +135,15 @@ cudaError_t launch_merge_list(bool f32, const void *const *parts, int n, int row
     return launch_merge(f32, at, n, rows, cols, ldp, out, ldo, stream);
 }
 
-cudaError_t launch_rowdot_reduce(const float *part, int rows, int n_tiles, int n_groups, float *rowdot,
-                                 cudaStream_t stream)
+cudaError_t launch_rowdot_reduce(const float *part, int rows, int n_tiles, float *rowdot, cudaStream_t stream)
 {
     if (rows <= 0) return cudaSuccess;
-    if (n_tiles < 1 || n_tiles > kMaxLeaves || n_groups < 1 || n_groups > 4 * n_tiles) return cudaErrorInvalidValue;
+    if (n_tiles < 1 || n_tiles > kMaxLeaves) return cudaErrorInvalidValue;
     RowdotParams p;
     p.part = part;
     p.rowdot = rowdot;
     p.rows = rows;
     p.n_tiles = n_tiles;
-    p.n_groups = n_groups;
     if (det_gemm_tree_schedule(n_tiles, p.sched) != DET_GEMM_OK) return cudaErrorInvalidValue;
     const int threads = 128;
     rowdot_reduce_kernel<<<(rows + threads - 1) / threads, threads, 0, stream>>>(p);

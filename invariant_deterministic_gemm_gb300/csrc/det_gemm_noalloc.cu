@@ -19,10 +19,10 @@
 
 namespace {
 
-// One CTA needs at most 3 x 32 KiB of scratch (its three least used
-// pending-partial slots, at the longest contraction). 160 CTAs -- one per
-// SM on a GPU of up to 160 SMs -- therefore need 15 MiB. Every GPU that
-// loads this library holds this array until the process exits.
+// One CTA needs 3 x 32 KiB of scratch (its three least used pending-partial
+// slots). 160 CTAs -- one per SM on a GPU of up to 160 SMs -- therefore need
+// 15 MiB. Every GPU that loads this library holds this array until the
+// process exits.
 constexpr size_t kNoAllocScratchBytes = size_t{160} * 3 * 32768;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 

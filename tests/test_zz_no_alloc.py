@@ -6,8 +6,8 @@ fixed array of the library instead of a cudaMalloc'd buffer -- call after
 call, whatever an earlier call left in that array.
 
 The shapes make the kernel use the array: a contraction of 32768 (1024
-leaves) parks the tree's highest pending partials there; the ragged column
-count of the second call also takes the clipped-store path.
+leaves) parks the tree's highest pending partials there, and a ragged
+column count sends the output of the last column tile through it.
 
 This file is named to be collected last, so that a run stopping at its first
 failure has already run every other test."""
