@@ -350,12 +350,16 @@ void choose_tile_order(Problem &pb, int64_t rows, int64_t cols, int64_t kc, int 
 // the merge tree gives that many work units per tile, and the tree's top
 // levels are applied afterwards (launch_merge_parts). The bits are the same
 // for every choice. The busiest CTA walks ceil(units / SMs) * leaves-per-unit
-// leaves; the fewest parts that cut that by a quarter or more are taken
-// (each range keeps at least 8 leaves), since every part costs a round trip
-// of partial results through memory and a merge launch.
+// leaves, plus, for a split, the merge launch and the partial results'
+// round trip through memory, counted as 8 leaves (fitted on GB300: it keeps
+// the QKV launch at M <= 64, 96 tiles, unsplit and splits M = 256 in two,
+// the faster choice for each). The fewest parts that cut that cost by a
+// quarter or more are taken (each range keeps at least 8 leaves).
 int choose_parts(int64_t tiles, int64_t L, int sms)
 {
-    auto busiest = [&](int parts) { return (tiles * parts + sms - 1) / sms * (L / parts); };
+    auto busiest = [&](int parts) {
+        return (tiles * parts + sms - 1) / sms * (L / parts) + (parts > 1 ? int64_t{8} : int64_t{0});
+    };
     int best = 1;
     for (int parts = 2; parts <= 8; parts *= 2) {
         if (L % parts != 0 || L / parts < 8) break;
