@@ -151,6 +151,14 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar)
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
+// mbar_arrive by the lanes for which `pred` holds, without a branch.
+__device__ __forceinline__ void mbar_arrive_if(uint32_t bar, bool pred)
+{
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %1, 0;\n\t@p mbarrier.arrive.shared::cta.b64 _, [%0];\n\t}" ::"r"(bar),
+                 "r"(static_cast<uint32_t>(pred))
+                 : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes)
 {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
@@ -218,6 +226,17 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, vola
             return false;
         }
     }
+}
+
+// The whole warp waits for the phase with the given parity. When it has
+// completed already (the common case) this is one test, one vote and one
+// uniform branch, with no per-lane branch; otherwise the bounded wait.
+// True when every lane saw the phase complete.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag, int *status,
+                                          unsigned long long timeout_ns)
+{
+    if (__all_sync(0xFFFFFFFFu, mbar_try_wait(bar, parity))) return true;
+    return __all_sync(0xFFFFFFFFu, wait_bounded(bar, parity, abort_flag, status, timeout_ns, true));
 }
 
 // One lane of the (converged) warp: the one that issues TMA copies, MMAs
@@ -714,8 +733,7 @@ __device__ __forceinline__ void stage_role(const Params &p, const Smem<F32, SWAP
         int mt, nt;
         tile_coords(t, pb, p.n_tiles, mt, nt);
         // ---- copy the stage into the slot once the MMAs of its last use are done
-        bool got = wait_bounded(empty, round ^ 1u, S.abort_flag, p.status, p.timeout_ns, true);
-        if (!__all_sync(0xFFFFFFFFu, got)) {
+        if (!warp_wait(empty, round ^ 1u, S.abort_flag, p.status, p.timeout_ns)) {
             ok = false;
             break;
         }
@@ -765,11 +783,11 @@ __device__ __forceinline__ void stage_role(const Params &p, const Smem<F32, SWAP
         tma_pending = true;
         tma_parity = round;
         // ---- wait for the data and for this stage's turn to issue MMAs
-        got = wait_bounded(full, round, S.abort_flag, p.status, p.timeout_ns, true);
+        bool got = warp_wait(full, round, S.abort_flag, p.status, p.timeout_ns);
         if (got && g > 0)
-            got = wait_bounded(my_turn, static_cast<uint32_t>((g - 1) / kStageWarps) & 1u, S.abort_flag, p.status,
-                               p.timeout_ns, true);
-        if (!__all_sync(0xFFFFFFFFu, got)) {
+            got = warp_wait(my_turn, static_cast<uint32_t>((g - 1) / kStageWarps) & 1u, S.abort_flag, p.status,
+                            p.timeout_ns);
+        if (!got) {
             ok = false;
             break;
         }
@@ -783,9 +801,8 @@ __device__ __forceinline__ void stage_role(const Params &p, const Smem<F32, SWAP
             const int G = tl * L + leaf;
             const int use = G / C::NACC;
             const int acc = G - use * C::NACC;
-            got = wait_bounded(S.acce(acc), (static_cast<uint32_t>(use) & 1u) ^ 1u, S.abort_flag, p.status,
-                               p.timeout_ns, true);
-            if (!__all_sync(0xFFFFFFFFu, got)) {
+            if (!warp_wait(S.acce(acc), (static_cast<uint32_t>(use) & 1u) ^ 1u, S.abort_flag, p.status,
+                           p.timeout_ns)) {
                 ok = false;
                 break;
             }
@@ -853,8 +870,7 @@ __device__ __forceinline__ void epilogue_role(const Params &p, const Smem<F32, S
     // MMA (which may then fill it with the leaf NACC ahead) and rounds the
     // leaf into dst.
     auto take = [&](Val &dst) {
-        const bool got = wait_bounded(S.accf(acc), acc_phase, S.abort_flag, p.status, p.timeout_ns, true);
-        if (!__all_sync(0xFFFFFFFFu, got)) {
+        if (!warp_wait(S.accf(acc), acc_phase, S.abort_flag, p.status, p.timeout_ns)) {
             ok = false;
             return;
         }
@@ -862,7 +878,7 @@ __device__ __forceinline__ void epilogue_role(const Params &p, const Smem<F32, S
         stage_load<F32>(acc0 + static_cast<uint32_t>(acc * C::BN), stg);
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(S.acce(acc));
+        mbar_arrive_if(S.acce(acc), lane == 0);
         if (++acc == C::NACC) {
             acc = 0;
             acc_phase ^= 1u;
