@@ -487,7 +487,10 @@ det_gemm_status run_problems(Variant v, bool a_kmajor, bool b_kmajor, const Prob
             else ok = encode(&pb.tmap_b, q.b.ptr, cols, kc, q.b.ld, 64, 64);
         }
         if (!ok) return DET_GEMM_ERR_LAUNCH;
-        pb.stage_tx = a_box_rows * kBK * 2 + b_box_rows * kBK * 2;
+        // An MN-major B operand is copied in boxes of 64 columns, the tile's
+        // BN columns rounded up (the copy counts whole boxes).
+        const int b_copy_rows = b_kmajor ? b_box_rows : (ops.bn + 63) / 64 * 64;
+        pb.stage_tx = a_box_rows * kBK * 2 + b_copy_rows * kBK * 2;
         pb.out = const_cast<void *>(q.out.ptr);
         pb.ldo = q.out.ld;
         choose_tile_order(pb, q.rows, cols, kc, ops.bn, p.n_tiles);

@@ -17,9 +17,7 @@ constexpr int kMaxSlots = 10;             // ceil(log2(kMaxLeaves)) pending part
 constexpr int kBM = 128;                  // output rows per tile (one TMEM lane per row)
 constexpr int kBK = 64;                   // contraction elements per shared-memory stage (two leaves)
 constexpr int kStageWarps = 4;            // TMA copies and MMAs of the K-stages: one per SM sub-partition
-constexpr int kLaunchRegs = 96;           // registers per thread at launch of the plain tile's 640 threads
 constexpr int kProdRegs = 40;             // stage warpgroup after setmaxnreg
-constexpr int kEpiRegs = 104;             // epilogue warpgroups after setmaxnreg
 
 // Operand major-ness as seen by the MMA: K-major = contraction contiguous.
 enum Major { kKMajor = 0, kMNMajor = 1 };
@@ -117,8 +115,9 @@ struct RmsParams {
 constexpr int kRmsWarps = 8;      // rows per CTA
 cudaError_t launch_rmsnorm(const RmsParams &p, cudaStream_t stream);
 
-// Largest scratch_cta_bytes over all variants (bf16: 3 slots x 32 KiB).
-constexpr int kMaxScratchCtaBytes = 3 * 32768;
+// Largest scratch_cta_bytes over all variants (fp32: 4 slots x 48 KiB;
+// bf16: 3 slots x 32 KiB).
+constexpr int kMaxScratchCtaBytes = 4 * 49152;
 
 VariantOps ops_bf16_kmn();
 VariantOps ops_bf16_kk();

@@ -75,16 +75,27 @@ constexpr int kPrefetchRounds = 2;  // transposed tile: L2 prefetch distance, in
 // against the plain tile on the GPU).
 template <bool F32, bool SWAP = false>
 struct Cfg {
-    static constexpr int EPI_WARPS = SWAP ? 8 : 16;     // epilogue warps
+    // Epilogue warps and output columns per tile (rows when SWAP). The FP32
+    // tile is 96 columns wide with three epilogue warps per scheduler, 32
+    // FP32 columns each: an MMA of 128 rows costs the tensor core the same
+    // time for any N up to 256, and 96 columns of FP32 values and pending
+    // partials still fit the registers, TMEM and shared memory.
+    static constexpr int EPI_WARPS = SWAP ? 8 : (F32 ? 12 : 16);
     static constexpr int GROUPS = EPI_WARPS / 4;        // epilogue warps per TMEM lane quadrant
-    static constexpr int BN = SWAP ? 64 : (F32 ? 64 : 128);   // output columns per tile (rows when SWAP)
-    static constexpr int NACC = SWAP ? 4 : (F32 ? 4 : 3);     // TMEM accumulator buffers
+    static constexpr int BN = SWAP ? 64 : (F32 ? 96 : 128);
+    // TMEM accumulator buffers. Three in the plain tiles leave TMEM room for
+    // two pending-partial slots; with four, the FP32 tile's fourth-highest
+    // slots went to global memory and long contractions slowed by a tenth.
+    static constexpr int NACC = SWAP ? 4 : 3;
     static constexpr int STAGES = kStageWarps;          // shared-memory ring depth: one slot per stage warp
     static constexpr int A_STAGE = kBM * kBK * 2;       // bytes of one A stage
-    static constexpr int B_STAGE = BN * kBK * 2;        // bytes of one B stage
+    // MN-major B tiles are copied in boxes of 64 columns (one 128-byte
+    // swizzle span), so a stage holds BN rounded up to 64 columns.
+    static constexpr int B_COPY_COLS = (BN + 63) / 64 * 64;
+    static constexpr int B_STAGE = B_COPY_COLS * kBK * 2;   // bytes of one B stage
     static constexpr int STAGE_TX = A_STAGE + B_STAGE;  // TMA bytes per stage with full boxes
     static constexpr int COLS = BN / GROUPS;            // accumulator columns per epilogue thread
-    static constexpr int WORDS = F32 ? COLS : COLS / 2; // 32-bit words per value per thread (16)
+    static constexpr int WORDS = F32 ? COLS : COLS / 2; // 32-bit words per value per thread (16, or 32 for fp32)
     static constexpr int TMEM_COLS = 512;
     static constexpr int TMEM_SLOT_BASE = NACC * BN;    // after the accumulators
     static constexpr int TMEM_SLOT_STRIDE = WORDS * GROUPS;   // TMEM columns of one slot
@@ -96,7 +107,7 @@ struct Cfg {
     static constexpr int SMEM_SLOTS = SWAP ? 0 : (F32 ? 2 : 3);
     static constexpr int GLOBAL_FIRST = SMEM_FIRST + SMEM_SLOTS;
     static constexpr int GLOBAL_SLOTS = kMaxSlots - GLOBAL_FIRST;
-    static constexpr int LINE = WORDS * 4;              // bytes of one value of one thread (64)
+    static constexpr int LINE = WORDS * 4;              // bytes of one value of one thread
     static constexpr int SLOT_BYTES = EPI_WARPS * 32 * LINE;   // one slot for the whole CTA
     static constexpr int SCRATCH_CTA_BYTES = GLOBAL_SLOTS * SLOT_BYTES;
 
@@ -104,9 +115,13 @@ struct Cfg {
     static constexpr int FIRST_STAGE_WARP = EPI_WARPS;
     static constexpr int TMEM_WARP = EPI_WARPS + 1;     // allocates and frees TMEM
     static constexpr int THREADS = 32 * (EPI_WARPS + kStageWarps);
-    // Registers per thread at launch: the register split below redistributes
-    // exactly these (plain tile); the transposed tile needs no split.
-    static constexpr int LAUNCH_REGS = SWAP ? 0 : kLaunchRegs;
+    // Registers per thread at launch (the most one CTA of THREADS per SM can
+    // have): the plain tile's register split redistributes exactly these,
+    // kProdRegs to each stage warp and EPI_REGS to each epilogue warp; the
+    // transposed tile needs no split.
+    static constexpr int LAUNCH_REGS = SWAP ? 0 : (65536 / THREADS) & ~7;
+    static constexpr int EPI_REGS =
+        SWAP ? 0 : ((LAUNCH_REGS * THREADS - kProdRegs * 32 * kStageWarps) / (32 * EPI_WARPS)) & ~7;
 
     static constexpr int OFF_A = 0;
     static constexpr int OFF_B = OFF_A + STAGES * A_STAGE;
@@ -124,7 +139,8 @@ struct Cfg {
     static_assert(SCRATCH_CTA_BYTES <= kMaxScratchCtaBytes, "scratch");
     static_assert(SMEM_BYTES <= 232448, "shared memory");
     static_assert(A_STAGE % 1024 == 0 && B_STAGE % 1024 == 0, "swizzle atoms");
-    static_assert(WORDS == 16, "epilogue values are 16 words per thread");
+    static_assert(WORDS == 16 || WORDS == 32, "epilogue values are 16 or 32 words per thread");
+    static_assert(EPI_WARPS % 4 == 0, "whole TMEM lane quadrants");
 };
 
 // ----------------------------------------------------------- PTX helpers
@@ -342,6 +358,19 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
         : "memory");
 }
 
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32])
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, "
+        "%21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
+        "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
+        "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+
 __device__ __forceinline__ void reg_fence16(uint32_t (&r)[16])
 {
     asm volatile(""
@@ -424,13 +453,37 @@ __device__ __forceinline__ int problem_of(const Params &p, int u)
 
 // Every epilogue value (a rounded leaf, a partial, the root) is 16 words per
 // thread: 32 BF16 columns packed in pairs, or 16 FP32 columns.
-using Val = uint32_t[16];
+template <int W>
+using ValW = uint32_t[W];
+using Val = ValW<16>;
+
+// TMEM <-> registers for one value of W (16 or 32) words.
+template <int W>
+__device__ __forceinline__ void tmem_ld_val(uint32_t taddr, ValW<W> &t)
+{
+    if constexpr (W == 16) tmem_ld16(taddr, t);
+    else tmem_ld32(taddr, t);
+}
+
+template <int W>
+__device__ __forceinline__ void tmem_st_val(uint32_t taddr, const ValW<W> &v)
+{
+    if constexpr (W == 16) tmem_st16(taddr, v);
+    else tmem_st32(taddr, v);
+}
+
+template <int W>
+__device__ __forceinline__ void reg_fence_val(ValW<W> &t)
+{
+    if constexpr (W == 16) reg_fence16(t);
+    else reg_fence(t);
+}
 
 // What one epilogue thread needs to reach its storage.
 struct EpiCtx {
     uint32_t tmem_slot;   // TMEM address of this thread's first TMEM slot
     uint32_t smem_slot;   // shared-memory address of this thread's line in the first shared slot
-    uint8_t *scratch;     // this thread's 64-byte line in the first global slot
+    uint8_t *scratch;     // this thread's line in the first global slot
     int lane;
     int row, col;         // first output element owned by this thread
     int rows;             // rows of the output (the problem's)
@@ -438,12 +491,16 @@ struct EpiCtx {
     long long ldo;        // its leading dimension, elements
 };
 
-// 16-byte chunk k (0..3) of a thread's 64-byte shared-memory line. Lines of
-// consecutive lanes are 64 bytes apart; swizzling the chunk by lane/2 puts
-// the eight lanes of a quarter-warp access on eight distinct bank groups.
+// 16-byte chunk k of a thread's shared-memory line of CHUNKS chunks (4 or
+// 8). Lines of consecutive lanes are 16*CHUNKS bytes apart; permuting the
+// chunks by lane puts the eight lanes of a quarter-warp access on eight
+// distinct bank groups.
+template <int CHUNKS>
 __device__ __forceinline__ uint32_t smem_chunk(uint32_t line, int lane, int k)
 {
-    return line + static_cast<uint32_t>((k ^ ((lane >> 1) & 3)) * 16);
+    static_assert(CHUNKS == 4 || CHUNKS == 8, "lines of 64 or 128 bytes");
+    if constexpr (CHUNKS == 4) return line + static_cast<uint32_t>((k ^ ((lane >> 1) & 3)) * 16);
+    else return line + static_cast<uint32_t>((k ^ (lane & 7)) * 16);
 }
 
 // Writes this thread's value of the root to the output, clipped to the
@@ -456,9 +513,10 @@ __device__ __forceinline__ uint32_t smem_chunk(uint32_t line, int lane, int k)
 // to out[(c.col + j) * ldo + c.row]. The 32 lanes of a warp hold 32
 // consecutive columns, so every store of the warp writes 64 contiguous bytes.
 template <bool F32, bool SWAP>
-__device__ __forceinline__ void store_out(const Val &v, const Params &p, const EpiCtx &c)
+__device__ __forceinline__ void store_out(const ValW<Cfg<F32, SWAP>::WORDS> &v, const Params &p, const EpiCtx &c)
 {
     using C = Cfg<F32, SWAP>;
+    constexpr int W = C::WORDS;
     constexpr int ES = F32 ? 4 : 2;
     if (c.row >= c.rows) return;
     if constexpr (SWAP) {
@@ -477,7 +535,7 @@ __device__ __forceinline__ void store_out(const Val &v, const Params &p, const E
     uint8_t *dst = c.out + (static_cast<long long>(c.row) * c.ldo + c.col) * ES;
     uint8_t *vec = full ? dst : c.scratch;
 #pragma unroll
-    for (int k = 0; k < 4; ++k)
+    for (int k = 0; k < W / 4; ++k)
         asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(vec + 16 * k), "r"(v[4 * k]),
                      "r"(v[4 * k + 1]), "r"(v[4 * k + 2]), "r"(v[4 * k + 3])
                      : "memory");
@@ -541,25 +599,26 @@ __device__ __forceinline__ void row_partial(const Val &v, const Params &p, const
 
 // Slot s >= 2 (TMEM, shared memory or global scratch) -> t.
 template <bool F32, bool SWAP>
-__device__ __forceinline__ void load_slot(int s, Val &t, const EpiCtx &c)
+__device__ __forceinline__ void load_slot(int s, ValW<Cfg<F32, SWAP>::WORDS> &t, const EpiCtx &c)
 {
     using C = Cfg<F32, SWAP>;
+    constexpr int W = C::WORDS;
     if (s < C::SMEM_FIRST) {
-        tmem_ld16(c.tmem_slot + static_cast<uint32_t>((s - C::TMEM_FIRST) * C::TMEM_SLOT_STRIDE), t);
+        tmem_ld_val<W>(c.tmem_slot + static_cast<uint32_t>((s - C::TMEM_FIRST) * C::TMEM_SLOT_STRIDE), t);
         tmem_wait_ld();
-        reg_fence16(t);
+        reg_fence_val<W>(t);
     } else if (s < C::GLOBAL_FIRST) {
         const uint32_t line = c.smem_slot + static_cast<uint32_t>((s - C::SMEM_FIRST) * C::SLOT_BYTES);
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
+        for (int k = 0; k < W / 4; ++k)
             asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
                          : "=r"(t[4 * k]), "=r"(t[4 * k + 1]), "=r"(t[4 * k + 2]), "=r"(t[4 * k + 3])
-                         : "r"(smem_chunk(line, c.lane, k))
+                         : "r"(smem_chunk<W / 4>(line, c.lane, k))
                          : "memory");
     } else {
         const uint8_t *src = c.scratch + (s - C::GLOBAL_FIRST) * C::SLOT_BYTES;
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
+        for (int k = 0; k < W / 4; ++k)
             asm volatile("ld.global.v4.b32 {%0, %1, %2, %3}, [%4];"
                          : "=r"(t[4 * k]), "=r"(t[4 * k + 1]), "=r"(t[4 * k + 2]), "=r"(t[4 * k + 3])
                          : "l"(src + 16 * k)
@@ -569,54 +628,48 @@ __device__ __forceinline__ void load_slot(int s, Val &t, const EpiCtx &c)
 
 // v -> slot s >= 2 (TMEM, shared memory or global scratch).
 template <bool F32, bool SWAP>
-__device__ __forceinline__ void store_slot(int s, const Val &v, const EpiCtx &c)
+__device__ __forceinline__ void store_slot(int s, const ValW<Cfg<F32, SWAP>::WORDS> &v, const EpiCtx &c)
 {
     using C = Cfg<F32, SWAP>;
+    constexpr int W = C::WORDS;
     if (s < C::SMEM_FIRST) {
-        tmem_st16(c.tmem_slot + static_cast<uint32_t>((s - C::TMEM_FIRST) * C::TMEM_SLOT_STRIDE), v);
+        tmem_st_val<W>(c.tmem_slot + static_cast<uint32_t>((s - C::TMEM_FIRST) * C::TMEM_SLOT_STRIDE), v);
         tmem_wait_st();
     } else if (s < C::GLOBAL_FIRST) {
         const uint32_t line = c.smem_slot + static_cast<uint32_t>((s - C::SMEM_FIRST) * C::SLOT_BYTES);
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(smem_chunk(line, c.lane, k)),
+        for (int k = 0; k < W / 4; ++k)
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(smem_chunk<W / 4>(line, c.lane, k)),
                          "r"(v[4 * k]), "r"(v[4 * k + 1]), "r"(v[4 * k + 2]), "r"(v[4 * k + 3])
                          : "memory");
     } else {
         uint8_t *dst = c.scratch + (s - C::GLOBAL_FIRST) * C::SLOT_BYTES;
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
+        for (int k = 0; k < W / 4; ++k)
             asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(dst + 16 * k), "r"(v[4 * k]),
                          "r"(v[4 * k + 1]), "r"(v[4 * k + 2]), "r"(v[4 * k + 3])
                          : "memory");
     }
 }
 
-// Loads this thread's BN/4 accumulator columns (32 FP32 for the bf16
-// variant, 16 for the fp32 one) into the staging registers and waits.
-template <bool F32>
+// Loads this thread's 32 accumulator columns (FP32) into the staging
+// registers and waits.
 __device__ __forceinline__ void stage_load(uint32_t acc_taddr, uint32_t (&stg)[32])
 {
-    if constexpr (F32) {
-        uint32_t(&lo)[16] = *reinterpret_cast<uint32_t(*)[16]>(&stg[0]);
-        tmem_ld16(acc_taddr, lo);
-        tmem_wait_ld();
-        reg_fence16(lo);
-    } else {
-        tmem_ld32(acc_taddr, stg);
-        tmem_wait_ld();
-        reg_fence(stg);
-    }
+    tmem_ld32(acc_taddr, stg);
+    tmem_wait_ld();
+    reg_fence(stg);
 }
 
 // The staged leaf -> F: rounded once to BF16 (RNE), two columns per word,
 // for the bf16 variant; as is for the fp32 variant.
-template <bool F32>
-__device__ __forceinline__ void stage_convert(const uint32_t (&stg)[32], Val &F)
+template <bool F32, int W>
+__device__ __forceinline__ void stage_convert(const uint32_t (&stg)[32], ValW<W> &F)
 {
+    static_assert(W == (F32 ? 32 : 16), "32 staged columns");
     if constexpr (F32) {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) F[i] = stg[i];
+        for (int i = 0; i < W; ++i) F[i] = stg[i];
     } else {
 #pragma unroll
         for (int i = 0; i < 16; ++i) F[i] = cvt_bf16x2(stg[2 * i], stg[2 * i + 1]);
@@ -722,7 +775,8 @@ __device__ __forceinline__ void stage_role(const Params &p, const Smem<F32, SWAP
                 tma_load_2d(b_dst, &pb.tmap_b, full, k0, n0);
             } else {
 #pragma unroll
-                for (int b = 0; b < C::BN / 64; ++b) tma_load_2d(b_dst + 8192 * b, &pb.tmap_b, full, n0 + 64 * b, k0);
+                for (int b = 0; b < C::B_COPY_COLS / 64; ++b)
+                    tma_load_2d(b_dst + 8192 * b, &pb.tmap_b, full, n0 + 64 * b, k0);
             }
             if constexpr (SWAP) {
                 // Transposed tile (few output rows): the launch streams the
@@ -820,6 +874,7 @@ template <bool F32, bool GROUPED, bool SWAP>
 __device__ __forceinline__ void epilogue_role(const Params &p, const Smem<F32, SWAP> &S, int warp, int lane)
 {
     using C = Cfg<F32, SWAP>;
+    constexpr int W = C::WORDS;
     const int q = warp & 3;               // TMEM lane quadrant (rows 32q .. 32q+31)
     const int cq = warp >> 2;             // column group of the tile (a quarter, or a half when SWAP)
     const uint32_t lane_bits = static_cast<uint32_t>(q * 32) << 16;
@@ -833,7 +888,7 @@ __device__ __forceinline__ void epilogue_role(const Params &p, const Smem<F32, S
     const int units = p.units;
     const int NB = p.num_blocks;
 
-    Val A, B, Cc;
+    ValW<W> A, B, Cc;
     uint32_t stg[32];
     int acc = 0;                          // accumulator of the next leaf
     uint32_t acc_phase = 0;
@@ -841,13 +896,13 @@ __device__ __forceinline__ void epilogue_role(const Params &p, const Smem<F32, S
     // Waits for the next leaf's accumulator, loads it, hands it back to the
     // MMA (which may then fill it with the leaf NACC ahead) and rounds the
     // leaf into dst.
-    auto take = [&](Val &dst) {
+    auto take = [&](ValW<W> &dst) {
         if (!warp_wait(S.accf(acc), acc_phase, S.abort_flag, p.status, p.timeout_ns)) {
             ok = false;
             return;
         }
         tc_fence_after();
-        stage_load<F32>(acc0 + static_cast<uint32_t>(acc * C::BN), stg);
+        stage_load(acc0 + static_cast<uint32_t>(acc * C::BN), stg);
         tc_fence_before();
         __syncwarp();
         mbar_arrive_if(S.acce(acc), lane == 0);
@@ -855,11 +910,11 @@ __device__ __forceinline__ void epilogue_role(const Params &p, const Smem<F32, S
             acc = 0;
             acc_phase ^= 1u;
         }
-        stage_convert<F32>(stg, dst);
+        stage_convert<F32, W>(stg, dst);
     };
-    auto add = [](Val &left, const Val &right) {
+    auto add = [](ValW<W> &left, const ValW<W> &right) {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) left[i] = merge<F32>(left[i], right[i]);
+        for (int i = 0; i < W; ++i) left[i] = merge<F32>(left[i], right[i]);
     };
 
     for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
@@ -902,7 +957,7 @@ __device__ __forceinline__ void epilogue_role(const Params &p, const Smem<F32, S
                 if (!(m & 1u)) continue;
                 load_slot<F32, SWAP>(static_cast<int>(s), B, c);   // B is free once the block is merged
 #pragma unroll
-                for (int i = 0; i < 16; ++i) A[i] = merge<F32>(B[i], A[i]);
+                for (int i = 0; i < W; ++i) A[i] = merge<F32>(B[i], A[i]);
             }
             const int st = static_cast<int>(e >> 12);
             if (st == kSlotRoot) {
@@ -974,14 +1029,15 @@ __global__ void __launch_bounds__(Cfg<F32, SWAP>::THREADS, 1) det_gemm_kernel(co
     S.tmem = *tmem_base_smem;
 
     if constexpr (!SWAP) {
-        // Register split: the stage warpgroup gives up registers and the four
-        // epilogue warpgroups take them (kProdRegs*128 + kEpiRegs*512 fits in
-        // the kLaunchRegs*640 the CTA is launched with). Each role's code sits
-        // inside its own branch so that the compiler allocates it under the
-        // matching limit.
-        static_assert(kProdRegs * 128 + kEpiRegs * 32 * C::EPI_WARPS <= kLaunchRegs * C::THREADS, "register split");
+        // Register split: the stage warpgroup gives up registers and the
+        // epilogue warpgroups take them (kProdRegs*128 + EPI_REGS*32*EPI_WARPS
+        // fits in the LAUNCH_REGS*THREADS the CTA is launched with). Each
+        // role's code sits inside its own branch so that the compiler
+        // allocates it under the matching limit.
+        static_assert(kProdRegs * 32 * kStageWarps + C::EPI_REGS * 32 * C::EPI_WARPS <= C::LAUNCH_REGS * C::THREADS,
+                      "register split");
         if (warp < C::EPI_WARPS) {
-            asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kEpiRegs));
+            asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::EPI_REGS));
             epilogue_role<F32, GROUPED, SWAP>(p, S, warp, lane);
         } else {
             asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kProdRegs));
