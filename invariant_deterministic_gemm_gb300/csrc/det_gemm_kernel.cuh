@@ -23,6 +23,10 @@
 //              stage's MMAs; MMA issue is handed from warp to warp in stage
 //              order (turn barriers). Warp 17 also allocates and frees TMEM.
 //
+// FP32-output tile (128 x 96): 512 threads, warps 0-11 epilogue (three per
+// scheduler, column third w/4, 32 FP32 columns per thread), warps 12-15
+// stage warps.
+//
 // Transposed tile (launches with at most 64 output rows, BF16 out): the
 // MMA's A operand is the weight, so its 128 TMEM lanes are 128 output
 // columns, and its N side (64) holds the rows. 384 threads: warps 0-7
@@ -451,8 +455,8 @@ __device__ __forceinline__ int problem_of(const Params &p, int u)
 
 // ------------------------------------------------------------- epilogue
 
-// Every epilogue value (a rounded leaf, a partial, the root) is 16 words per
-// thread: 32 BF16 columns packed in pairs, or 16 FP32 columns.
+// Every epilogue value (a rounded leaf, a partial, the root) holds a
+// thread's 32 columns: 16 words of BF16 pairs, or 32 FP32 words (ValW<W>).
 template <int W>
 using ValW = uint32_t[W];
 using Val = ValW<16>;
