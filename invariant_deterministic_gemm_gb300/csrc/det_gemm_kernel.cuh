@@ -957,9 +957,9 @@ __device__ __forceinline__ void epilogue_role(const Params &p, const Smem<F32, S
             if (n >= 2) add(A, B);
             // merge with the pending left siblings above the block, lowest first
 #pragma unroll 1
-            for (uint32_t m = (e & 0x3FFu) >> C::TMEM_FIRST, s = C::TMEM_FIRST; m != 0; m >>= 1, ++s) {
-                if (!(m & 1u)) continue;
-                load_slot<F32, SWAP>(static_cast<int>(s), B, c);   // B is free once the block is merged
+            for (uint32_t m = (e & 0x3FFu) >> C::TMEM_FIRST; m != 0; m &= m - 1) {
+                const int s = C::TMEM_FIRST + __ffs(static_cast<int>(m)) - 1;   // lowest pending slot left
+                load_slot<F32, SWAP>(s, B, c);   // B is free once the block is merged
 #pragma unroll
                 for (int i = 0; i < W; ++i) A[i] = merge<F32>(B[i], A[i]);
             }
