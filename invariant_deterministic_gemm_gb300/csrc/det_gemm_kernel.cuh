@@ -23,9 +23,8 @@
 //              stage's MMAs; MMA issue is handed from warp to warp in stage
 //              order (turn barriers). Warp 17 also allocates and frees TMEM.
 //
-// FP32-output tile (128 x 96): 512 threads, warps 0-11 epilogue (three per
-// scheduler, column third w/4, 32 FP32 columns per thread), warps 12-15
-// stage warps.
+// FP32-output tile (128 x 96): the same 640 threads and roles; each
+// epilogue thread owns 24 FP32 columns.
 //
 // Transposed tile (launches with at most 64 output rows, BF16 out): the
 // MMA's A operand is the weight, so its 128 TMEM lanes are 128 output
@@ -50,8 +49,8 @@
 // tree's maximal subtrees of at most four leaves ("blocks", height <= 2)
 // entirely in registers, so only slots 2 and up ever hold a value: the
 // next slots are TMEM columns past the accumulators, then shared memory,
-// and the last three (touched at most once per 256 leaves) a per-CTA
-// global-memory scratch line of 128 bytes per thread.
+// and the deepest (slots 7-9 for BF16, touched at most once per 256
+// leaves; 6-9 for FP32) a per-CTA global-memory scratch line per thread.
 //
 // Every mbarrier wait is bounded (Params::timeout_ns of %globaltimer). On
 // expiry the waiter records DET_GEMM_ERR_TIMEOUT in the status word and sets
@@ -80,11 +79,11 @@ constexpr int kPrefetchRounds = 2;  // transposed tile: L2 prefetch distance, in
 template <bool F32, bool SWAP = false>
 struct Cfg {
     // Epilogue warps and output columns per tile (rows when SWAP). The FP32
-    // tile is 96 columns wide with three epilogue warps per scheduler, 32
+    // tile is 96 columns wide with four epilogue warps per scheduler, 24
     // FP32 columns each: an MMA of 128 rows costs the tensor core the same
     // time for any N up to 256, and 96 columns of FP32 values and pending
     // partials still fit the registers, TMEM and shared memory.
-    static constexpr int EPI_WARPS = SWAP ? 8 : (F32 ? 12 : 16);
+    static constexpr int EPI_WARPS = SWAP ? 8 : 16;
     static constexpr int GROUPS = EPI_WARPS / 4;        // epilogue warps per TMEM lane quadrant
     static constexpr int BN = SWAP ? 64 : (F32 ? 96 : 128);
     // TMEM accumulator buffers. Three in the plain tiles leave TMEM room for
@@ -99,7 +98,7 @@ struct Cfg {
     static constexpr int B_STAGE = B_COPY_COLS * kBK * 2;   // bytes of one B stage
     static constexpr int STAGE_TX = A_STAGE + B_STAGE;  // TMA bytes per stage with full boxes
     static constexpr int COLS = BN / GROUPS;            // accumulator columns per epilogue thread
-    static constexpr int WORDS = F32 ? COLS : COLS / 2; // 32-bit words per value per thread (16, or 32 for fp32)
+    static constexpr int WORDS = F32 ? COLS : COLS / 2; // 32-bit words per value per thread (16, or 24 for fp32)
     static constexpr int TMEM_COLS = 512;
     static constexpr int TMEM_SLOT_BASE = NACC * BN;    // after the accumulators
     static constexpr int TMEM_SLOT_STRIDE = WORDS * GROUPS;   // TMEM columns of one slot
@@ -143,7 +142,7 @@ struct Cfg {
     static_assert(SCRATCH_CTA_BYTES <= kMaxScratchCtaBytes, "scratch");
     static_assert(SMEM_BYTES <= 232448, "shared memory");
     static_assert(A_STAGE % 1024 == 0 && B_STAGE % 1024 == 0, "swizzle atoms");
-    static_assert(WORDS == 16 || WORDS == 32, "epilogue values are 16 or 32 words per thread");
+    static_assert(F32 ? WORDS == 24 : WORDS == 16, "epilogue values are 16 (BF16) or 24 (FP32) words per thread");
     static_assert(EPI_WARPS % 4 == 0, "whole TMEM lane quadrants");
 };
 
@@ -362,17 +361,41 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
         : "memory");
 }
 
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32])
+// 24 columns as three loads of 8: every load starts on a multiple of its
+// own width (the FP32 tile's columns are 24 * group + 8 * i).
+__device__ __forceinline__ void tmem_ld24(uint32_t taddr, uint32_t (&r)[24])
 {
     asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
-        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, "
-        "%21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%24];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%8, %9, %10, %11, %12, %13, %14, %15}, [%25];\n\t"
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%16, %17, %18, %19, %20, %21, %22, %23}, [%26];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+          "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23])
+        : "r"(taddr), "r"(taddr + 8u), "r"(taddr + 16u));
+}
+
+__device__ __forceinline__ void tmem_st24(uint32_t taddr, const uint32_t (&r)[24])
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%3, %4, %5, %6, %7, %8, %9, %10};\n\t"
+        "tcgen05.st.sync.aligned.32x32b.x8.b32 [%1], {%11, %12, %13, %14, %15, %16, %17, %18};\n\t"
+        "tcgen05.st.sync.aligned.32x32b.x8.b32 [%2], {%19, %20, %21, %22, %23, %24, %25, %26};"
+        ::"r"(taddr), "r"(taddr + 8u), "r"(taddr + 16u),
         "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
         "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
-        "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
-        "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23])
         : "memory");
+}
+
+__device__ __forceinline__ void reg_fence24(uint32_t (&r)[24])
+{
+    asm volatile(""
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                   "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                   "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]),
+                   "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]));
 }
 
 __device__ __forceinline__ void reg_fence16(uint32_t (&r)[16])
@@ -456,30 +479,35 @@ __device__ __forceinline__ int problem_of(const Params &p, int u)
 // ------------------------------------------------------------- epilogue
 
 // Every epilogue value (a rounded leaf, a partial, the root) holds a
-// thread's 32 columns: 16 words of BF16 pairs, or 32 FP32 words (ValW<W>).
+// thread's columns (ValW<W>): 32 columns as 16 words of BF16 pairs, or 24
+// FP32 words.
 template <int W>
 using ValW = uint32_t[W];
 using Val = ValW<16>;
 
-// TMEM <-> registers for one value of W (16 or 32) words.
+// TMEM <-> registers for W (16, 24 or 32) words.
 template <int W>
 __device__ __forceinline__ void tmem_ld_val(uint32_t taddr, ValW<W> &t)
 {
+    static_assert(W == 16 || W == 24 || W == 32, "TMEM load width");
     if constexpr (W == 16) tmem_ld16(taddr, t);
+    else if constexpr (W == 24) tmem_ld24(taddr, t);
     else tmem_ld32(taddr, t);
 }
 
 template <int W>
 __device__ __forceinline__ void tmem_st_val(uint32_t taddr, const ValW<W> &v)
 {
+    static_assert(W == 16 || W == 24, "TMEM store width");
     if constexpr (W == 16) tmem_st16(taddr, v);
-    else tmem_st32(taddr, v);
+    else tmem_st24(taddr, v);
 }
 
 template <int W>
 __device__ __forceinline__ void reg_fence_val(ValW<W> &t)
 {
     if constexpr (W == 16) reg_fence16(t);
+    else if constexpr (W == 24) reg_fence24(t);
     else reg_fence(t);
 }
 
@@ -495,16 +523,21 @@ struct EpiCtx {
     long long ldo;        // its leading dimension, elements
 };
 
-// 16-byte chunk k of a thread's shared-memory line of CHUNKS chunks (4 or
-// 8). Lines of consecutive lanes are 16*CHUNKS bytes apart; permuting the
+// 16-byte chunk k of a thread's shared-memory line of CHUNKS chunks (4, 6
+// or 8). Lines of consecutive lanes are 16*CHUNKS bytes apart; permuting the
 // chunks by lane puts the eight lanes of a quarter-warp access on eight
-// distinct bank groups.
+// distinct bank groups. With 96-byte lines, lanes l and l+4 of a quarter
+// start on the same bank group and the four even ones on distinct ones;
+// rotating the upper four lanes' chunks by one puts them on the odd ones.
 template <int CHUNKS>
 __device__ __forceinline__ uint32_t smem_chunk(uint32_t line, int lane, int k)
 {
-    static_assert(CHUNKS == 4 || CHUNKS == 8, "lines of 64 or 128 bytes");
+    static_assert(CHUNKS == 4 || CHUNKS == 6 || CHUNKS == 8, "lines of 64, 96 or 128 bytes");
     if constexpr (CHUNKS == 4) return line + static_cast<uint32_t>((k ^ ((lane >> 1) & 3)) * 16);
-    else return line + static_cast<uint32_t>((k ^ (lane & 7)) * 16);
+    else if constexpr (CHUNKS == 6) {
+        const int r = (lane & 4) ? (k == 5 ? 0 : k + 1) : k;
+        return line + static_cast<uint32_t>(r * 16);
+    } else return line + static_cast<uint32_t>((k ^ (lane & 7)) * 16);
 }
 
 // Writes this thread's value of the root to the output, clipped to the
@@ -656,28 +689,23 @@ __device__ __forceinline__ void store_slot(int s, const ValW<Cfg<F32, SWAP>::WOR
     }
 }
 
-// Loads this thread's 32 accumulator columns (FP32) into the staging
-// registers and waits.
-__device__ __forceinline__ void stage_load(uint32_t acc_taddr, uint32_t (&stg)[32])
+// Loads this thread's N accumulator columns (FP32) into r and waits: the
+// staging registers of a BF16 leaf (32 columns), or the value itself of an
+// FP32 leaf (24 columns).
+template <int N>
+__device__ __forceinline__ void stage_load(uint32_t acc_taddr, ValW<N> &r)
 {
-    tmem_ld32(acc_taddr, stg);
+    tmem_ld_val<N>(acc_taddr, r);
     tmem_wait_ld();
-    reg_fence(stg);
+    reg_fence_val<N>(r);
 }
 
-// The staged leaf -> F: rounded once to BF16 (RNE), two columns per word,
-// for the bf16 variant; as is for the fp32 variant.
-template <bool F32, int W>
-__device__ __forceinline__ void stage_convert(const uint32_t (&stg)[32], ValW<W> &F)
+// A staged leaf's 32 FP32 columns -> F, rounded once to BF16 (RNE), two
+// columns per word.
+__device__ __forceinline__ void round_leaf(const uint32_t (&stg)[32], Val &F)
 {
-    static_assert(W == (F32 ? 32 : 16), "32 staged columns");
-    if constexpr (F32) {
 #pragma unroll
-        for (int i = 0; i < W; ++i) F[i] = stg[i];
-    } else {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) F[i] = cvt_bf16x2(stg[2 * i], stg[2 * i + 1]);
-    }
+    for (int i = 0; i < 16; ++i) F[i] = cvt_bf16x2(stg[2 * i], stg[2 * i + 1]);
 }
 
 // ----------------------------------------------------------------- kernel
@@ -899,14 +927,15 @@ __device__ __forceinline__ void epilogue_role(const Params &p, const Smem<F32, S
     bool ok = true;
     // Waits for the next leaf's accumulator, loads it, hands it back to the
     // MMA (which may then fill it with the leaf NACC ahead) and rounds the
-    // leaf into dst.
+    // leaf into dst (an FP32 leaf is loaded into dst as is).
     auto take = [&](ValW<W> &dst) {
         if (!warp_wait(S.accf(acc), acc_phase, S.abort_flag, p.status, p.timeout_ns)) {
             ok = false;
             return;
         }
         tc_fence_after();
-        stage_load(acc0 + static_cast<uint32_t>(acc * C::BN), stg);
+        if constexpr (F32) stage_load<W>(acc0 + static_cast<uint32_t>(acc * C::BN), dst);
+        else stage_load<32>(acc0 + static_cast<uint32_t>(acc * C::BN), stg);
         tc_fence_before();
         __syncwarp();
         mbar_arrive_if(S.acce(acc), lane == 0);
@@ -914,7 +943,7 @@ __device__ __forceinline__ void epilogue_role(const Params &p, const Smem<F32, S
             acc = 0;
             acc_phase ^= 1u;
         }
-        stage_convert<F32, W>(stg, dst);
+        if constexpr (!F32) round_leaf(stg, dst);
     };
     auto add = [](ValW<W> &left, const ValW<W> &right) {
 #pragma unroll
