@@ -317,8 +317,8 @@ det_gemm_status det_gemm_tree_schedule(int64_t num_leaves, uint16_t *out);
  * of more than four leaves these have 2, 3 or 4 leaves), in leaf order;
  * out[b] describes block b: bits 10..11 hold (leaves in the block - 1);
  * bits 0..9 the pending-partial slots its value is merged with, lowest
- * first; bits 12..15 the slot its result is parked in, or 15 for the root.
- * It is the per-leaf entry of the block's last leaf (det_gemm_tree_schedule)
+ * first; bits 12..15 the slot its result is parked in, or 15 for the root
+ * (the last block, and only it). It is the per-leaf entry of the block's last leaf (det_gemm_tree_schedule)
  * with the merges inside the block removed. `out` needs num_leaves entries;
  * *num_blocks receives the count.
  */

@@ -193,6 +193,10 @@ def test_block_schedule_replays_the_mid_split_tree_for_every_leaf_count(dg):
         if L > 4:
             assert set(sizes) <= {2, 3, 4}, L
         assert replay_blocks(blocks, L) == mid_split_tree(0, L), L
+        # the BF16 kernels store the root after the walk: the last block,
+        # and only it, must form the root (store value 15)
+        stores = [e >> 12 for e in blocks]
+        assert stores[-1] == 15 and stores.count(15) == 1, L
 
 
 # ---------------------------------------------------------------- merge API
