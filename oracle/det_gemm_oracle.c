@@ -28,6 +28,8 @@
  *
  * Pins (tests/test_oracle_pins.py): exact rational rounding for bf16_round and
  * bf16_add; exact double sums within the sequential error bound for leaves;
+ * hand-derived single-leaf sums (tests/golden/leaf_order_cases.txt) whose
+ * bits differ between the ascending order and a descending or pairwise one;
  * identity / permutation / all-ones / small-integer closed forms for the
  * whole GEMM; the half-K child identity; a hand-built three-leaf example that
  * separates the floor split from the left-to-right chain and from the ceil

@@ -20,6 +20,7 @@ import oracle
 import workloads as W
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "tree_split_cases.txt")
+LEAF_ORDER = os.path.join(os.path.dirname(__file__), "golden", "leaf_order_cases.txt")
 
 
 def f32_bits(x):
@@ -148,6 +149,42 @@ def test_single_leaf_gemm_is_rounded_dot_product():
                     assert got == exact.rne(q), (Kc, i, j)
                 else:
                     assert got in (lo, hi), (Kc, i, j)
+
+
+def _leaf_order_rows():
+    rows = []
+    with open(LEAF_ORDER) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            name, x, y, leaf32, leaf16, _ = [p.strip() for p in line.split("|", 5)]
+            rows.append((name, np.array([int(h, 16) for h in x.split()], np.uint16),
+                         np.array([int(h, 16) for h in y.split()], np.uint16), int(leaf32, 16), int(leaf16, 16)))
+    return rows
+
+
+@pytest.mark.parametrize("case", _leaf_order_rows(), ids=lambda c: c[0])
+def test_leaf_sums_its_products_in_ascending_k(case):
+    """The FP32 leaf and the single-leaf products of every entry point match
+    hand-derived sums in ascending k order (tests/golden/leaf_order_cases.txt,
+    where a descending or pairwise loop gives other bits). dA and dB reach
+    the same contraction through their own operand layouts."""
+    _, x, y, leaf32, leaf16 = case
+    Kc = x.size
+    assert x.size == y.size <= 32
+    X, Y = x[None, :], y[:, None]
+    assert int(oracle.leaves_f32(X, Y, 0, 0)[0].view(np.uint32)) == leaf32
+    assert int(f32_bits(oracle.fwd_fp32(X, Y))[0, 0]) == leaf32
+    assert int(oracle.fwd(X, Y)[0, 0]) == leaf16
+    assert int(oracle.fwd_rhs_transposed(X, y[None, :])[0, 0]) == leaf16
+    # dA[0, 0] = sum_n dC[0, n] B[0, n]: dC = x as a row, B = y as a row
+    assert int(oracle.da(X, y[None, :])[0, 0]) == leaf16
+    # dB[0, 0] = sum_m A[m, 0] dC[m, 0]: the contraction runs down the rows
+    A = np.ascontiguousarray(np.stack([x, np.zeros(Kc, np.uint16)], axis=1))
+    dC = np.ascontiguousarray(np.stack([y, np.zeros(Kc, np.uint16)], axis=1))
+    assert int(oracle.db(A, dC)[0, 0]) == leaf16
+    assert int(oracle.db_transposed(A, dC)[0, 0]) == leaf16
 
 
 # -------------------------------------------------------------- trees -----
