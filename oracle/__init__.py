@@ -215,8 +215,9 @@ def rmsnorm(x: np.ndarray, w: np.ndarray, eps: float) -> np.ndarray:
 
 def rowdot(C: np.ndarray, D: np.ndarray) -> np.ndarray:
     """rowdot[i] = sum_n C[i, n] * D[i, n] (BF16 bits in, FP32 out) in the
-    grouped-GEMM epilogue's fixed order (see oracle_rowdot in
-    det_gemm_oracle.c)."""
+    grouped-GEMM epilogue's fixed order: one slot per 128-column N-tile (its
+    FP32 sum in ascending column order), the slots merged by the mid-split
+    tree (see oracle_rowdot in det_gemm_oracle.c)."""
     lib = _load()
     C = np.ascontiguousarray(C, dtype=np.uint16)
     D = np.ascontiguousarray(D, dtype=np.uint16)

@@ -327,13 +327,13 @@ int oracle_rmsnorm(const uint16_t *x, int64_t ldx, const uint16_t *w, int64_t M,
 /*
  * rowdot[i] = sum over n of C[i, n] * D[i, n] in FP32, in the fixed order of
  * the grouped-GEMM epilogue (Megatron Core notes, "Kernel redesign: the
- * grouped-GEMM epilogue": per-tile private slots, then a fixed reduction
- * tree, instead of atomic adds across N-tiles). The order is this
- * library's reading: columns are cut into tiles of 128 and quarters of 32;
- * a quarter's value is the FP32 sum of its products (exact: BF16 x BF16) in
- * ascending column order from +0, a quarter past the last column is +0;
- * a tile's value is ((q0 + q1) + (q2 + q3)); rowdot is the mid-split tree of
- * FP32 adds over the tiles (the contraction's tree, tiles for leaves).
+ * grouped-GEMM epilogue": each N-tile writes its own private slot, and the
+ * slots are combined by a fixed reduction tree instead of atomic adds
+ * across N-tiles). Reading: an N-tile is 128 columns (the GEMM's fixed
+ * output tile width); its slot holds the FP32 sum of its products (exact:
+ * BF16 x BF16) in ascending column order from +0, the same running sum a
+ * leaf uses; rowdot is the mid-split tree of FP32 adds over the slots (the
+ * contraction's tree, with slots for leaves).
  */
 int oracle_rowdot(const uint16_t *C, int64_t ldc, const uint16_t *D, int64_t ldd, int64_t M, int64_t N,
                   float *out)
@@ -344,15 +344,9 @@ int oracle_rowdot(const uint16_t *C, int64_t ldc, const uint16_t *D, int64_t ldd
     if (!tiles) return -1;
     for (int64_t i = 0; i < M; ++i) {
         for (int64_t t = 0; t < T; ++t) {
-            float q[4];
-            for (int k = 0; k < 4; ++k) {
-                float s = 0.0f;
-                const int64_t c0 = 128 * t + 32 * k;
-                for (int64_t n = c0; n < c0 + 32 && n < N; ++n)
-                    s = s + bf16_to_f32(C[i * ldc + n]) * bf16_to_f32(D[i * ldd + n]);
-                q[k] = s;
-            }
-            tiles[t] = (q[0] + q[1]) + (q[2] + q[3]);
+            const int64_t c0 = 128 * t;
+            const int64_t c1 = (c0 + 128 < N) ? c0 + 128 : N;
+            tiles[t] = leaf_f32(C + i * ldc, 1, D + i * ldd, 1, c0, c1);
         }
         float mx = 0.0f;
         out[i] = tree_f32(tiles, 0, T, &mx);

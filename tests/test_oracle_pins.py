@@ -471,6 +471,10 @@ def test_rowdot_order_separates_tiles_from_a_running_sum():
     # Three column tiles with dot values 1, 2^-24, 2^-24. The fixed order is
     # the mid-split tree over tiles: 1 + (2^-24 + 2^-24) = 1 + 2^-23 (exact);
     # a running sum would give (1 + 2^-24) + 2^-24 = 1 (ties to even twice).
+    # The same products also fix the tile width: tiles of 256 columns give
+    # slots 1 + 2^-24 = 1 and 2^-24, root 1; tiles of 64 give six slots
+    # 1, 0, 2^-24, 0, 2^-24, 0 and the root (1 + (0 + 2^-24)) + (0 + (2^-24
+    # + 0)) = 1.
     N = 3 * 128
     C = np.zeros((1, N), dtype=np.float32)
     D = np.zeros((1, N), dtype=np.float32)
@@ -482,15 +486,29 @@ def test_rowdot_order_separates_tiles_from_a_running_sum():
     assert oracle.rowdot(cb, db)[0] == np.float32(1.0 + 2.0 ** -23)
 
 
-def test_rowdot_quarters_combine_as_two_pairs():
-    # One tile with quarter values 2^-24, 2^-24, 1, 0 (one product each).
-    # Pairs: (2^-24 + 2^-24) + (1 + 0) = 2^-23 + 1, exact. A running sum over
-    # the quarters would give ((2^-24 + 2^-24) + 1) + 0, the same here, but a
-    # running sum over the row's columns or the pair (q0 + q2) first would
-    # not: 2^-24 + 1 rounds to 1 (a tie, to even).
-    C = np.zeros((1, 128), dtype=np.float32)
-    C[0, 0] = 2.0 ** -12
-    C[0, 32] = 2.0 ** -12
-    C[0, 64] = 1.0
-    cb = W.bits(torch.from_numpy(C).to(torch.bfloat16))
-    assert oracle.rowdot(cb, cb)[0] == np.float32(1.0 + 2.0 ** -23)
+def _one_row(N, products):
+    """BF16 bits of one row C and one row D whose products C[n] * D[n] are
+    the given powers of two (column -> value), all other products zero."""
+    C = np.zeros((1, N), dtype=np.float32)
+    D = np.zeros((1, N), dtype=np.float32)
+    for n, v in products.items():
+        e = int(np.log2(v))
+        C[0, n], D[0, n] = 2.0 ** (e // 2), 2.0 ** (e - e // 2)
+    return (W.bits(torch.from_numpy(C).to(torch.bfloat16)), W.bits(torch.from_numpy(D).to(torch.bfloat16)))
+
+
+def test_rowdot_sums_a_tile_in_ascending_column_order():
+    """One 128-column tile holding 1 and 127 products 2^-24 (u = 2^-23).
+    Ascending from column 0: each 1 + 2^-24 is a tie that stays 1, so the
+    slot is 1. A descending sum gives 1 + 63.5u, a tie to the even 1 + 64u;
+    32-column quarters merged in pairs give (1 + 16u) + 32u = 1 + 48u. With
+    the 1 in the last column instead, ascending gives 127 x 2^-24 exactly,
+    then 1 + 63.5u ties to 1 + 64u, and descending gives 1."""
+    prods = {0: 1.0}
+    prods.update({n: 2.0 ** -24 for n in range(1, 128)})
+    c, d = _one_row(128, prods)
+    assert int(f32_bits(oracle.rowdot(c, d))[0]) == 0x3F800000
+    prods = {127: 1.0}
+    prods.update({n: 2.0 ** -24 for n in range(0, 127)})
+    c, d = _one_row(128, prods)
+    assert int(f32_bits(oracle.rowdot(c, d))[0]) == 0x3F800040
