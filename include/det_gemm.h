@@ -162,11 +162,11 @@ det_gemm_status det_gemm_db_transposed(const det_gemm_bf16 *A, const det_gemm_bf
  * describe as accumulated atomically across N-tiles, section "Kernel
  * redesign: the grouped-GEMM epilogue"): when rowdot and rowdot[g] are not
  * NULL, rowdot[g][i] = sum over n of C_g[i, n] * D_g[i, n] in FP32, formed
- * with private per-tile partial slots and a fixed reduction order, never
- * with atomics: for each 128-column tile t and 32-column quarter q the FP32
- * sum of the (exact) products in ascending column order; each tile's
- * quarters combined as ((q0 + q1) + (q2 + q3)); the tiles by the mid-split
- * tree of FP32 adds. Same bits every run. N must then be <= 131072 (1024
+ * with one private slot per 128-column N-tile and a fixed reduction order,
+ * never with atomics: a tile's slot is the FP32 sum of its (exact) products
+ * in ascending column order from +0, and the slots are merged by the
+ * mid-split tree of FP32 adds. The reduction runs after the product, from
+ * the stored C_g. Same bits every run. N must then be <= 131072 (1024
  * column tiles).
  *
  *   A[g]    device, [M[g],K] BF16, row pitch lda[g]
@@ -262,9 +262,11 @@ det_gemm_status det_rmsnorm(const det_gemm_bf16 *x, const det_gemm_bf16 *w, det_
  * library holds it until the process exits), and allocates nothing: no
  * cudaMalloc, no cudaFree, no host allocation.
  *
- *   - The first call on a device looks up the array's device address
- *     (cudaGetSymbolAddress) and initialises the library's state for that
- *     device; make that first call before any stream capture.
+ *   - The first call on a device does all of the set-up for that device:
+ *     the library's state, the attributes of both kernels a forward launch
+ *     can take (the plain tile, and the transposed tile for at most 64
+ *     rows), and the array's device address (cudaGetSymbolAddress). Later
+ *     calls do none of it. Make that first call before any stream capture.
  *   - The array holds scratch for 160 CTAs (one per SM up to 160 SMs). A
  *     launch that would need more is rejected with DET_GEMM_ERR_INVALID_ARG
  *     before anything is enqueued (det_gemm_last_error_detail says why).

@@ -455,6 +455,7 @@ det_gemm_status run_problems(Variant v, bool a_kmajor, bool b_kmajor, const Prob
 
     Params p;
     std::memset(&p, 0, sizeof(p));
+    uint8_t *rd_slots = nullptr;   // the row reduction's slots (scratch)
     p.num_problems = g;
     p.n_tiles = static_cast<int>(n_tiles);
     int64_t units = 0;
@@ -494,11 +495,7 @@ det_gemm_status run_problems(Variant v, bool a_kmajor, bool b_kmajor, const Prob
         pb.out = const_cast<void *>(q.out.ptr);
         pb.ldo = q.out.ld;
         choose_tile_order(pb, q.rows, cols, kc, ops.bn, p.n_tiles);
-        if (q.rowdot) {
-            pb.rd_d = static_cast<const uint16_t *>(q.d);
-            pb.rd_ldd = q.ldd;
-            rd_bytes += align256(sizeof(float) * 4 * n_tiles * q.rows);
-        }
+        if (q.rowdot) rd_bytes += align256(sizeof(float) * ((cols + kRowdotTile - 1) / kRowdotTile) * q.rows);
     }
     if (units > (int64_t{1} << 31) - 1) return DET_GEMM_ERR_INVALID_ARG;
     p.units = static_cast<int>(units);
@@ -517,19 +514,14 @@ det_gemm_status run_problems(Variant v, bool a_kmajor, bool b_kmajor, const Prob
         cudaGetDevice(&dev);
         // The deep-slot part is sized for the largest variant and a grid of
         // one CTA per SM, so every launch on this stream can reuse it; the
-        // part slabs of a split launch and the row-reduction partials
-        // follow it.
+        // part slabs of a split launch and the row reduction's slots follow
+        // it.
         const size_t slot_bytes = static_cast<size_t>(st->sm_count) * kMaxScratchCtaBytes;
         uint8_t *base = static_cast<uint8_t *>(scratch_for(dev, stream, slot_bytes + part_bytes + rd_bytes));
         if (!base) return DET_GEMM_ERR_LAUNCH;
         p.scratch = base;
         p.part_out = parts > 1 ? base + slot_bytes : nullptr;
-        uint8_t *rd = base + slot_bytes + part_bytes;
-        for (int i = 0; i < g; ++i) {
-            if (!pa[i].rowdot || pa[i].rows == 0) continue;
-            p.prob[i].rd_part = reinterpret_cast<float *>(rd);
-            rd += align256(sizeof(float) * 4 * n_tiles * pa[i].rows);
-        }
+        rd_slots = base + slot_bytes + part_bytes;
     }
     p.parts = parts;
     p.part_ld = part_ld;
@@ -565,10 +557,17 @@ det_gemm_status run_problems(Variant v, bool a_kmajor, bool b_kmajor, const Prob
                                                   const_cast<void *>(pa[0].out.ptr), pa[0].out.ld, stream);
         if (me != cudaSuccess) return fail_cuda(DET_GEMM_ERR_LAUNCH, me, "merge launch");
     }
+    // Row reductions: after the product, from the stored output (each
+    // problem's slots follow the previous one's in the scratch).
     for (int i = 0; i < g; ++i) {
         if (!pa[i].rowdot || pa[i].rows == 0) continue;
-        const cudaError_t re = launch_rowdot_reduce(p.prob[i].rd_part, p.prob[i].rows, p.n_tiles, pa[i].rowdot, stream);
+        const ProblemArgs &q = pa[i];
+        const cudaError_t re =
+            launch_rowdot(static_cast<const uint16_t *>(q.out.ptr), q.out.ld, static_cast<const uint16_t *>(q.d), q.ldd,
+                          static_cast<int>(q.rows), static_cast<int>(cols), reinterpret_cast<float *>(rd_slots),
+                          q.rowdot, stream);
         if (re != cudaSuccess) return fail_cuda(DET_GEMM_ERR_LAUNCH, re, "row reduction launch");
+        rd_slots += align256(sizeof(float) * ((cols + kRowdotTile - 1) / kRowdotTile) * q.rows);
     }
     return DET_GEMM_OK;
 }
@@ -638,6 +637,15 @@ int fwd_with_fixed_scratch_status(const void *A, const void *B, void *C, long lo
 }
 
 void record_detail(const char *msg) { std::snprintf(g_detail, sizeof g_detail, "%s", msg); }
+
+int prepare_forward_status()
+{
+    DeviceState *st = nullptr;
+    det_gemm_status s = device_state(&st);
+    if (s == DET_GEMM_OK) s = prepare_variant(st, kBf16KMN);
+    if (s == DET_GEMM_OK) s = prepare_variant(st, kBf16SwapMNK);
+    return static_cast<int>(s);
+}
 
 }  // namespace detg
 
@@ -739,10 +747,8 @@ det_gemm_status det_gemm_fwd_grouped(int G, const det_gemm_bf16 *const *A, const
             pa[j] = ProblemArgs{bf16(A[i], M[i], K, lda[i]), bf16(B[i], K, N, ldb[i]), bf16(C[i], M[i], N, ldc[i]),
                                 M[i], rd ? D[i] : nullptr, rd ? ldd[i] : 0, rd ? rowdot[i] : nullptr};
         }
-        // One problem without a row reduction is a plain launch (same bits).
-        bool reduce = false;
-        for (int j = 0; j < g; ++j) reduce = reduce || pa[j].rowdot != nullptr;
-        const Variant v = (g > 1 || reduce) ? kBf16KMNGrouped : kBf16KMN;
+        // One problem is a plain launch (same bits).
+        const Variant v = g > 1 ? kBf16KMNGrouped : kBf16KMN;
         const det_gemm_status s = run_problems(v, true, false, pa, g, N, K, reinterpret_cast<cudaStream_t>(stream));
         if (s != DET_GEMM_OK) return s;
     }

@@ -44,9 +44,6 @@ struct Problem {
     CUtensorMap tmap_b;           // "B operand": contraction x output columns
     void *out;                    // row-major output, rows x cols
     long long ldo;                // output leading dimension, elements
-    float *rd_part;               // row reduction: per (column tile, quarter) partials [4 n_tiles][rows], or null
-    const uint16_t *rd_d;         // row reduction: the BF16 [rows, cols] operand D, row pitch rd_ldd
-    long long rd_ldd;
     int rows;                     // output rows
     int m_tiles;
     int first_unit;               // index of this problem's first work unit in the launch
@@ -99,9 +96,13 @@ cudaError_t launch_merge_parts(bool f32, const void *part, int parts, int rows, 
 cudaError_t launch_merge_list(bool f32, const void *const *parts, int n, int rows, int cols, long long ldp, void *out,
                               long long ldo, cudaStream_t stream);
 
-// Row reduction of a grouped launch: rowdot[i] = the partials of row i
-// (four per column tile, written by the kernel) combined in a fixed order.
-cudaError_t launch_rowdot_reduce(const float *part, int rows, int n_tiles, float *rowdot, cudaStream_t stream);
+// Row reduction of a grouped launch: rowdot[i] = sum over n of C[i, n] *
+// D[i, n] in a fixed order (one slot per 128-column tile, the FP32 sum of
+// its products in ascending column order; slots merged by the mid-split
+// tree). `slots` is scratch for ceil(cols / 128) * rows floats.
+constexpr int kRowdotTile = 128;
+cudaError_t launch_rowdot(const uint16_t *C, long long ldc, const uint16_t *D, long long ldd, int rows, int cols,
+                          float *slots, float *rowdot, cudaStream_t stream);
 
 // Batch-invariant RMSNorm (det_rmsnorm): one warp per row.
 struct RmsParams {
@@ -135,5 +136,9 @@ int fwd_with_fixed_scratch_status(const void *A, const void *B, void *C, long lo
                                   size_t scratch_bytes);
 // Stores a message for det_gemm_last_error_detail().
 void record_detail(const char *msg);
+// Sets up the current device's library state and both kernels a BF16
+// forward launch can take (the plain tile, and the transposed tile for at
+// most kSwapMaxRows rows). Returns a det_gemm_status.
+int prepare_forward_status();
 
 }  // namespace detg

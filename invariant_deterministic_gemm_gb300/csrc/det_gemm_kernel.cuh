@@ -591,49 +591,6 @@ __device__ __forceinline__ void store_out(const ValW<Cfg<F32, SWAP>::WORDS> &v, 
     }
 }
 
-// Row reduction of a grouped launch (bf16 variant): this thread's share of
-// rowdot[row] = sum over columns n of C[row, n] * D[row, n], for its 32
-// columns of column tile nt and quarter cq: the FP32 sum of the products
-// (exact: BF16 x BF16) in ascending column order, from +0 (+0 for a quarter
-// entirely past the last column). It goes to its own slot; no other thread
-// writes there, and the slots are combined later in a fixed order.
-__device__ __forceinline__ void row_partial(const Val &v, const Params &p, const Problem &pb, const EpiCtx &c,
-                                            int nt, int cq)
-{
-    if (c.row >= c.rows) return;
-    const int ncols = p.cols - c.col;
-    float s = 0.0f;
-    if (ncols > 0) {
-        const uint16_t *d = pb.rd_d + static_cast<long long>(c.row) * pb.rd_ldd + c.col;
-        uint32_t dw[16];
-        if (ncols >= 32) {
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const uint4 x = *reinterpret_cast<const uint4 *>(d + 8 * k);
-                dw[4 * k] = x.x;
-                dw[4 * k + 1] = x.y;
-                dw[4 * k + 2] = x.z;
-                dw[4 * k + 3] = x.w;
-            }
-        } else {
-#pragma unroll
-            for (int k = 0; k < 16; ++k) {
-                const uint32_t lo = 2 * k < ncols ? d[2 * k] : 0u;
-                const uint32_t hi = 2 * k + 1 < ncols ? d[2 * k + 1] : 0u;
-                dw[k] = lo | (hi << 16);
-            }
-        }
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {
-            if (2 * k < ncols)
-                s = __fadd_rn(s, __fmul_rn(__uint_as_float(v[k] << 16), __uint_as_float(dw[k] << 16)));
-            if (2 * k + 1 < ncols)
-                s = __fadd_rn(s, __fmul_rn(__uint_as_float(v[k] & 0xFFFF0000u), __uint_as_float(dw[k] & 0xFFFF0000u)));
-        }
-    }
-    pb.rd_part[static_cast<long long>(nt * 4 + cq) * pb.rows + c.row] = s;
-}
-
 // Slot s >= 2 (TMEM, shared memory or global scratch) -> t.
 template <bool F32, bool SWAP>
 __device__ __forceinline__ void load_slot(int s, ValW<Cfg<F32, SWAP>::WORDS> &t, const EpiCtx &c)
@@ -1004,12 +961,7 @@ __device__ __forceinline__ void epilogue_role(const Params &p, const Smem<F32, S
         // variants store it after the walk, which keeps that once-per-tile
         // code out of the block loop (2 % faster on their launches); the
         // FP32 variant measured 6 % slower that way and stores it in place.
-        if constexpr (!F32) {
-            store_out<F32, SWAP>(A, p, c);
-            if constexpr (GROUPED) {
-                if (pb.rd_part != nullptr) row_partial(A, p, pb, c, nt, cq);
-            }
-        }
+        if constexpr (!F32) store_out<F32, SWAP>(A, p, c);
     }
 }
 

@@ -77,14 +77,13 @@ cudaError_t launch_merge(bool f32, const PartPtrs &at, int parts, int rows, int 
     return cudaGetLastError();
 }
 
-// Row reduction of a grouped launch. The kernel leaves, for every row i,
-// one FP32 partial per (column tile t, quarter q): part[(4 t + q) rows + i].
-// rowdot[i] combines them in a fixed order: each tile's four quarters as
-// ((q0 + q1) + (q2 + q3)), then the tiles by the same mid-split tree of FP32
-// adds the contraction uses, walked with its per-leaf schedule (pending left
-// children in slots). No atomics: the same bits every run, whichever CTA
-// wrote which partial first (Megatron Core notes, "Kernel redesign: the
-// grouped-GEMM epilogue": private per-tile slots, then a fixed tree).
+// Row reduction of a grouped launch (Megatron Core notes, "Kernel redesign:
+// the grouped-GEMM epilogue": a private slot per N-tile, then a fixed tree,
+// instead of atomic adds across N-tiles). It runs after the product, from
+// the stored output: rowdot_slots_kernel forms every (row, 128-column tile)
+// slot, rowdot_reduce_kernel merges each row's slots by the mid-split tree
+// of FP32 adds the contraction uses, walked with its per-leaf schedule. The
+// same bits every run, whichever CTA computed which tile first.
 struct RowdotParams {
     const float *part;
     float *rowdot;
@@ -92,16 +91,51 @@ struct RowdotParams {
     uint16_t sched[kMaxLeaves];
 };
 
+// One slot of the row reduction per thread: slot (t, i) = the FP32 sum of
+// C[i, n] * D[i, n] over the columns n of tile t in ascending order, from
+// +0. A product of two BF16 values is exact in FP32, so every step is one
+// rounding, as in a leaf. Rows are 16-byte aligned and tiles start on 256
+// bytes, so whole groups of eight columns are read with 16-byte loads.
+__global__ void rowdot_slots_kernel(const uint16_t *C, long long ldc, const uint16_t *D, long long ldd, int rows,
+                                    int cols, int n_tiles, float *slots)
+{
+    const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (idx >= static_cast<long long>(rows) * n_tiles) return;
+    const int i = static_cast<int>(idx / n_tiles);
+    const int t = static_cast<int>(idx - static_cast<long long>(i) * n_tiles);
+    const int c0 = kRowdotTile * t;
+    const int c1 = min(c0 + kRowdotTile, cols);
+    const uint16_t *c = C + static_cast<long long>(i) * ldc;
+    const uint16_t *d = D + static_cast<long long>(i) * ldd;
+    auto bf = [](uint32_t h) { return __uint_as_float(h << 16); };
+    float s = 0.0f;
+    int n = c0;
+    for (; n + 8 <= c1; n += 8) {
+        const uint4 x = *reinterpret_cast<const uint4 *>(c + n);
+        const uint4 y = *reinterpret_cast<const uint4 *>(d + n);
+        const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
+        const uint32_t ys[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            s = __fadd_rn(s, __fmul_rn(bf(xs[k] & 0xFFFFu), bf(ys[k] & 0xFFFFu)));
+            s = __fadd_rn(s, __fmul_rn(bf(xs[k] >> 16), bf(ys[k] >> 16)));
+        }
+    }
+    for (; n < c1; ++n) s = __fadd_rn(s, __fmul_rn(bf(c[n]), bf(d[n])));
+    slots[static_cast<long long>(t) * rows + i] = s;
+}
+
+// rowdot[i]: the slots of row i merged by the mid-split tree of FP32 adds,
+// walked with its per-leaf schedule (det_gemm_tree_schedule, slots for
+// leaves).
 __global__ void rowdot_reduce_kernel(const __grid_constant__ RowdotParams p)
 {
     const int i = blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= p.rows) return;
     float slot[kMaxSlots];
     float root = 0.0f;
-    const long long stride = p.rows;
     for (int t = 0; t < p.n_tiles; ++t) {
-        const float *q = p.part + static_cast<long long>(4 * t) * stride + i;
-        float v = __fadd_rn(__fadd_rn(q[0], q[stride]), __fadd_rn(q[2 * stride], q[3 * stride]));
+        float v = p.part[static_cast<long long>(t) * p.rows + i];
         const uint32_t e = p.sched[t];
 #pragma unroll
         for (int s = 0; s < kMaxSlots; ++s)
@@ -135,17 +169,24 @@ cudaError_t launch_merge_list(bool f32, const void *const *parts, int n, int row
     return launch_merge(f32, at, n, rows, cols, ldp, out, ldo, stream);
 }
 
-cudaError_t launch_rowdot_reduce(const float *part, int rows, int n_tiles, float *rowdot, cudaStream_t stream)
+cudaError_t launch_rowdot(const uint16_t *C, long long ldc, const uint16_t *D, long long ldd, int rows, int cols,
+                          float *slots, float *rowdot, cudaStream_t stream)
 {
     if (rows <= 0) return cudaSuccess;
+    const int n_tiles = (cols + kRowdotTile - 1) / kRowdotTile;
     if (n_tiles < 1 || n_tiles > kMaxLeaves) return cudaErrorInvalidValue;
     RowdotParams p;
-    p.part = part;
+    p.part = slots;
     p.rowdot = rowdot;
     p.rows = rows;
     p.n_tiles = n_tiles;
     if (det_gemm_tree_schedule(n_tiles, p.sched) != DET_GEMM_OK) return cudaErrorInvalidValue;
     const int threads = 128;
+    const long long work = static_cast<long long>(rows) * n_tiles;
+    rowdot_slots_kernel<<<static_cast<unsigned>((work + threads - 1) / threads), threads, 0, stream>>>(
+        C, ldc, D, ldd, rows, cols, n_tiles, slots);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
     rowdot_reduce_kernel<<<(rows + threads - 1) / threads, threads, 0, stream>>>(p);
     return cudaGetLastError();
 }

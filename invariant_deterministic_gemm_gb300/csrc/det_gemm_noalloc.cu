@@ -30,23 +30,32 @@ constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 bool g_done[kMaxDevices] = {};
 void *g_addr[kMaxDevices] = {};
-cudaError_t g_err[kMaxDevices] = {};
+int g_setup_status[kMaxDevices] = {};
 
-// The device address of g_noalloc_scratch on the current device. In host
-// code the array's name is only a host-side handle; the address the kernel
-// must be given is looked up once per device, with that device current.
-void *scratch_address(int dev, cudaError_t *err)
+// Set-up, once per device, with that device current: the library's state
+// and the kernel attributes of both kernels a forward launch can take, then
+// the device address of g_noalloc_scratch (in host code the array's name is
+// only a host-side handle; the address the kernel must be given is looked
+// up here), so that no later call does any set-up work.
+int setup(int dev, void **scratch)
 {
     std::lock_guard<std::mutex> lk(g_mu);
     if (!g_done[dev]) {
         g_done[dev] = true;
+        g_setup_status[dev] = detg::prepare_forward_status();
         void *ptr = nullptr;
-        g_err[dev] = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
-        g_addr[dev] = (g_err[dev] == cudaSuccess) ? ptr : nullptr;
-        if (g_err[dev] != cudaSuccess) cudaGetLastError();
+        if (g_setup_status[dev] == DET_GEMM_OK) {
+            if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr) {
+                cudaGetLastError();
+                detg::record_detail("cudaGetSymbolAddress failed for the no-alloc scratch array");
+                g_setup_status[dev] = DET_GEMM_ERR_LAUNCH;
+            } else {
+                g_addr[dev] = ptr;
+            }
+        }
     }
-    *err = g_err[dev];
-    return g_addr[dev];
+    *scratch = g_addr[dev];
+    return g_setup_status[dev];
 }
 
 }  // namespace
@@ -60,12 +69,9 @@ extern "C" det_gemm_status det_gemm_fwd_noalloc(const det_gemm_bf16 *A, const de
         cudaGetLastError();
         return DET_GEMM_ERR_UNSUPPORTED_DEVICE;
     }
-    cudaError_t err = cudaSuccess;
-    void *scratch = scratch_address(dev, &err);
-    if (!scratch) {
-        detg::record_detail("cudaGetSymbolAddress failed for the no-alloc scratch array");
-        return DET_GEMM_ERR_LAUNCH;
-    }
+    void *scratch = nullptr;
+    const int st = setup(dev, &scratch);
+    if (st != DET_GEMM_OK) return static_cast<det_gemm_status>(st);
     return static_cast<det_gemm_status>(detg::fwd_with_fixed_scratch_status(
         A, B, C, M, N, K, lda, ldb, ldc, reinterpret_cast<cudaStream_t>(stream), scratch, kNoAllocScratchBytes));
 }

@@ -72,3 +72,33 @@ def test_grouped_row_reduction_is_the_oracle_fixed_order(N):
     Cs2, rd2 = dg.det_gemm_fwd_grouped(As, Bs, D=Ds)
     for g in (0, 2):
         assert torch.equal(rd[g], rd2[g])
+
+
+def test_grouped_row_reduction_order_on_hand_built_rows():
+    """The row reduction's order, pinned on the GPU with hand-derived bits.
+    B is the identity, so C = A exactly (a one-product leaf is its own
+    rounding), and D = A makes every product C*D a chosen power of two
+    (u = 2^-23). Row 0: 1 then 127 products 2^-24 in one 128-column tile:
+    ascending keeps 1 (each add is a tie to even). Row 1: the same with the 1
+    in the tile's last column: 127 x 2^-24 = 63.5u first, then 1 + 63.5u
+    ties to 1 + 64u. Row 2: products 1, 2^-24, 2^-24 at the starts of three
+    tiles: the mid-split tree gives 1 + (2^-24 + 2^-24) = 1 + u, where a
+    running sum would give 1."""
+    N = 384
+    A = torch.zeros(3, N, dtype=torch.float32)
+    A[0, 0] = 1.0
+    A[0, 1:128] = 2.0 ** -12
+    A[1, 127] = 1.0
+    A[1, 0:127] = 2.0 ** -12
+    A[2, 0] = 1.0
+    A[2, 128] = 2.0 ** -12
+    A[2, 256] = 2.0 ** -12
+    Ab = A.to(torch.bfloat16).cuda()
+    eye = torch.eye(N, dtype=torch.bfloat16).cuda()
+    Cs, rd = dg.det_gemm_fwd_grouped([Ab], [eye], D=[Ab])
+    check()
+    assert torch.equal(bits(Cs[0]), bits(Ab))
+    got = rd[0].cpu().numpy().view(np.uint32)
+    assert list(got) == [0x3F800000, 0x3F800040, 0x3F800001], [hex(x) for x in got]
+    want = oracle.rowdot(W.bits(Ab.cpu()), W.bits(Ab.cpu()))
+    assert np.array_equal(got, want.view(np.uint32))

@@ -1,18 +1,20 @@
 """det_gemm_fwd_noalloc: the forward product for callers that cannot
-allocate device memory (stream capture, caller-owned memory arenas, paths
-that must not synchronise the device). It must give exactly what
-det_gemm_fwd gives -- the same kernel and arithmetic, with its scratch in a
-fixed array of the library instead of a cudaMalloc'd buffer -- call after
-call, whatever an earlier call left in that array.
+allocate device memory -- code being captured into a CUDA graph (cudaMalloc
+may not run while a stream captures), serving paths that hand every byte of
+device memory out of their own arena, and paths that must never trigger the
+device-wide synchronisation an allocation can imply. It must give exactly
+what det_gemm_fwd gives (the same kernel and arithmetic, with its scratch in
+a fixed array of the library instead of a cudaMalloc'd buffer), call after
+call, whatever an earlier call left in that array, and it must leave the
+device's free memory untouched.
 
 The shapes make the kernel use the array: a contraction of 32768 (1024
 leaves) parks the tree's highest pending partials there, and a ragged
-column count sends the output of the last column tile through it.
+column count sends the output of the last column tile through it. A third
+shape with 5 rows takes the transposed tile.
 
 This file is named to be collected last, so that a run stopping at its first
 failure has already run every other test."""
-import ctypes
-
 import pytest
 import torch
 
@@ -21,6 +23,8 @@ import workloads as W
 from gpu_util import check, dev
 
 pytestmark = pytest.mark.gpu
+
+SHAPES = [(200, 300, 32768), (129, 136, 5000), (5, 264, 4096)]
 
 
 def _noalloc(A, B, out):
@@ -33,14 +37,28 @@ def _noalloc(A, B, out):
     assert st == 0, dg.status_string(st)
 
 
-@pytest.mark.parametrize("shapes", [[(200, 300, 32768), (129, 136, 5000)]])
-def test_noalloc_forward_matches_det_gemm_fwd_on_two_calls_in_a_row(shapes):
-    for i, (M, N, K) in enumerate(shapes):
+def test_noalloc_forward_matches_det_gemm_fwd_on_two_calls_in_a_row_and_allocates_nothing():
+    ins, refs, outs = [], [], []
+    for i, (M, N, K) in enumerate(SHAPES):
         A = dev(W.randn_bf16((M, K), 1.0, 9100 + i))
         B = dev(W.randn_bf16((K, N), 0.02, 9200 + i))
-        out = dev(torch.zeros(M, N, dtype=torch.bfloat16))
-        _noalloc(A, B, out)
-        ref = dg.det_gemm_fwd(A, B)
-        check()
-        # identical kernel and arithmetic: equal bit for bit
-        assert torch.equal(out.contiguous().view(torch.int16), ref.contiguous().view(torch.int16)), (M, N, K)
+        ins.append((A, B))
+        refs.append(dg.det_gemm_fwd(A, B))
+        outs.append(dev(torch.zeros(M, N, dtype=torch.bfloat16)))     # 16-byte row pitch
+    # one call first: its set-up (and the kernels' first load) comes before
+    # the measurement
+    _noalloc(ins[0][0], ins[0][1], outs[0])
+    check()
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    for rep in range(2):                                   # two calls in a row per shape
+        for (A, B), out in zip(ins, outs):
+            out.zero_()
+            _noalloc(A, B, out)
+        torch.cuda.synchronize()
+        for (M, N, K), out, ref in zip(SHAPES, outs, refs):
+            # identical kernel and arithmetic: equal bit for bit
+            assert torch.equal(out.contiguous().view(torch.int16), ref.contiguous().view(torch.int16)), (rep, M, N, K)
+    free1, _ = torch.cuda.mem_get_info()
+    check()
+    assert free1 == free0, "device free memory changed by %d bytes" % (free0 - free1)
