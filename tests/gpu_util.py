@@ -10,6 +10,13 @@ import workloads as W
 
 DEV = "cuda"
 
+# Parity rates of every BF16 comparison within tolerance, in call order:
+# (what, elements, bit-equal fraction, fraction within 1 ulp of the tree's
+# largest node S, fraction within 1 ulp of |C|, largest |difference| in
+# ulp(S)). tests/conftest.py prints them after the run and, when
+# DET_GEMM_RATES_OUT names a file, writes them there as JSON lines.
+RATES = []
+
 
 def f32(h):
     return oracle.bf16_bits_to_f32(h)
@@ -22,7 +29,7 @@ def ulp_bf16(x):
     return np.ldexp(1.0, (e - 7).astype(np.int64))
 
 
-def assert_bf16_close(got_bits, want_bits, node_max, num_leaves, what="", max_frac_above_1ulp=1e-3):
+def assert_bf16_close(got_bits, want_bits, node_max, num_leaves, what="", max_frac_above_1ulp=1e-4):
     """Tolerance for BF16 outputs, derived from the arithmetic.
 
     The GPU and the oracle differ only in the FP32 summation order inside a
@@ -33,8 +40,15 @@ def assert_bf16_close(got_bits, want_bits, node_max, num_leaves, what="", max_fr
     rounds. Hence, with S the largest |node| of the oracle's tree for the
     element and d = ceil(log2 L) the tree depth:
       - every element is within (1 + d) ulp(S) (one flipped leaf), and
-      - all but a small fraction are within 1 ulp(S) (the north-star
-        bound; exceeding it needs a flip whose effect survives cancellation).
+      - all but a fraction max_frac_above_1ulp of the elements are within
+        1 ulp(S), the benchmark spec's bound read against the tree's largest
+        node; exceeding it needs a flipped leaf whose effect survives the
+        later roundings. Measured over every comparison of the GPU suite:
+        5 of about 2.4 million elements, each at exactly 2 ulp(S), the most
+        in one comparison a fraction of 1.7e-5 (RATES records the rates of
+        each run). The inputs are seeded and the kernel deterministic, so
+        the same elements exceed it on every run; 1e-4 is the regression
+        threshold.
     Returns (bit-equal fraction, fraction within 1 ulp(S), fraction within
     1 ulp of |C|)."""
     g = f32(got_bits).astype(np.float64)
@@ -54,9 +68,11 @@ def assert_bf16_close(got_bits, want_bits, node_max, num_leaves, what="", max_fr
             what, int(bad.sum()), int(ok.sum()), depth,
             [(tuple(i), float(g[tuple(i)]), float(w[tuple(i)]), float(u[tuple(i)])) for i in idx]))
     above = float((d > u)[ok].mean()) if ok.any() else 0.0
-    assert above <= max_frac_above_1ulp, "%s: %.2e of elements beyond 1 ulp(S)" % (what, above)
     same = float(((g == w) | (nan_g & nan_w)).mean())
     lit = float((d <= ulp_bf16(np.abs(w)))[ok].mean()) if ok.any() else 1.0
+    worst = float((d / u)[ok].max()) if ok.any() else 0.0
+    RATES.append((what, int(ok.sum()), same, 1.0 - above, lit, worst))
+    assert above <= max_frac_above_1ulp, "%s: %.2e of elements beyond 1 ulp(S)" % (what, above)
     return same, 1.0 - above, lit
 
 

@@ -100,14 +100,15 @@ def test_normal_inputs_within_one_ulp_of_oracle(M, N, K):
             assert_f32_close(g, want[name][0], want[name][1], name)
         else:
             L = (kc.get(name, K) + 31) // 32
-            assert_bf16_close(g, want[name][0], want[name][1], L, name)
+            assert_bf16_close(g, want[name][0], want[name][1], L, "%s %dx%dx%d" % (name, M, N, K))
 
 
-@pytest.mark.parametrize("M,N,K", [(150, 140, 224), (40, 130, 1000), (17, 33, 4096)])
+@pytest.mark.parametrize("M,N,K", [(150, 140, 224), (40, 130, 1000), (17, 33, 4096), (9, 20, 14336)])
 def test_result_is_the_oracle_tree_over_the_gpu_leaves(M, N, K):
     """C_gpu == tree(leaves_gpu) exactly, where leaves_gpu[l] is the GPU's
     BF16 result on the single leaf l alone (a one-leaf product is its own
-    root); and every GPU leaf is within one leaf-ulp of the oracle's."""
+    root); and every GPU leaf is within one leaf-ulp of the oracle's.
+    K = 14336 is 448 leaves: the tree's ranges of 7 leaves split 3 + 4."""
     A, B, _ = _operands(M, N, K, 4000 + K)
     Ag, Bg = dev(A), dev(B)
     C = W.bits(dg.det_gemm_fwd(Ag, Bg))

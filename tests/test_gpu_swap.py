@@ -6,7 +6,19 @@ bits do not depend on how many rows are computed with it (RL-Kernel,
 "Guarantees"), so every case here checks the transposed launch against the
 same rows computed by the plain tile (more than 64 rows), bit for bit, and
 against the oracle on exact inputs and within the derived tolerance on
-normal ones."""
+normal ones.
+
+Why the bits can be equal: with the operands' roles swapped the tensor core
+still forms, for each output element, the same 32 products of the same
+BF16 pairs (a product of two BF16 values is exact and commutative) into a
+fresh FP32 accumulator, in the same two K = 16 steps; what could differ is
+only how the hardware orders and aligns those products inside a step if
+that depended on the operand roles. The stress cases below are built to
+expose such a dependence: products spread over 60 binades, so that the
+alignment of a hardware FP32 sum decides which low bits survive, and sums
+of signed powers of two that land exactly on BF16 rounding midpoints with
+residues far below them, over contractions from one leaf to 1024 leaves,
+at row counts on both sides of 64."""
 import numpy as np
 import pytest
 import torch
@@ -105,3 +117,42 @@ def test_normal_inputs_within_tolerance_of_oracle():
     assert_bf16_close(got, want, nodemax, K // 32, "fwd, 3 rows")
     want_t, nodemax_t = oracle.gemm(W.bits(A), np.ascontiguousarray(W.bits(Wt).T), with_node_max=True)
     assert_bf16_close(got_t, want_t, nodemax_t, K // 32, "rhs_transposed, 3 rows")
+
+
+ADV_KC = [32, 96, 4096, 14336, 32768]
+
+
+def _adversarial(kind, shape, seed):
+    if kind == "normal":
+        return W.randn_bf16(shape, 1.0, seed)
+    if kind == "wide":
+        return W.wide_exponent_bf16(shape, -15, 15, seed)
+    # "ties": signed powers of two; products 1, 2^-8, 2^-9 sum onto BF16
+    # midpoints, products near 2^-24 .. 2^-34 are residues an FP32 sum may
+    # keep or drop depending on its alignment
+    return W.power_of_two_bf16(shape, [0, 0, 0, -8, -9, -12, -17], seed)
+
+
+@pytest.mark.parametrize("kind", ["normal", "wide", "ties"])
+@pytest.mark.parametrize("Kc", ADV_KC)
+def test_transposed_tile_equals_the_plain_tile_on_stress_inputs(kind, Kc):
+    """Five seeds per case. Rows 1, 17, 64 take the transposed tile (both of
+    its instances: B stored [K, N] for the forward, and K-major operands for
+    the rhs-transposed forward and dA); rows 65 and 128 take the plain tile;
+    all are compared with the same rows of a 256-row launch."""
+    N = 192                                            # two column tiles, the second ragged
+    for seed in range(5):
+        base = 20000 + 100 * seed + Kc
+        A = dev(_adversarial(kind, (256, Kc), base))
+        B = dev(_adversarial(kind, (Kc, N), base + 1))
+        Wt = dev(_adversarial(kind, (N, Kc), base + 2))
+        dC = dev(_adversarial(kind, (256, Kc), base + 3))    # dA with contraction Kc
+        Bd = dev(_adversarial(kind, (N, Kc), base + 4))      # dA = dC Bd^T: [256, N]
+        full = dg.det_gemm_fwd(A, B)
+        full_t = dg.det_gemm_fwd_rhs_transposed(A, Wt)
+        full_da = dg.det_gemm_da(dC, Bd)
+        for M in (1, 17, 64, 65, 128):
+            assert bits_equal(dg.det_gemm_fwd(A[:M], B), full[:M]), (kind, Kc, seed, M, "fwd")
+            assert bits_equal(dg.det_gemm_fwd_rhs_transposed(A[:M], Wt), full_t[:M]), (kind, Kc, seed, M, "rhs_t")
+            assert bits_equal(dg.det_gemm_da(dC[:M], Bd), full_da[:M]), (kind, Kc, seed, M, "da")
+        check()

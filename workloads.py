@@ -55,6 +55,39 @@ def randint_bf16(shape, lo: int, hi: int, seed: int) -> torch.Tensor:
     return x.to(torch.float32).to(torch.bfloat16)
 
 
+def randint_bf16_cuda(shape, lo: int, hi: int, seed: int) -> torch.Tensor:
+    """CUDA BF16 tensor of integers uniform in [lo, hi], drawn on the device
+    from a seeded CUDA generator (for operands of a gigabyte or more)."""
+    g = torch.Generator(device="cuda").manual_seed(int(seed))
+    x = torch.randint(lo, hi + 1, tuple(shape), generator=g, dtype=torch.int32, device="cuda")
+    return x.to(torch.bfloat16)
+
+
+def wide_exponent_bf16(shape, emin: int, emax: int, seed: int) -> torch.Tensor:
+    """CPU BF16 tensor of values +-(1 + m/128) * 2^e with the sign, the 7
+    mantissa bits m and the exponent e in [emin, emax] all uniform: operands
+    whose products span many binades, so that the order and alignment of a
+    hardware FP32 sum matter."""
+    g = torch.Generator(device="cpu").manual_seed(int(seed))
+    e = torch.randint(emin, emax + 1, tuple(shape), generator=g, dtype=torch.int32)
+    m = torch.randint(0, 128, tuple(shape), generator=g, dtype=torch.int32)
+    sgn = torch.randint(0, 2, tuple(shape), generator=g, dtype=torch.int32)
+    h = (sgn << 15) | ((e + 127) << 7) | m
+    return h.to(torch.int16).view(torch.bfloat16)
+
+
+def power_of_two_bf16(shape, exponents, seed: int) -> torch.Tensor:
+    """CPU BF16 tensor of +-2^e with a uniform random sign and e drawn
+    uniformly from the given list: sums of such products land exactly on
+    BF16 rounding midpoints often, with small residues below them."""
+    g = torch.Generator(device="cpu").manual_seed(int(seed))
+    ex = torch.tensor(list(exponents), dtype=torch.int32)
+    e = ex[torch.randint(0, len(exponents), tuple(shape), generator=g)]
+    sgn = torch.randint(0, 2, tuple(shape), generator=g, dtype=torch.int32)
+    h = (sgn << 15) | ((e + 127) << 7)
+    return h.to(torch.int16).view(torch.bfloat16)
+
+
 def garbage_bf16(shape, seed: int) -> torch.Tensor:
     """CPU BF16 tensor of uniformly random 16-bit patterns (NaN/Inf included)."""
     g = torch.Generator(device="cpu").manual_seed(int(seed))
