@@ -365,7 +365,10 @@ def gpu_arm(args):
     dom = max(by_kernel, key=lambda k: sum(by_kernel[k]))
     dom_ms = float(np.mean(by_kernel[dom]))
     achieved = FLOP_PER_GEMM / (dom_ms * 1e-3) / 1e12
-    peak = pk["bf16_sustained"]
+    # The timed region lasts well under a second at the maximum SM clock
+    # (see "clocks"), so the kernel is held against the burst figure; the
+    # sustained one (a seconds-long loop under the power cap) is context.
+    peak = pk["bf16_burst"]
     traffic = traffic_from_profiles(dom)
     launches = {}
     for i, (name, kern, kc) in enumerate(LAUNCHES):
@@ -392,7 +395,9 @@ def gpu_arm(args):
         "impl": "det_gemm_gb300",
         "roofline": {"bound": "tensor", "kernel": "det_gemm_kernel<%s>" % dom, "achieved": round(achieved, 1),
                      "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
-                     "peak_source": "%s bf16_tflops_sustained (kernel timed inside a long step)" % pk["source"],
+                     "peak_source": "%s bf16_tflops (burst: the timed region is %.2f s at the clocks below)" % (
+                         pk["source"], ms_total * 1e-3),
+                     "peak_sustained": pk["bf16_sustained"], "frac_of_sustained": round(achieved / pk["bf16_sustained"], 4),
                      "flop_per_launch": FLOP_PER_GEMM, "traffic": traffic},
         "launches": launches,
         "e2e": {"value": round(whole_job_tflops(flop_step, ws, e2e_ms), 2), "unit": "TFLOP/s",
@@ -402,6 +407,9 @@ def gpu_arm(args):
                 "results_bitwise_equal_to_device_run": e2e_equal},
         "gpu_launches": n_l * args.steps,
         "clocks": clk,
+        "context": torch_context(dev_in, step, per_launch_ms, args),
+        "configs": {c["workload"]: {k: v for k, v in c.items() if k != "workload"}
+                    for c in measure_configs(dg, device, pk, HEADLINE_CONFIGS)},
     }
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(max_seconds=args.cpu_seconds)
@@ -409,6 +417,51 @@ def gpu_arm(args):
     if ws > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def torch_context(dev_in, step, per_launch_ms, args):
+    """torch.matmul (cuBLAS) on the step's six products, TF32 and reduced-
+    precision BF16 reductions off, timed like the step: context only, and
+    the determinism tax t_det / t_torch - 1 (Megatron Core notes: the
+    overhead of the deterministic path against the fastest one). cuBLAS has
+    no FP32-output form of a BF16 product here, so the FP32-output launch is
+    set against cuBLAS's BF16-output product of the same operands."""
+    torch.backends.cuda.matmul.allow_tf32 = False
+    torch.backends.cuda.matmul.allow_bf16_reduced_precision_reduction = False
+    t = dev_in
+    prods = [
+        lambda: torch.matmul(t["x"], t["w_up"], out=step.h),
+        lambda: torch.matmul(step.h, t["w_down"]),
+        lambda: torch.matmul(t["dy"], t["w_down"].t(), out=step.dh),
+        lambda: torch.matmul(step.h.t(), t["dy"], out=step.dwd),
+        lambda: torch.matmul(step.dh, t["w_up"].t(), out=step.dx),
+        lambda: torch.matmul(step.dh.t(), t["x"], out=step.dwu),
+    ]
+    for _ in range(args.warmup):
+        for fn in prods:
+            fn()
+    n = max(3, min(args.steps, 10))
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in prods] for _ in range(n)]
+    torch.cuda.synchronize()
+    for k in range(n):
+        for i, fn in enumerate(prods):
+            ev[k][i][0].record()
+            fn()
+            ev[k][i][1].record()
+    torch.cuda.synchronize()
+    tms = np.array([[ev[k][i][0].elapsed_time(ev[k][i][1]) for i in range(len(prods))] for k in range(n)]).mean(axis=0)
+    dms = per_launch_ms.mean(axis=0)
+    per = {}
+    for i, (name, _, _) in enumerate(LAUNCHES):
+        per[name] = {"torch_ms": round(float(tms[i]), 4),
+                     "torch_tflops": round(FLOP_PER_GEMM / (tms[i] * 1e-3) / 1e12, 1),
+                     "determinism_tax": round(float(dms[i] / tms[i] - 1.0), 3)}
+    return {"what": "torch.matmul (cuBLAS), allow_tf32=False, allow_bf16_reduced_precision_reduction=False; "
+                    "fwd_fp32_down against cuBLAS's BF16-output product",
+            "torch_step_ms": round(float(tms.sum()), 4),
+            "torch_tflops": round(FLOP_PER_GEMM * len(prods) / (tms.sum() * 1e-3) / 1e12, 1),
+            "determinism_tax_step": round(float(dms.sum() / tms.sum() - 1.0), 3),
+            "launches": per}
 
 
 # ------------------------------------------------------------- CPU oracle
@@ -533,15 +586,18 @@ def single_arm(args):
                       "tflops_best": round(flop / (best * 1e-3) / 1e12, 1)}))
 
 
-def configs_arm(args):
-    """Times every workload of the page on one GPU (not the headline line):
-    the QKV sweep over M, the LM head in BF16 and FP32 output, the long-K
-    product, and the tiny case. Prints one JSON object per workload with
-    TFLOP/s and the fraction of the roofline max(flops / peak, bytes / HBM)."""
-    import invariant_deterministic_gemm_gb300 as dg
-    dg.lib()
-    dev = torch.device("cuda", 0)
-    pk = peaks()
+# Workloads of the page timed in the headline line (the rest with --configs).
+HEADLINE_CONFIGS = ("qkv1", "qkv17", "qkv256", "qkv4096", "lm_head", "long_k")
+
+
+def measure_configs(dg, dev, pk, which):
+    """Times the page's workloads on one GPU and returns one dict each, with
+    TFLOP/s, the fraction of the roofline max(flops / burst peak, bytes / HBM)
+    and, where cuBLAS has the same product, torch.matmul with TF32 off and
+    the determinism tax. `which` selects from: qkv<M> (M in 1, 3, 17, 256,
+    1024, 4096; L2 flushed before every run), lm_head (BF16 and FP32 out),
+    long_k, moe, rmsnorm, tiny."""
+    out = []
 
     def timeit(fn, iters=10, flush=None):
         fn()
@@ -563,88 +619,104 @@ def configs_arm(args):
 
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)   # 256 MB > L2
 
-    def report(name, ms, flop, nbytes, torch_ms=None):
+    def report(name, ms, flop, nbytes, torch_ms=None, **extra):
         t_roof = max(flop / (pk["bf16_burst"] * 1e12), nbytes / (pk["hbm"] * 1e9))
-        out = {"workload": name, "ms": round(ms, 4), "tflops": round(flop / (ms * 1e-3) / 1e12, 1),
-               "roofline_frac": round(t_roof / (ms * 1e-3), 4),
-               "bound": "tensor" if flop / (pk["bf16_burst"] * 1e12) >= nbytes / (pk["hbm"] * 1e9) else "hbm",
-               "peaks": "%s burst bf16 %.0f TFLOP/s, HBM %.0f GB/s" % (pk["source"], pk["bf16_burst"], pk["hbm"])}
+        r = {"workload": name, "ms": round(ms, 4), "tflops": round(flop / (ms * 1e-3) / 1e12, 1),
+             "roofline_frac": round(t_roof / (ms * 1e-3), 4),
+             "bound": "tensor" if flop / (pk["bf16_burst"] * 1e12) >= nbytes / (pk["hbm"] * 1e9) else "hbm",
+             "peaks": "%s burst bf16 %.0f TFLOP/s, HBM %.0f GB/s" % (pk["source"], pk["bf16_burst"], pk["hbm"])}
         if torch_ms is not None:
-            out["torch_matmul_ms"] = round(torch_ms, 4)
-            out["determinism_tax"] = round(ms / torch_ms - 1.0, 3)
-        print(json.dumps(out), flush=True)
+            r["torch_matmul_ms"] = round(torch_ms, 4)
+            r["determinism_tax"] = round(ms / torch_ms - 1.0, 3)
+        r.update(extra)
+        out.append(r)
 
     torch.backends.cuda.matmul.allow_tf32 = False
     torch.backends.cuda.matmul.allow_bf16_reduced_precision_reduction = False
 
-    # QKV: one A, every row count
-    A = W.randn_bf16((4096, 4096), W.STD_ACT, W.seed_for(W.QKV, W.T_A)).to(dev)
-    B = W.randn_bf16((4096, 12288), W.STD_W, W.seed_for(W.QKV, W.T_B)).to(dev)
-    for M in (1, 3, 17, 256, 1024, 4096):
-        a = A[:M]
-        ms = timeit(lambda: dg.det_gemm_fwd(a, B), flush=flush)
-        tms = timeit(lambda: torch.matmul(a, B), flush=flush)
-        report("qkv M=%d [%d,4096]@[4096,12288]" % (M, M), ms, 2.0 * M * 4096 * 12288,
-               2 * (M * 4096 + 4096 * 12288 + M * 12288), tms)
-    del A, B
-    # LM head, weight stored [151936, 4096]
-    A = W.randn_bf16((2048, 4096), W.STD_ACT, W.seed_for(W.LMHEAD, W.T_A)).to(dev)
-    Wt = W.randn_bf16((151936, 4096), W.STD_W, W.seed_for(W.LMHEAD, W.T_B)).to(dev)
-    C = torch.empty((2048, 151936), dtype=torch.bfloat16, device=dev)
-    C32 = torch.empty((2048, 151936), dtype=torch.float32, device=dev)
-    flop = 2.0 * 2048 * 4096 * 151936
-    ins = 2 * (2048 * 4096 + 151936 * 4096)
-    ms = timeit(lambda: dg.det_gemm_fwd_rhs_transposed(A, Wt, out=C), iters=5)
-    tms = timeit(lambda: torch.matmul(A, Wt.t()), iters=5)
-    report("lm_head bf16 out [2048,4096]@[151936,4096]^T", ms, flop, ins + 2 * 2048 * 151936, tms)
-    ms = timeit(lambda: dg.det_gemm_fwd_fp32_rhs_transposed(A, Wt, out=C32), iters=5)
-    report("lm_head fp32 out [2048,4096]@[151936,4096]^T", ms, flop, ins + 4 * 2048 * 151936)
-    del A, Wt, C, C32
-    # long K
-    A = W.randn_bf16((4096, 32768), 1.0, W.seed_for(W.LONGK, W.T_A)).to(dev)
-    B = W.randn_bf16((32768, 4096), 1.0, W.seed_for(W.LONGK, W.T_B)).to(dev)
-    ms = timeit(lambda: dg.det_gemm_fwd(A, B), iters=5)
-    tms = timeit(lambda: torch.matmul(A, B), iters=5)
-    report("long_k [4096,32768]@[32768,4096]", ms, 2.0 * 4096 * 32768 * 4096,
-           2 * (2 * 4096 * 32768 + 4096 * 4096), tms)
-    del A, B
-    # mixture-of-experts: 8 experts of an MLP up projection (4096 -> 14336),
-    # 8192 routed tokens split unevenly, one grouped launch vs one launch per
-    # expert; with the fixed-order row reduction against a second operand
-    counts = [2048, 1536, 1280, 1024, 896, 768, 384, 256]
-    Ae = [W.randn_bf16((m, 4096), W.STD_ACT, W.seed_for(W.MLP, W.T_A) + 300 + g).to(dev) for g, m in enumerate(counts)]
-    Be = [W.randn_bf16((4096, 1792), W.STD_W, W.seed_for(W.MLP, W.T_B) + 300 + g).to(dev) for g in range(8)]
-    De = [W.randn_bf16((m, 1792), W.STD_DC, W.seed_for(W.MLP, W.T_DC) + 300 + g).to(dev) for g, m in enumerate(counts)]
-    Ce = [torch.empty((m, 1792), dtype=torch.bfloat16, device=dev) for m in counts]
-    flop = 2.0 * sum(counts) * 4096 * 1792
-    ms = timeit(lambda: dg.det_gemm_fwd_grouped(Ae, Be, outs=Ce), iters=10, flush=flush)
-    ms_loop = timeit(lambda: [dg.det_gemm_fwd(a, b, out=c) for a, b, c in zip(Ae, Be, Ce)], iters=10, flush=flush)
-    ms_rd = timeit(lambda: dg.det_gemm_fwd_grouped(Ae, Be, outs=Ce, D=De), iters=10, flush=flush)
-    print(json.dumps({"workload": "moe grouped 8 experts, 8192 tokens [m_g,4096]@[4096,1792]", "ms": round(ms, 4),
-                      "tflops": round(flop / (ms * 1e-3) / 1e12, 1),
-                      "one_launch_per_expert_ms": round(ms_loop, 4), "with_row_reduction_ms": round(ms_rd, 4),
-                      "roofline_frac": round(flop / (pk["bf16_burst"] * 1e12) / (ms * 1e-3), 4), "bound": "tensor",
-                      "peaks": "%s burst bf16 %.0f TFLOP/s" % (pk["source"], pk["bf16_burst"])}), flush=True)
-    del Ae, Be, De, Ce
-    # batch-invariant RMSNorm over the MLP activations (HBM-bound: read x and
-    # w, write y)
-    x = W.randn_bf16((8192, 4096), W.STD_ACT, W.seed_for(W.MLP, W.T_A)).to(dev)
-    wn = W.randn_bf16((4096,), 1.0, W.seed_for(W.MLP, W.T_B) + 200).to(dev)
-    yn = torch.empty_like(x)
-    ms = timeit(lambda: dg.det_rmsnorm(x, wn, 1e-6, out=yn), flush=flush)
-    nbytes = 2 * (2 * 8192 * 4096 + 4096)
-    tms = timeit(lambda: torch.nn.functional.rms_norm(x, (4096,), wn, 1e-6), flush=flush)
-    print(json.dumps({"workload": "rmsnorm [8192,4096]", "ms": round(ms, 4),
-                      "gb_per_s": round(nbytes / (ms * 1e-3) / 1e9, 1),
-                      "roofline_frac": round(nbytes / (pk["hbm"] * 1e9) / (ms * 1e-3), 4), "bound": "hbm",
-                      "peaks": "%s HBM %.0f GB/s" % (pk["source"], pk["hbm"]),
-                      "torch_rms_norm_ms": round(tms, 4)}), flush=True)
-    del x, yn
-    # tiny
-    A = W.randn_bf16((64, 256), 1.0, W.seed_for(W.TINY, W.T_A)).to(dev)
-    B = W.randn_bf16((256, 64), 1.0, W.seed_for(W.TINY, W.T_B)).to(dev)
-    ms = timeit(lambda: dg.det_gemm_fwd(A, B), iters=20)
-    report("tiny [64,256]@[256,64]", ms, 2.0 * 64 * 256 * 64, 2 * (64 * 256 + 256 * 64 + 64 * 64))
+    qkv = [int(w[3:]) for w in which if w.startswith("qkv")]
+    if qkv:
+        # QKV: one A, every row count; the 100 MB weight is flushed from L2
+        A = W.randn_bf16((4096, 4096), W.STD_ACT, W.seed_for(W.QKV, W.T_A)).to(dev)
+        B = W.randn_bf16((4096, 12288), W.STD_W, W.seed_for(W.QKV, W.T_B)).to(dev)
+        for M in qkv:
+            a = A[:M]
+            ms = timeit(lambda: dg.det_gemm_fwd(a, B), flush=flush)
+            tms = timeit(lambda: torch.matmul(a, B), flush=flush)
+            report("qkv M=%d [%d,4096]@[4096,12288]" % (M, M), ms, 2.0 * M * 4096 * 12288,
+                   2 * (M * 4096 + 4096 * 12288 + M * 12288), tms, l2="flushed before every run")
+        del A, B
+    if "lm_head" in which:
+        # LM head, weight stored [151936, 4096]
+        A = W.randn_bf16((2048, 4096), W.STD_ACT, W.seed_for(W.LMHEAD, W.T_A)).to(dev)
+        Wt = W.randn_bf16((151936, 4096), W.STD_W, W.seed_for(W.LMHEAD, W.T_B)).to(dev)
+        C = torch.empty((2048, 151936), dtype=torch.bfloat16, device=dev)
+        C32 = torch.empty((2048, 151936), dtype=torch.float32, device=dev)
+        flop = 2.0 * 2048 * 4096 * 151936
+        ins = 2 * (2048 * 4096 + 151936 * 4096)
+        ms = timeit(lambda: dg.det_gemm_fwd_rhs_transposed(A, Wt, out=C), iters=5)
+        tms = timeit(lambda: torch.matmul(A, Wt.t()), iters=5)
+        report("lm_head bf16 out [2048,4096]@[151936,4096]^T", ms, flop, ins + 2 * 2048 * 151936, tms)
+        ms = timeit(lambda: dg.det_gemm_fwd_fp32_rhs_transposed(A, Wt, out=C32), iters=5)
+        report("lm_head fp32 out [2048,4096]@[151936,4096]^T", ms, flop, ins + 4 * 2048 * 151936)
+        del A, Wt, C, C32
+    if "long_k" in which:
+        A = W.randn_bf16((4096, 32768), 1.0, W.seed_for(W.LONGK, W.T_A)).to(dev)
+        B = W.randn_bf16((32768, 4096), 1.0, W.seed_for(W.LONGK, W.T_B)).to(dev)
+        ms = timeit(lambda: dg.det_gemm_fwd(A, B), iters=5)
+        tms = timeit(lambda: torch.matmul(A, B), iters=5)
+        report("long_k [4096,32768]@[32768,4096]", ms, 2.0 * 4096 * 32768 * 4096,
+               2 * (2 * 4096 * 32768 + 4096 * 4096), tms)
+        del A, B
+    if "moe" in which:
+        # mixture-of-experts: 8 experts of [m_g, 4096] @ [4096, 1792], 8192
+        # routed tokens split unevenly; one grouped launch against one launch
+        # per expert, and with the fixed-order row reduction
+        counts = [2048, 1536, 1280, 1024, 896, 768, 384, 256]
+        Ae = [W.randn_bf16((m, 4096), W.STD_ACT, W.seed_for(W.MLP, W.T_A) + 300 + g).to(dev) for g, m in enumerate(counts)]
+        Be = [W.randn_bf16((4096, 1792), W.STD_W, W.seed_for(W.MLP, W.T_B) + 300 + g).to(dev) for g in range(8)]
+        De = [W.randn_bf16((m, 1792), W.STD_DC, W.seed_for(W.MLP, W.T_DC) + 300 + g).to(dev) for g, m in enumerate(counts)]
+        Ce = [torch.empty((m, 1792), dtype=torch.bfloat16, device=dev) for m in counts]
+        flop = 2.0 * sum(counts) * 4096 * 1792
+        nbytes = 2 * sum(m * 4096 + 4096 * 1792 + m * 1792 for m in counts)
+        ms = timeit(lambda: dg.det_gemm_fwd_grouped(Ae, Be, outs=Ce), iters=10, flush=flush)
+        ms_loop = timeit(lambda: [dg.det_gemm_fwd(a, b, out=c) for a, b, c in zip(Ae, Be, Ce)], iters=10, flush=flush)
+        ms_rd = timeit(lambda: dg.det_gemm_fwd_grouped(Ae, Be, outs=Ce, D=De), iters=10, flush=flush)
+        report("moe grouped 8 experts, 8192 tokens [m_g,4096]@[4096,1792]", ms, flop, nbytes,
+               one_launch_per_expert_ms=round(ms_loop, 4), with_row_reduction_ms=round(ms_rd, 4))
+        del Ae, Be, De, Ce
+    if "rmsnorm" in which:
+        # batch-invariant RMSNorm over the MLP activations (HBM-bound)
+        x = W.randn_bf16((8192, 4096), W.STD_ACT, W.seed_for(W.MLP, W.T_A)).to(dev)
+        wn = W.randn_bf16((4096,), 1.0, W.seed_for(W.MLP, W.T_B) + 200).to(dev)
+        yn = torch.empty_like(x)
+        ms = timeit(lambda: dg.det_rmsnorm(x, wn, 1e-6, out=yn), flush=flush)
+        nbytes = 2 * (2 * 8192 * 4096 + 4096)
+        tms = timeit(lambda: torch.nn.functional.rms_norm(x, (4096,), wn, 1e-6), flush=flush)
+        out.append({"workload": "rmsnorm [8192,4096]", "ms": round(ms, 4),
+                    "gb_per_s": round(nbytes / (ms * 1e-3) / 1e9, 1),
+                    "roofline_frac": round(nbytes / (pk["hbm"] * 1e9) / (ms * 1e-3), 4), "bound": "hbm",
+                    "peaks": "%s HBM %.0f GB/s" % (pk["source"], pk["hbm"]),
+                    "torch_rms_norm_ms": round(tms, 4)})
+        del x, yn
+    if "tiny" in which:
+        A = W.randn_bf16((64, 256), 1.0, W.seed_for(W.TINY, W.T_A)).to(dev)
+        B = W.randn_bf16((256, 64), 1.0, W.seed_for(W.TINY, W.T_B)).to(dev)
+        ms = timeit(lambda: dg.det_gemm_fwd(A, B), iters=20)
+        report("tiny [64,256]@[256,64]", ms, 2.0 * 64 * 256 * 64, 2 * (64 * 256 + 256 * 64 + 64 * 64))
+    del flush
+    return out
+
+
+def configs_arm(args):
+    """Times every workload of the page on one GPU (not the headline line)
+    and prints one JSON object per workload."""
+    import invariant_deterministic_gemm_gb300 as dg
+    dg.lib()
+    dev = torch.device("cuda", 0)
+    which = ("qkv1", "qkv3", "qkv17", "qkv256", "qkv1024", "qkv4096", "lm_head", "long_k", "moe", "rmsnorm", "tiny")
+    for r in measure_configs(dg, dev, peaks(), which):
+        print(json.dumps(r), flush=True)
 
 
 def main():
