@@ -342,6 +342,12 @@ void choose_tile_order(Problem &pb, int64_t rows, int64_t cols, int64_t kc, int 
     const int tiles = pb.rows_fast ? pb.m_tiles : n_tiles;
     const int fit = panel > 0 ? static_cast<int>(kResidentBytes / panel) : tiles;
     pb.group = std::max(1, std::min(tiles, fit));
+    const int slow = pb.rows_fast ? n_tiles : pb.m_tiles;
+    pb.span = pb.group * slow;
+    pb.div_span = make_fast_div(static_cast<unsigned>(pb.span));
+    pb.div_group = make_fast_div(static_cast<unsigned>(pb.group));
+    const int rem = tiles % pb.group;
+    pb.div_last = make_fast_div(static_cast<unsigned>(rem == 0 ? pb.group : rem));
 }
 
 // Contraction parts per tile. A launch with few output tiles (skinny M)
@@ -524,6 +530,8 @@ det_gemm_status run_problems(Variant v, bool a_kmajor, bool b_kmajor, const Prob
         rd_slots = base + slot_bytes + part_bytes;
     }
     p.parts = parts;
+    p.div_parts = make_fast_div(static_cast<unsigned>(parts));
+    p.div_stages = make_fast_div(static_cast<unsigned>((Lp + 1) / 2));
     p.part_ld = part_ld;
     p.part_stride = out_rows * part_ld;
     p.status = st->status_ptr;

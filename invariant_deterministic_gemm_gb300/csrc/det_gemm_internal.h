@@ -35,6 +35,29 @@ enum Variant {
     kVariantCount
 };
 
+// Division of a non-negative int below 2^31 by a fixed divisor d >= 1 as
+// one 64-bit multiply and a shift: q = (n * mul) >> shift with
+// shift = 32 + ceil(log2 d) and mul = ceil(2^shift / d) (at most 2^33). The
+// error term mul * d - 2^shift is below d <= 2^(shift - 32), so n * that
+// error stays below 2^shift for every n < 2^32 and the floor is exact
+// (Granlund and Montgomery, "Division by invariant integers using
+// multiplication", 1994). The kernels divide tile indices this way instead
+// of with the runtime's integer division, a long dependent chain.
+struct FastDiv {
+    unsigned long long mul;
+    unsigned int shift;
+};
+
+inline FastDiv make_fast_div(unsigned int d)
+{
+    unsigned int s = 0;
+    while ((1ull << s) < d) ++s;
+    FastDiv f;
+    f.shift = 32 + s;
+    f.mul = ((1ull << f.shift) + d - 1) / d;
+    return f;
+}
+
 // Everything a launch needs; passed by value as a __grid_constant__ param.
 // One GEMM of a launch. A plain launch has one; a grouped launch
 // (det_gemm_fwd_grouped) has one per group, all with the same columns and
@@ -50,6 +73,8 @@ struct Problem {
     int stage_tx;                 // bytes one K-stage's TMA copies bring in (A box + B box)
     int group;                    // tile order: tiles of this many row (or column) panels per group
     int rows_fast;                // 1: row tiles vary fastest (A panels stay in L2), 0: column tiles
+    int span;                     // tiles per group: group x the other operand's panel count
+    FastDiv div_span, div_group, div_last;   // by span, by group, by the last group's panel count
 };
 
 constexpr int kMaxProblems = 8;
@@ -65,6 +90,7 @@ struct Params {
     int n_tiles;
     int num_leaves;               // leaves per work unit (the whole contraction when parts == 1)
     int parts;                    // contraction parts per tile: subtrees of the merge tree (1, 2, 4, 8)
+    FastDiv div_parts, div_stages;    // by parts, by the K-stages per work unit
     void *part_out;               // parts > 1: part p of tile rows/cols goes to part_out + p * part_stride
     long long part_ld, part_stride;   // elements
     int force_timeout;

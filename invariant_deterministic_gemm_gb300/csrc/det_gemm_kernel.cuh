@@ -453,17 +453,21 @@ __device__ __forceinline__ uint32_t merge(uint32_t left, uint32_t right)
 // the CTAs running at the same time share the streamed operand's panel and
 // each streamed panel is read from DRAM once per group. The host picks the
 // order; only timing depends on it.
+__device__ __forceinline__ int fdiv(int n, const FastDiv &d)
+{
+    return static_cast<int>((static_cast<unsigned long long>(static_cast<unsigned int>(n)) * d.mul) >> d.shift);
+}
+
 __device__ __forceinline__ void tile_coords(int t, const Problem &pb, int n_tiles, int &mt, int &nt)
 {
     const int fast_tiles = pb.rows_fast ? pb.m_tiles : n_tiles;
-    const int slow_tiles = pb.rows_fast ? n_tiles : pb.m_tiles;
-    const int span = pb.group * slow_tiles;
-    const int g = t / span;
+    const int g = fdiv(t, pb.div_span);
     const int first = g * pb.group;
-    const int gf = min(pb.group, fast_tiles - first);
-    const int r = t - g * span;
-    const int f = first + r % gf;
-    const int o = r / gf;
+    const bool last = first + pb.group > fast_tiles;   // the last group may hold fewer panels
+    const int gf = last ? fast_tiles - first : pb.group;
+    const int r = t - g * pb.span;
+    const int o = fdiv(r, last ? pb.div_last : pb.div_group);
+    const int f = first + (r - o * gf);
     mt = pb.rows_fast ? f : o;
     nt = pb.rows_fast ? o : f;
 }
@@ -737,12 +741,12 @@ __device__ __forceinline__ void stage_role(const Params &p, const Smem<F32, SWAP
     }
     for (int g = j; ok && g < total; g += kStageWarps) {
         const uint32_t round = static_cast<uint32_t>(g / kStageWarps) & 1u;
-        const int tl = g / KS;                        // unit of this CTA
+        const int tl = fdiv(g, p.div_stages);         // unit of this CTA
         const int ks = g - tl * KS;
         const int u = blockIdx.x + tl * gridDim.x;
         const Problem &pb = p.prob[GROUPED ? problem_of(p, u) : 0];
         const int ul = u - pb.first_unit;
-        const int t = ul / p.parts;
+        const int t = fdiv(ul, p.div_parts);
         const int part = ul - t * p.parts;
         int mt, nt;
         tile_coords(t, pb, p.n_tiles, mt, nt);
@@ -775,12 +779,12 @@ __device__ __forceinline__ void stage_role(const Params &p, const Smem<F32, SWAP
                 // rounds from now is fetched into L2 already.
                 const int gp = g + kPrefetchRounds * kStageWarps;
                 if (gp < total) {
-                    const int tlp = gp / KS;
+                    const int tlp = fdiv(gp, p.div_stages);
                     const int ksp = gp - tlp * KS;
                     const int up = blockIdx.x + tlp * gridDim.x;
                     const Problem &pbp = p.prob[GROUPED ? problem_of(p, up) : 0];
                     const int ulp = up - pbp.first_unit;
-                    const int tp = ulp / p.parts;
+                    const int tp = fdiv(ulp, p.div_parts);
                     const int partp = ulp - tp * p.parts;
                     int mtp, ntp;
                     tile_coords(tp, pbp, p.n_tiles, mtp, ntp);
@@ -910,7 +914,7 @@ __device__ __forceinline__ void epilogue_role(const Params &p, const Smem<F32, S
     for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
         const Problem &pb = p.prob[GROUPED ? problem_of(p, u) : 0];
         const int ul = u - pb.first_unit;
-        const int t = ul / p.parts;
+        const int t = fdiv(ul, p.div_parts);
         const int part = ul - t * p.parts;
         int mt, nt;
         tile_coords(t, pb, p.n_tiles, mt, nt);
