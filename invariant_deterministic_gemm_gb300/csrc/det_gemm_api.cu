@@ -565,17 +565,20 @@ det_gemm_status run_problems(Variant v, bool a_kmajor, bool b_kmajor, const Prob
                                                   const_cast<void *>(pa[0].out.ptr), pa[0].out.ld, stream);
         if (me != cudaSuccess) return fail_cuda(DET_GEMM_ERR_LAUNCH, me, "merge launch");
     }
-    // Row reductions: after the product, from the stored output (each
-    // problem's slots follow the previous one's in the scratch).
+    // Row reductions: after the product, from the stored output, all
+    // groups of the launch together.
+    RowdotJob jobs[kMaxProblems];
+    int n_jobs = 0;
     for (int i = 0; i < g; ++i) {
         if (!pa[i].rowdot || pa[i].rows == 0) continue;
         const ProblemArgs &q = pa[i];
-        const cudaError_t re =
-            launch_rowdot(static_cast<const uint16_t *>(q.out.ptr), q.out.ld, static_cast<const uint16_t *>(q.d), q.ldd,
-                          static_cast<int>(q.rows), static_cast<int>(cols), reinterpret_cast<float *>(rd_slots),
-                          q.rowdot, stream);
+        jobs[n_jobs++] = RowdotJob{static_cast<const uint16_t *>(q.out.ptr), static_cast<const uint16_t *>(q.d),
+                                   q.out.ld, q.ldd, static_cast<int>(q.rows), q.rowdot};
+    }
+    if (n_jobs > 0) {
+        const cudaError_t re = launch_rowdot(jobs, n_jobs, static_cast<int>(cols), reinterpret_cast<float *>(rd_slots),
+                                             stream);
         if (re != cudaSuccess) return fail_cuda(DET_GEMM_ERR_LAUNCH, re, "row reduction launch");
-        rd_slots += align256(sizeof(float) * ((cols + kRowdotTile - 1) / kRowdotTile) * q.rows);
     }
     return DET_GEMM_OK;
 }

@@ -125,10 +125,18 @@ cudaError_t launch_merge_list(bool f32, const void *const *parts, int n, int row
 // Row reduction of a grouped launch: rowdot[i] = sum over n of C[i, n] *
 // D[i, n] in a fixed order (one slot per 128-column tile, the FP32 sum of
 // its products in ascending column order; slots merged by the mid-split
-// tree). `slots` is scratch for ceil(cols / 128) * rows floats.
+// tree), for n <= kMaxProblems groups with the same column count in one
+// pair of launches. `slots` is scratch for ceil(cols / 128) floats per row
+// of all groups together.
 constexpr int kRowdotTile = 128;
-cudaError_t launch_rowdot(const uint16_t *C, long long ldc, const uint16_t *D, long long ldd, int rows, int cols,
-                          float *slots, float *rowdot, cudaStream_t stream);
+struct RowdotJob {
+    const uint16_t *C;            // [rows, cols] BF16, row pitch ldc
+    const uint16_t *D;            // [rows, cols] BF16, row pitch ldd
+    long long ldc, ldd;
+    int rows;
+    float *rowdot;                // [rows] FP32
+};
+cudaError_t launch_rowdot(const RowdotJob *jobs, int n, int cols, float *slots, cudaStream_t stream);
 
 // Batch-invariant RMSNorm (det_rmsnorm): one warp per row.
 struct RmsParams {

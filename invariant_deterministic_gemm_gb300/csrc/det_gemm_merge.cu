@@ -84,29 +84,45 @@ cudaError_t launch_merge(bool f32, const PartPtrs &at, int parts, int rows, int 
 // slot, rowdot_reduce_kernel merges each row's slots by the mid-split tree
 // of FP32 adds the contraction uses, walked with its per-leaf schedule. The
 // same bits every run, whichever CTA computed which tile first.
+// Up to kMaxProblems row reductions (the groups of one grouped launch, all
+// with the same column count) in one pair of launches; the slots of all
+// groups are one array, group g's starting at slot_off[g].
 struct RowdotParams {
-    const float *part;
-    float *rowdot;
-    int rows, n_tiles;
+    const uint16_t *C[kMaxProblems];
+    const uint16_t *D[kMaxProblems];
+    float *rowdot[kMaxProblems];
+    long long ldc[kMaxProblems], ldd[kMaxProblems];
+    int row_start[kMaxProblems + 1];          // prefix sums of the groups' rows
+    float *slots;                             // [n_tiles][total rows]
+    int groups, cols, n_tiles;
     uint16_t sched[kMaxLeaves];
 };
 
-// One slot of the row reduction per thread: slot (t, i) = the FP32 sum of
-// C[i, n] * D[i, n] over the columns n of tile t in ascending order, from
-// +0. A product of two BF16 values is exact in FP32, so every step is one
-// rounding, as in a leaf. Rows are 16-byte aligned and tiles start on 256
-// bytes, so whole groups of eight columns are read with 16-byte loads.
-__global__ void rowdot_slots_kernel(const uint16_t *C, long long ldc, const uint16_t *D, long long ldd, int rows,
-                                    int cols, int n_tiles, float *slots)
+__device__ __forceinline__ int rowdot_group(const RowdotParams &p, int r)
 {
+    int g = 0;
+    while (g + 1 < p.groups && r >= p.row_start[g + 1]) ++g;
+    return g;
+}
+
+// One slot of the row reduction per thread: slot (t, row) = the FP32 sum
+// of C[i, n] * D[i, n] over the columns n of tile t in ascending order,
+// from +0. A product of two BF16 values is exact in FP32, so every step is
+// one rounding, as in a leaf. Rows are 16-byte aligned and tiles start on
+// 256 bytes, so whole groups of eight columns are read with 16-byte loads.
+__global__ void rowdot_slots_kernel(const __grid_constant__ RowdotParams p)
+{
+    const int total = p.row_start[p.groups];
     const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (idx >= static_cast<long long>(rows) * n_tiles) return;
-    const int i = static_cast<int>(idx / n_tiles);
-    const int t = static_cast<int>(idx - static_cast<long long>(i) * n_tiles);
+    if (idx >= static_cast<long long>(total) * p.n_tiles) return;
+    const int r = static_cast<int>(idx / p.n_tiles);
+    const int t = static_cast<int>(idx - static_cast<long long>(r) * p.n_tiles);
+    const int g = rowdot_group(p, r);
+    const int i = r - p.row_start[g];
     const int c0 = kRowdotTile * t;
-    const int c1 = min(c0 + kRowdotTile, cols);
-    const uint16_t *c = C + static_cast<long long>(i) * ldc;
-    const uint16_t *d = D + static_cast<long long>(i) * ldd;
+    const int c1 = min(c0 + kRowdotTile, p.cols);
+    const uint16_t *c = p.C[g] + static_cast<long long>(i) * p.ldc[g];
+    const uint16_t *d = p.D[g] + static_cast<long long>(i) * p.ldd[g];
     auto bf = [](uint32_t h) { return __uint_as_float(h << 16); };
     float s = 0.0f;
     int n = c0;
@@ -122,7 +138,7 @@ __global__ void rowdot_slots_kernel(const uint16_t *C, long long ldc, const uint
         }
     }
     for (; n < c1; ++n) s = __fadd_rn(s, __fmul_rn(bf(c[n]), bf(d[n])));
-    slots[static_cast<long long>(t) * rows + i] = s;
+    p.slots[static_cast<long long>(t) * total + r] = s;
 }
 
 // rowdot[i]: the slots of row i merged by the mid-split tree of FP32 adds,
@@ -130,12 +146,13 @@ __global__ void rowdot_slots_kernel(const uint16_t *C, long long ldc, const uint
 // leaves).
 __global__ void rowdot_reduce_kernel(const __grid_constant__ RowdotParams p)
 {
-    const int i = blockIdx.x * blockDim.x + threadIdx.x;
-    if (i >= p.rows) return;
+    const int total = p.row_start[p.groups];
+    const int r = blockIdx.x * blockDim.x + threadIdx.x;
+    if (r >= total) return;
     float slot[kMaxSlots];
     float root = 0.0f;
     for (int t = 0; t < p.n_tiles; ++t) {
-        float v = p.part[static_cast<long long>(t) * p.rows + i];
+        float v = p.slots[static_cast<long long>(t) * total + r];
         const uint32_t e = p.sched[t];
 #pragma unroll
         for (int s = 0; s < kMaxSlots; ++s)
@@ -146,7 +163,8 @@ __global__ void rowdot_reduce_kernel(const __grid_constant__ RowdotParams p)
             if (dst == static_cast<uint32_t>(s)) slot[s] = v;
         if (dst == kSlotRoot) root = v;
     }
-    p.rowdot[i] = root;
+    const int g = rowdot_group(p, r);
+    p.rowdot[g][r - p.row_start[g]] = root;
 }
 
 }  // namespace
@@ -169,25 +187,34 @@ cudaError_t launch_merge_list(bool f32, const void *const *parts, int n, int row
     return launch_merge(f32, at, n, rows, cols, ldp, out, ldo, stream);
 }
 
-cudaError_t launch_rowdot(const uint16_t *C, long long ldc, const uint16_t *D, long long ldd, int rows, int cols,
-                          float *slots, float *rowdot, cudaStream_t stream)
+cudaError_t launch_rowdot(const RowdotJob *jobs, int n, int cols, float *slots, cudaStream_t stream)
 {
-    if (rows <= 0) return cudaSuccess;
+    if (n < 1 || n > kMaxProblems) return cudaErrorInvalidValue;
     const int n_tiles = (cols + kRowdotTile - 1) / kRowdotTile;
     if (n_tiles < 1 || n_tiles > kMaxLeaves) return cudaErrorInvalidValue;
     RowdotParams p;
-    p.part = slots;
-    p.rowdot = rowdot;
-    p.rows = rows;
+    p.groups = n;
+    p.cols = cols;
     p.n_tiles = n_tiles;
+    p.slots = slots;
+    p.row_start[0] = 0;
+    for (int g = 0; g < n; ++g) {
+        p.C[g] = jobs[g].C;
+        p.D[g] = jobs[g].D;
+        p.ldc[g] = jobs[g].ldc;
+        p.ldd[g] = jobs[g].ldd;
+        p.rowdot[g] = jobs[g].rowdot;
+        p.row_start[g + 1] = p.row_start[g] + jobs[g].rows;
+    }
+    const int total = p.row_start[n];
+    if (total <= 0) return cudaSuccess;
     if (det_gemm_tree_schedule(n_tiles, p.sched) != DET_GEMM_OK) return cudaErrorInvalidValue;
     const int threads = 128;
-    const long long work = static_cast<long long>(rows) * n_tiles;
-    rowdot_slots_kernel<<<static_cast<unsigned>((work + threads - 1) / threads), threads, 0, stream>>>(
-        C, ldc, D, ldd, rows, cols, n_tiles, slots);
+    const long long work = static_cast<long long>(total) * n_tiles;
+    rowdot_slots_kernel<<<static_cast<unsigned>((work + threads - 1) / threads), threads, 0, stream>>>(p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    rowdot_reduce_kernel<<<(rows + threads - 1) / threads, threads, 0, stream>>>(p);
+    rowdot_reduce_kernel<<<(total + threads - 1) / threads, threads, 0, stream>>>(p);
     return cudaGetLastError();
 }
 
