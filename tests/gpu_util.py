@@ -44,8 +44,8 @@ def assert_bf16_close(got_bits, want_bits, node_max, num_leaves, what="", max_fr
         1 ulp(S), the benchmark spec's bound read against the tree's largest
         node; exceeding it needs a flipped leaf whose effect survives the
         later roundings. Measured over every comparison of the GPU suite:
-        5 of about 2.4 million elements, each at exactly 2 ulp(S), the most
-        in one comparison a fraction of 1.7e-5 (RATES records the rates of
+        8 of about 7.1 million elements, each at exactly 2 ulp(S), the most
+        in one comparison a fraction of 2.3e-5 (RATES records the rates of
         each run). The inputs are seeded and the kernel deterministic, so
         the same elements exceed it on every run; 1e-4 is the regression
         threshold.
