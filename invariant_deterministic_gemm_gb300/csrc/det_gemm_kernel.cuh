@@ -80,9 +80,10 @@ template <bool F32, bool SWAP = false>
 struct Cfg {
     // Epilogue warps and output columns per tile (rows when SWAP). The FP32
     // tile is 96 columns wide with four epilogue warps per scheduler, 24
-    // FP32 columns each: an MMA of 128 rows costs the tensor core the same
-    // time for any N up to 256, and 96 columns of FP32 values and pending
-    // partials still fit the registers, TMEM and shared memory.
+    // FP32 columns each: the thread that issues an MMA of 128 rows waits
+    // about as long for any N up to 256, so a wider tile does more per MMA
+    // issued, and 96 columns of FP32 values and pending partials still fit
+    // the registers, TMEM and shared memory.
     static constexpr int EPI_WARPS = SWAP ? 8 : 16;
     static constexpr int GROUPS = EPI_WARPS / 4;        // epilogue warps per TMEM lane quadrant
     static constexpr int BN = SWAP ? 64 : (F32 ? 96 : 128);
@@ -691,11 +692,14 @@ struct Smem {
 // stage's TMA copies into its slot, waits for them, then issues the stage's
 // MMAs (two K=16 MMAs per leaf into a fresh accumulator) and the commits that
 // hand the accumulators to the epilogue and the slot back for the stage
-// kStageWarps later. The tensor core takes about 180 cycles per K=16 MMA of
-// 128 rows whatever N is (up to 256), and a warp that issues an MMA while
-// it is busy waits until it is accepted. With the stages rotated over four
-// warps, one warp's waits for data, accumulators and acceptance overlap the
-// others' issue; on GB300 this ran faster than one issuing warp.
+// kStageWarps later. A thread that issues a tcgen05.mma waits for it to be
+// taken, about 180 cycles on GB300 whatever N is (up to 256), while the
+// tensor core finishes a 128 x 128 x 16 MMA in about 64. With the stages
+// rotated over four warps, one warp's waits for data and accumulators
+// overlap the others' issue; on GB300 this ran faster than one issuing warp,
+// and faster on the large launches than issuing different leaves' MMAs
+// from several warps at once (which overlaps the issue waits but slowed the
+// epilogue, the tighter bound).
 //
 // MMAs are still issued in leaf order: warp j issues stage g's MMAs only
 // after warp j-1 has issued stage g-1's (the turn barriers). The barrier
