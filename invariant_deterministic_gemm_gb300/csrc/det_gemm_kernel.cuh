@@ -49,8 +49,10 @@
 // tree's maximal subtrees of at most four leaves ("blocks", height <= 2)
 // entirely in registers, so only slots 2 and up ever hold a value: the
 // next slots are TMEM columns past the accumulators, then shared memory,
-// and the deepest (slots 7-9 for BF16, touched at most once per 256
-// leaves; 6-9 for FP32) a per-CTA global-memory scratch line per thread.
+// and the deepest (slots 7-9, touched at most once per 256 leaves) per-CTA
+// global scratch. Global scratch is laid out chunk-major within a warp: the
+// k-th 16 bytes of the 32 lanes' values are 512 contiguous bytes, so every
+// vector access of a warp covers whole cache lines.
 //
 // Every mbarrier wait is bounded (Params::timeout_ns of %globaltimer). On
 // expiry the waiter records DET_GEMM_ERR_TIMEOUT in the status word and sets
@@ -87,10 +89,15 @@ struct Cfg {
     static constexpr int EPI_WARPS = SWAP ? 8 : 16;
     static constexpr int GROUPS = EPI_WARPS / 4;        // epilogue warps per TMEM lane quadrant
     static constexpr int BN = SWAP ? 64 : (F32 ? 96 : 128);
-    // TMEM accumulator buffers. Three in the plain tiles leave TMEM room for
-    // two pending-partial slots; with four, the FP32 tile's fourth-highest
-    // slots went to global memory and long contractions slowed by a tenth.
-    static constexpr int NACC = SWAP ? 4 : 3;
+    // TMEM accumulator buffers. The BF16 tile takes three, which leaves
+    // TMEM room for two pending-partial slots (with two accumulators and four
+    // TMEM slots it ran 5 % slower: the MMAs then run only one leaf ahead).
+    // The FP32 tile takes two: its 96-column slots are 48 KiB each, and with
+    // three of them in TMEM a 448-leaf tree parks 12 instead of 24 values
+    // per tile in shared memory and 3 instead of 7 in global memory, which
+    // made that launch 4 % faster (with four accumulators it was a tenth
+    // slower).
+    static constexpr int NACC = SWAP ? 4 : (F32 ? 2 : 3);
     static constexpr int STAGES = kStageWarps;          // shared-memory ring depth: one slot per stage warp
     static constexpr int A_STAGE = kBM * kBK * 2;       // bytes of one A stage
     // MN-major B tiles are copied in boxes of 64 columns (one 128-byte
@@ -520,7 +527,7 @@ __device__ __forceinline__ void reg_fence_val(ValW<W> &t)
 struct EpiCtx {
     uint32_t tmem_slot;   // TMEM address of this thread's first TMEM slot
     uint32_t smem_slot;   // shared-memory address of this thread's line in the first shared slot
-    uint8_t *scratch;     // this thread's line in the first global slot
+    uint8_t *scratch;     // this thread's first 16 bytes in the first global slot (chunk k: +512 k)
     int lane;
     int row, col;         // first output element owned by this thread
     int rows;             // rows of the output (the problem's)
@@ -547,8 +554,8 @@ __device__ __forceinline__ uint32_t smem_chunk(uint32_t line, int lane, int k)
 
 // Writes this thread's value of the root to the output, clipped to the
 // matrix. A row the matrix clips goes element by element through the
-// thread's scratch line, which is free once the root is formed (every
-// pending partial has been merged into it).
+// thread's part of the first global slot, which is free once the root is
+// formed (every pending partial has been merged into it).
 //
 // Transposed tile (SWAP): the thread's TMEM lane is output column c.row and
 // its 32 values are output rows c.col .. c.col+31 of that column; each goes
@@ -576,9 +583,10 @@ __device__ __forceinline__ void store_out(const ValW<Cfg<F32, SWAP>::WORDS> &v, 
     const bool full = ncols >= C::COLS;
     uint8_t *dst = c.out + (static_cast<long long>(c.row) * c.ldo + c.col) * ES;
     uint8_t *vec = full ? dst : c.scratch;
+    const int vstride = full ? 16 : 512;
 #pragma unroll
     for (int k = 0; k < W / 4; ++k)
-        asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(vec + 16 * k), "r"(v[4 * k]),
+        asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(vec + vstride * k), "r"(v[4 * k]),
                      "r"(v[4 * k + 1]), "r"(v[4 * k + 2]), "r"(v[4 * k + 3])
                      : "memory");
     if (full) return;
@@ -586,11 +594,11 @@ __device__ __forceinline__ void store_out(const ValW<Cfg<F32, SWAP>::WORDS> &v, 
     for (int j = 0; j < ncols; ++j) {
         if constexpr (F32) {
             uint32_t w;
-            asm volatile("ld.global.b32 %0, [%1];" : "=r"(w) : "l"(c.scratch + 4 * j) : "memory");
+            asm volatile("ld.global.b32 %0, [%1];" : "=r"(w) : "l"(c.scratch + (j >> 2) * 512 + 4 * (j & 3)) : "memory");
             asm volatile("st.global.b32 [%0], %1;" ::"l"(dst + 4 * j), "r"(w) : "memory");
         } else {
             uint16_t w;
-            asm volatile("ld.global.u16 %0, [%1];" : "=h"(w) : "l"(c.scratch + 2 * j) : "memory");
+            asm volatile("ld.global.u16 %0, [%1];" : "=h"(w) : "l"(c.scratch + (j >> 3) * 512 + 2 * (j & 7)) : "memory");
             asm volatile("st.global.u16 [%0], %1;" ::"l"(dst + 2 * j), "h"(w) : "memory");
         }
     }
@@ -620,7 +628,7 @@ __device__ __forceinline__ void load_slot(int s, ValW<Cfg<F32, SWAP>::WORDS> &t,
         for (int k = 0; k < W / 4; ++k)
             asm volatile("ld.global.v4.b32 {%0, %1, %2, %3}, [%4];"
                          : "=r"(t[4 * k]), "=r"(t[4 * k + 1]), "=r"(t[4 * k + 2]), "=r"(t[4 * k + 3])
-                         : "l"(src + 16 * k)
+                         : "l"(src + 512 * k)
                          : "memory");
     }
 }
@@ -645,7 +653,7 @@ __device__ __forceinline__ void store_slot(int s, const ValW<Cfg<F32, SWAP>::WOR
         uint8_t *dst = c.scratch + (s - C::GLOBAL_FIRST) * C::SLOT_BYTES;
 #pragma unroll
         for (int k = 0; k < W / 4; ++k)
-            asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(dst + 16 * k), "r"(v[4 * k]),
+            asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(dst + 512 * k), "r"(v[4 * k]),
                          "r"(v[4 * k + 1]), "r"(v[4 * k + 2]), "r"(v[4 * k + 3])
                          : "memory");
     }
@@ -880,7 +888,7 @@ __device__ __forceinline__ void epilogue_role(const Params &p, const Smem<F32, S
     c.tmem_slot = S.tmem + lane_bits + static_cast<uint32_t>(C::TMEM_SLOT_BASE + cq * C::WORDS);
     c.smem_slot = S.sSlots + static_cast<uint32_t>((warp * 32 + lane) * C::LINE);
     c.scratch = static_cast<uint8_t *>(p.scratch) + static_cast<long long>(blockIdx.x) * C::SCRATCH_CTA_BYTES +
-                (warp * 32 + lane) * C::LINE;
+                warp * 32 * C::LINE + lane * 16;
     c.lane = lane;
     const int units = p.units;
     const int NB = p.num_blocks;
