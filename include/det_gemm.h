@@ -314,9 +314,10 @@ const char *det_gemm_last_error_detail(void);
 det_gemm_status det_gemm_tree_schedule(int64_t num_leaves, uint16_t *out);
 
 /*
- * Host-only helper, no GPU needed: the block schedule the kernels walk. The
- * tree is cut into its maximal subtrees of at most four leaves (for a tree
- * of more than four leaves these have 2, 3 or 4 leaves), in leaf order;
+ * Host-only helper, no GPU needed: the block schedule the plain-tile kernels
+ * walk. The tree is cut into its maximal subtrees of at most four leaves
+ * (for a tree of more than four leaves these have 2, 3 or 4 leaves), in
+ * leaf order;
  * out[b] describes block b: bits 10..11 hold (leaves in the block - 1);
  * bits 0..9 the pending-partial slots its value is merged with, lowest
  * first; bits 12..15 the slot its result is parked in, or 15 for the root
@@ -325,6 +326,23 @@ det_gemm_status det_gemm_tree_schedule(int64_t num_leaves, uint16_t *out);
  * *num_blocks receives the count.
  */
 det_gemm_status det_gemm_block_schedule(int64_t num_leaves, uint16_t *out, int64_t *num_blocks);
+
+/*
+ * Host-only helper, no GPU needed: the block schedule of the transposed
+ * tile (launches with at most 64 output rows). The tree is cut into its
+ * maximal subtrees of at most eight leaves (for a tree of more than eight
+ * leaves these have 4 to 8 leaves), in leaf order. Such a block's parent has
+ * more than eight leaves, so its merges and its parking slot are slot 3 or
+ * higher, and out[b] holds: bits 0..2 (leaves in the block - 1); bits 3..9
+ * the pending-partial slots its value is merged with, lowest first; bits
+ * 12..15 the slot its result is parked in, or 15 for the root (the last
+ * block, and only it). The kernel evaluates a block of n leaves as a left
+ * half of n/2 (rounded down) and a right half of the rest, each of one to
+ * four leaves shaped as in the mid-split tree. `out` needs num_leaves
+ * entries; *num_blocks receives the count. DET_GEMM_ERR_INVALID_ARG for a
+ * bad count or a NULL pointer.
+ */
+det_gemm_status det_gemm_block_schedule8(int64_t num_leaves, uint16_t *out, int64_t *num_blocks);
 
 /*
  * Frees the per-stream scratch buffers and forgets them; the next launch on

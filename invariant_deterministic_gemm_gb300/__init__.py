@@ -100,6 +100,8 @@ def lib() -> ctypes.CDLL:
         L.det_gemm_tree_schedule.restype = ctypes.c_int
         L.det_gemm_block_schedule.argtypes = [i64, p, p]
         L.det_gemm_block_schedule.restype = ctypes.c_int
+        L.det_gemm_block_schedule8.argtypes = [i64, p, p]
+        L.det_gemm_block_schedule8.restype = ctypes.c_int
         L.det_gemm_shutdown.argtypes = []
         L.det_gemm_shutdown.restype = ctypes.c_int
         L.det_gemm_debug_force_timeout.argtypes = [ctypes.c_int]
@@ -400,12 +402,22 @@ def det_gemm_tree_schedule(num_leaves: int) -> list[int]:
 
 
 def det_gemm_block_schedule(num_leaves: int) -> list[int]:
-    """Host-only: the block schedule the kernels walk (see det_gemm.h)."""
+    """Host-only: the block schedule the plain-tile kernels walk (see det_gemm.h)."""
     buf = (ctypes.c_uint16 * max(1, num_leaves))()
     nb = ctypes.c_int64(0)
     st = lib().det_gemm_block_schedule(int(num_leaves), buf, ctypes.byref(nb))
     if st != OK:
         raise DetGemmError(st, "det_gemm_block_schedule")
+    return list(buf)[:nb.value]
+
+
+def det_gemm_block_schedule8(num_leaves: int) -> list[int]:
+    """Host-only: the eight-leaf block schedule of the transposed tile (see det_gemm.h)."""
+    buf = (ctypes.c_uint16 * max(1, num_leaves))()
+    nb = ctypes.c_int64(0)
+    st = lib().det_gemm_block_schedule8(int(num_leaves), buf, ctypes.byref(nb))
+    if st != OK:
+        raise DetGemmError(st, "det_gemm_block_schedule8")
     return list(buf)[:nb.value]
 
 
@@ -422,7 +434,7 @@ def det_gemm_debug_force_timeout(enable: bool) -> None:
 __all__ = [
     "det_gemm_fwd", "det_gemm_fwd_noalloc", "det_gemm_fwd_rhs_transposed", "det_gemm_fwd_fp32",
     "det_gemm_fwd_fp32_rhs_transposed", "det_gemm_da", "det_gemm_db",
-    "det_gemm_db_transposed", "det_gemm_check", "det_gemm_tree_schedule", "det_gemm_block_schedule",
+    "det_gemm_db_transposed", "det_gemm_check", "det_gemm_tree_schedule", "det_gemm_block_schedule", "det_gemm_block_schedule8",
     "det_gemm_debug_force_timeout", "det_gemm_shutdown", "DetGemmError", "lib", "status_string",
     "det_gemm_merge",
     "det_gemm_merge_fp32",

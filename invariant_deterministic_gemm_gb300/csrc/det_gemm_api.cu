@@ -136,46 +136,54 @@ void build_schedule(int64_t L, uint16_t *out)
 // merged among themselves in registers; its entry says which pending
 // partials to merge its value with and where to park the result, which is
 // the per-leaf entry of its last leaf without the merges inside the block.
-void add_blocks(const uint16_t *leaf_sched, int64_t lo, int64_t hi, uint16_t *out, int64_t *nb)
+void add_blocks(const uint16_t *leaf_sched, int64_t lo, int64_t hi, int max_leaves, uint16_t *out, int64_t *nb)
 {
     const int64_t n = hi - lo;
-    if (n > 4) {
+    if (n > max_leaves) {
         const int64_t mid = (lo + hi) >> 1;
-        add_blocks(leaf_sched, lo, mid, out, nb);
-        add_blocks(leaf_sched, mid, hi, out, nb);
+        add_blocks(leaf_sched, lo, mid, max_leaves, out, nb);
+        add_blocks(leaf_sched, mid, hi, max_leaves, out, nb);
         return;
     }
     const uint32_t e = leaf_sched[hi - 1];
     const int h = ceil_log2(n);                  // the block's height
     const uint32_t up = (e & 0x3FFu) & ~((1u << h) - 1u);
-    out[(*nb)++] = static_cast<uint16_t>(up | (static_cast<uint32_t>(n - 1) << 10) | (e & 0xF000u));
+    if (max_leaves == 4) {
+        out[(*nb)++] = static_cast<uint16_t>(up | (static_cast<uint32_t>(n - 1) << 10) | (e & 0xF000u));
+    } else {
+        // Blocks of up to eight leaves: a block's parent has more than eight
+        // leaves (height 4 or more), so its merges and its store use slots 3
+        // and up, and bits 0..2 carry the leaf count.
+        out[(*nb)++] = static_cast<uint16_t>(up | static_cast<uint32_t>(n - 1) | (e & 0xF000u));
+    }
 }
 
-void build_blocks(int64_t L, uint16_t *out, int64_t *nb)
+void build_blocks(int64_t L, int max_leaves, uint16_t *out, int64_t *nb)
 {
     uint16_t leaf_sched[kMaxLeaves];
     build_schedule(L, leaf_sched);
     *nb = 0;
-    add_blocks(leaf_sched, 0, L, out, nb);
+    add_blocks(leaf_sched, 0, L, max_leaves, out, nb);
 }
 
 struct BlockSchedule {
     uint16_t *entries;
     int64_t count;
 };
-BlockSchedule g_block_cache[kMaxLeaves + 1] = {};
+BlockSchedule g_block_cache[2][kMaxLeaves + 1] = {};
 
-const BlockSchedule *blocks_for(int64_t L)
+const BlockSchedule *blocks_for(int64_t L, int max_leaves)
 {
     std::lock_guard<std::mutex> lk(g_mu);
-    if (!g_block_cache[L].entries) {
+    BlockSchedule &b = g_block_cache[max_leaves == 8][L];
+    if (!b.entries) {
         uint16_t *s = static_cast<uint16_t *>(std::malloc(sizeof(uint16_t) * L));
         if (!s) return nullptr;
         int64_t nb = 0;
-        build_blocks(L, s, &nb);
-        g_block_cache[L] = BlockSchedule{s, nb};
+        build_blocks(L, max_leaves, s, &nb);
+        b = BlockSchedule{s, nb};
     }
-    return &g_block_cache[L];
+    return &b;
 }
 
 // ---------------------------------------------------------- validation
@@ -455,7 +463,7 @@ det_gemm_status run_problems(Variant v, bool a_kmajor, bool b_kmajor, const Prob
     const int64_t Lp = L / parts;
     const BlockSchedule *blocks = nullptr;
     if (!fixed_scratch) {
-        blocks = blocks_for(Lp);
+        blocks = blocks_for(Lp, ops.block_leaves);
         if (!blocks) return DET_GEMM_ERR_LAUNCH;
     }
 
@@ -545,7 +553,7 @@ det_gemm_status run_problems(Variant v, bool a_kmajor, bool b_kmajor, const Prob
         std::memcpy(p.blocks, blocks->entries, sizeof(uint16_t) * blocks->count);
     } else {
         int64_t nb = 0;
-        build_blocks(Lp, p.blocks, &nb);
+        build_blocks(Lp, ops.block_leaves, p.blocks, &nb);
         p.num_blocks = static_cast<int>(nb);
     }
 
@@ -867,7 +875,15 @@ det_gemm_status det_gemm_block_schedule(int64_t num_leaves, uint16_t *out, int64
 {
     if (out == nullptr || num_blocks == nullptr || num_leaves < 1 || num_leaves > kMaxLeaves)
         return DET_GEMM_ERR_INVALID_ARG;
-    build_blocks(num_leaves, out, num_blocks);
+    build_blocks(num_leaves, 4, out, num_blocks);
+    return DET_GEMM_OK;
+}
+
+det_gemm_status det_gemm_block_schedule8(int64_t num_leaves, uint16_t *out, int64_t *num_blocks)
+{
+    if (out == nullptr || num_blocks == nullptr || num_leaves < 1 || num_leaves > kMaxLeaves)
+        return DET_GEMM_ERR_INVALID_ARG;
+    build_blocks(num_leaves, 8, out, num_blocks);
     return DET_GEMM_OK;
 }
 

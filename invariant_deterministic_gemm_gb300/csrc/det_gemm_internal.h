@@ -107,6 +107,7 @@ struct VariantOps {
     int scratch_cta_bytes;        // global scratch each CTA needs for its deep slots
     int split_regs;               // registers per thread the kernel must be built with (0: no register split)
     bool swap;                    // transposed tile: the kernel's rows are the output's columns
+    int block_leaves;             // leaves per block of the block schedule the kernel walks (4 or 8)
 };
 
 // Output rows up to which a BF16 launch uses the transposed tile.

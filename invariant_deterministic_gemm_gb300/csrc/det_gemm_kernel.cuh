@@ -110,7 +110,14 @@ struct Cfg {
     static constexpr int TMEM_COLS = 512;
     static constexpr int TMEM_SLOT_BASE = NACC * BN;    // after the accumulators
     static constexpr int TMEM_SLOT_STRIDE = WORDS * GROUPS;   // TMEM columns of one slot
-    static constexpr int TMEM_FIRST = 2;                // slots 0-1 never leave a block's registers
+    // Leaves per block of the block schedule. The transposed tile merges up
+    // to eight leaves in registers (the last leaf of a right half rounded
+    // straight into its sibling), so slots 0-2 never leave its registers:
+    // with half as many epilogue warps, its per-block overheads weigh more
+    // (QKV at one row: 36 -> 33.4 us). The plain tiles keep blocks of four
+    // leaves: eight measured 1 % slower on the large launches.
+    static constexpr int BLOCK_LEAVES = SWAP ? 8 : 4;
+    static constexpr int TMEM_FIRST = BLOCK_LEAVES == 8 ? 3 : 2;   // slots below never leave a block's registers
     static constexpr int TMEM_SLOTS_FIT = (TMEM_COLS - TMEM_SLOT_BASE) / TMEM_SLOT_STRIDE;
     static constexpr int TMEM_SLOTS =
         TMEM_SLOTS_FIT < kMaxSlots - TMEM_FIRST ? TMEM_SLOTS_FIT : kMaxSlots - TMEM_FIRST;
@@ -918,6 +925,25 @@ __device__ __forceinline__ void epilogue_role(const Params &p, const Smem<F32, S
         }
         if constexpr (!F32) round_leaf(stg, dst);
     };
+    // The same for a BF16 leaf that is the right child of dst (eight-leaf
+    // blocks): each rounded pair is added to dst as it is formed.
+    auto take_into = [&](ValW<W> &dst) {
+        if (!warp_wait(S.accf(acc), acc_phase, S.abort_flag, p.status, p.timeout_ns)) {
+            ok = false;
+            return;
+        }
+        tc_fence_after();
+        stage_load<32>(acc0 + static_cast<uint32_t>(acc * C::BN), stg);
+        tc_fence_before();
+        __syncwarp();
+        mbar_arrive_if(S.acce(acc), lane == 0);
+        if (++acc == C::NACC) {
+            acc = 0;
+            acc_phase ^= 1u;
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) dst[i] = merge<false>(dst[i], cvt_bf16x2(stg[2 * i], stg[2 * i + 1]));
+    };
     auto add = [](ValW<W> &left, const ValW<W> &right) {
 #pragma unroll
         for (int i = 0; i < W; ++i) left[i] = merge<F32>(left[i], right[i]);
@@ -942,21 +968,56 @@ __device__ __forceinline__ void epilogue_role(const Params &p, const Smem<F32, S
         }
         for (int b = 0; b < NB; ++b) {
             const uint32_t e = p.blocks[b];
-            const int n = static_cast<int>((e >> 10) & 3u) + 1;   // leaves in the block
-            // n = 1: A = l0          n = 2: A = l0 + l1
-            // n = 3: A = l0 + (l1 + l2)     n = 4: A = (l0 + l1) + (l2 + l3)
-            take(A);
-            if (n >= 2) take(B);
-            if (n == 4) {
-                add(A, B);
-                take(B);
+            if constexpr (C::BLOCK_LEAVES == 4) {
+                const int n = static_cast<int>((e >> 10) & 3u) + 1;   // leaves in the block
+                // n = 1: A = l0          n = 2: A = l0 + l1
+                // n = 3: A = l0 + (l1 + l2)     n = 4: A = (l0 + l1) + (l2 + l3)
+                take(A);
+                if (n >= 2) take(B);
+                if (n == 4) {
+                    add(A, B);
+                    take(B);
+                }
+                if (n >= 3) {
+                    take(Cc);
+                    add(B, Cc);
+                }
+                if (!ok) return;
+                if (n >= 2) add(A, B);
+            } else {
+                // n leaves = a left half of n/2 (rounded down) and a right
+                // half of the rest, each of the four-leaf shapes:
+                // 1: x0   2: x0 + x1   3: x0 + (x1 + x2)   4: (x0 + x1) + (x2 + x3)
+                const int n = static_cast<int>(e & 7u) + 1;
+                const int nl = n >> 1, nr = n - nl;
+                if (nl > 0) {                    // left half -> A
+                    take(A);
+                    if (nl >= 2) take(B);
+                    if (nl == 4) {
+                        add(A, B);
+                        take(B);
+                    }
+                    if (nl >= 3) {
+                        take(Cc);
+                        add(B, Cc);
+                    }
+                    if (nl >= 2) add(A, B);
+                }
+                take(B);                         // right half -> B
+                if (nr >= 2) take(Cc);
+                if (nr == 4) {
+                    add(B, Cc);
+                    take(Cc);
+                }
+                if (nr >= 3) take_into(Cc);
+                if (nr >= 2) add(B, Cc);
+                if (!ok) return;
+                if (nl > 0) add(A, B);
+                else {
+#pragma unroll
+                    for (int i = 0; i < W; ++i) A[i] = B[i];
+                }
             }
-            if (n >= 3) {
-                take(Cc);
-                add(B, Cc);
-            }
-            if (!ok) return;
-            if (n >= 2) add(A, B);
             // merge with the pending left siblings above the block, lowest first
 #pragma unroll 1
             for (uint32_t m = (e & 0x3FFu) >> C::TMEM_FIRST; m != 0; m &= m - 1) {
@@ -1100,6 +1161,7 @@ struct Launcher {
         o.scratch_cta_bytes = C::SCRATCH_CTA_BYTES;
         o.split_regs = C::LAUNCH_REGS;
         o.swap = SWAP;
+        o.block_leaves = C::BLOCK_LEAVES;
         return o;
     }
 };

@@ -199,6 +199,72 @@ def test_block_schedule_replays_the_mid_split_tree_for_every_leaf_count(dg):
         assert stores[-1] == 15 and stores.count(15) == 1, L
 
 
+def four_leaf_shape(x):
+    """A block half as the kernel merges it: x0, x0 + x1, x0 + (x1 + x2) or
+    (x0 + x1) + (x2 + x3)."""
+    if len(x) == 1:
+        return x[0]
+    if len(x) == 2:
+        return (x[0], x[1])
+    if len(x) == 3:
+        return (x[0], (x[1], x[2]))
+    assert len(x) == 4
+    return ((x[0], x[1]), (x[2], x[3]))
+
+
+def replay_blocks8(blocks, L):
+    """Run the eight-leaf block schedule on symbolic leaves the way the
+    transposed tile does: a block of n leaves is a left half of n // 2
+    leaves and a right half of the rest."""
+    slots = {}
+    root = None
+    nxt = 0
+    for e in blocks:
+        n = (e & 7) + 1
+        mask, store = e & 0x3F8, e >> 12
+        x = list(range(nxt, nxt + n))
+        nxt += n
+        nl = n // 2
+        v = x[0] if n == 1 else (four_leaf_shape(x[:nl]), four_leaf_shape(x[nl:]))
+        for s in range(10):
+            if mask >> s & 1:
+                assert s in slots, ("read of an empty slot", s)
+                v = (slots.pop(s), v)
+        if store == 15:
+            assert root is None
+            root = v
+        else:
+            assert 3 <= store < 10 and store not in slots
+            slots[store] = v
+    assert nxt == L and not slots
+    return root
+
+
+def test_eight_leaf_block_schedule_replays_the_mid_split_tree_for_every_leaf_count(dg):
+    for L in range(1, 1025):
+        blocks = dg.det_gemm_block_schedule8(L)
+        sizes = [(e & 7) + 1 for e in blocks]
+        if L > 8:
+            assert set(sizes) <= {4, 5, 6, 7, 8}, L
+        assert replay_blocks8(blocks, L) == mid_split_tree(0, L), L
+        # the transposed tile stores the root after the walk too
+        stores = [e >> 12 for e in blocks]
+        assert stores[-1] == 15 and stores.count(15) == 1, L
+        # bits 10..11 are unused in this format
+        assert all(e & 0xC00 == 0 for e in blocks), L
+
+
+def test_block_schedules_reject_bad_counts(dg):
+    L = dg.lib()
+    buf = (ctypes.c_uint16 * 2)()
+    nb = ctypes.c_int64(0)
+    for fn in (L.det_gemm_block_schedule, L.det_gemm_block_schedule8):
+        assert fn(0, buf, ctypes.byref(nb)) == 1
+        assert fn(1025, buf, ctypes.byref(nb)) == 1
+        assert fn(4, None, ctypes.byref(nb)) == 1
+        assert fn(4, buf, None) == 1
+
+
 # ---------------------------------------------------------------- merge API
 
 def merge_call(dg, name, parts, n, out, M, N, ldp, ldc):
