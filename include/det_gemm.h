@@ -50,7 +50,7 @@
  *     det_gemm_check(), not by the launching call.
  *   - The library allocates no device memory per call. It keeps one small
  *     device scratch buffer per (device, stream) it has launched on (one CTA
- *     per SM x 192 KiB: the tree's most rarely touched pending partials), created
+ *     per SM x 144 KiB: the tree's most rarely touched pending partials), created
  *     on the first launch on that stream and reused by every later one, so
  *     launches on different streams never share it. det_gemm_shutdown()
  *     releases them.

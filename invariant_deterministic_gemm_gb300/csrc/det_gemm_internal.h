@@ -151,9 +151,9 @@ struct RmsParams {
 constexpr int kRmsWarps = 8;      // rows per CTA
 cudaError_t launch_rmsnorm(const RmsParams &p, cudaStream_t stream);
 
-// Largest scratch_cta_bytes over all variants (fp32: 4 slots x 48 KiB;
-// bf16: 3 slots x 32 KiB).
-constexpr int kMaxScratchCtaBytes = 4 * 49152;
+// Largest scratch_cta_bytes over all variants (slots 7-9 in global
+// scratch: fp32 3 x 48 KiB, bf16 3 x 32 KiB).
+constexpr int kMaxScratchCtaBytes = 3 * 49152;
 
 VariantOps ops_bf16_kmn();
 VariantOps ops_bf16_kk();

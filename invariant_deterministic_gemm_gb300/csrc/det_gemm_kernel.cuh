@@ -44,13 +44,14 @@
 // root after the last leaf.
 //
 // Pending partials ("slots"): slot s holds the finished left child of a tree
-// node of height s + 1, so at most ceil(log2 L) <= 10 are live, and slot s
-// is written at most once per 2^(s+1) leaves. The epilogue evaluates the
-// tree's maximal subtrees of at most four leaves ("blocks", height <= 2)
-// entirely in registers, so only slots 2 and up ever hold a value: the
-// next slots are TMEM columns past the accumulators, then shared memory,
-// and the deepest (slots 7-9, touched at most once per 256 leaves) per-CTA
-// global scratch. Global scratch is laid out chunk-major within a warp: the
+// node of height s + 1, so at most ceil(log2 L) <= 10 are live. Such a node
+// spans more than 2^s leaves and nodes of one height are disjoint, so slot s
+// is written at most once per 2^s + 1 leaves. The epilogue evaluates the
+// tree's maximal subtrees of at most four leaves ("blocks", height <= 2;
+// eight leaves and height <= 3 in the transposed tile) entirely in
+// registers, so only slots 2 and up ever hold a value: the next slots are
+// TMEM columns past the accumulators, then shared memory, and the deepest
+// (slots 7-9, touched at most once per 129 leaves) per-CTA global scratch. Global scratch is laid out chunk-major within a warp: the
 // k-th 16 bytes of the 32 lanes' values are 512 contiguous bytes, so every
 // vector access of a warp covers whole cache lines.
 //
