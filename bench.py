@@ -500,7 +500,8 @@ def cpu_sample(problems, rows, threads):
 
 
 def cpu_baseline(max_seconds=15.0):
-    """The oracle on a bounded row sample of one step, on all host cores."""
+    """The oracle on a bounded row sample of one step, on all host cores,
+    and on one core (the first row of each product)."""
     import oracle
     oracle.build()
     threads = oracle.default_threads()
@@ -509,9 +510,13 @@ def cpu_baseline(max_seconds=15.0):
     reps = max(1, min(64, int(max_seconds / max(t1, 1e-3))))
     rows = threads * reps
     flops, dt = cpu_sample(problems, rows, threads)
+    f_one, t_one = cpu_sample(problems, 1, 1)
     return {"value": round(flops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
             "sample": "first %d rows of each of the six products of one step (%.3g GFLOP in %.1f s)" % (
-                rows, flops / 1e9, dt)}
+                rows, flops / 1e9, dt),
+            "one_core": {"value": round(f_one / t_one / 1e12, 6), "unit": "TFLOP/s",
+                         "sample": "first row of each of the six products (%.3g GFLOP in %.1f s)" % (
+                             f_one / 1e9, t_one)}}
 
 
 def reference_arm(args):
