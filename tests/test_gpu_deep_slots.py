@@ -17,7 +17,10 @@ bit for bit, while the leaf roundings and the tree's BF16 adds still round
 (leaf sums reach 288, beyond BF16's 8 significant bits). The operands are a
 gigabyte or more, so they are drawn on the device from a seeded generator
 and the oracle checks sampled rows and columns: the first and last, both
-sides of the first tile edge, and random ones across every tile."""
+sides of the first tile edge, and random ones across every tile. Every
+kernel instance of the plain tiles is covered: the BF16 forward (and the
+allocation-free forward), dA, dB and dB stored [N, K], both FP32-output
+instances and the grouped launch."""
 import numpy as np
 import pytest
 import torch
@@ -106,3 +109,30 @@ def test_db_and_db_transposed(Kc):
     check()
     want_t = oracle.db_transposed(_host_bits(A2[:, r]), _host_bits(dC2[:, c]))
     assert exact_equal(_host_bits(dBt[c][:, r]), want_t), Kc
+
+
+@pytest.mark.parametrize("Kc", KCS)
+def test_fp32_rhs_transposed(Kc):
+    # the FP32-output instance with a K-major weight stored [N, K]
+    M, N = 128, 96 * _sms()
+    A = W.randint_bf16_cuda((M, Kc), -3, 3, 13000 + Kc)
+    Wt = W.randint_bf16_cuda((N, Kc), -3, 3, 13100 + Kc)
+    C = dg.det_gemm_fwd_fp32_rhs_transposed(A, Wt)
+    check()
+    r, c = _sample(M, 6, Kc), _sample(N, 60, Kc + 5)
+    want = oracle.fwd_fp32_rhs_transposed(_host_bits(A[r]), _host_bits(Wt[c]))
+    assert np.array_equal(C[r][:, c].cpu().numpy(), want), Kc
+
+
+@pytest.mark.parametrize("Kc", [4160, 14336])
+def test_grouped(Kc):
+    # two groups of one row tile each, N wide enough for one tile per SM in all
+    N = 64 * _sms()
+    As = [W.randint_bf16_cuda((128, Kc), -3, 3, 13200 + Kc + g) for g in range(2)]
+    Bs = [W.randint_bf16_cuda((Kc, N), -3, 3, 13300 + Kc + g) for g in range(2)]
+    Cs = dg.det_gemm_fwd_grouped(As, Bs)
+    check()
+    for g in range(2):
+        r, c = _sample(128, 6, Kc + g), _sample(N, 40, Kc + 6 + g)
+        want = oracle.fwd(_host_bits(As[g][r]), _host_bits(Bs[g][:, c]))
+        assert exact_equal(_host_bits(Cs[g][r][:, c]), want), (Kc, g)
