@@ -30,9 +30,11 @@
 // MMA's A operand is the weight, so its 128 TMEM lanes are 128 output
 // columns, and its N side (64) holds the rows. 384 threads: warps 0-7
 // epilogue, two per scheduler, each owning one output column per lane and
-// 32 rows; warps 8-11 stage warps. The accumulators and all eight pending
-// slots fit in TMEM, and the stage warps also prefetch the weight tiles of
-// later stages into L2.
+// 32 rows (a warp whose 32 rows are all past the output's only hands the
+// accumulators back); warp 8 copies every stage in with TMA and prefetches
+// the weight tiles of later stages into L2, and warps 9-11 issue the MMAs,
+// each into its own accumulator and without a turn order. The accumulators
+// and all seven pending slots fit in TMEM.
 //
 // Per tile: 64-wide K stages (two leaves) of the A and B operand tiles go
 // through a ring of four swizzled shared-memory slots. For leaf l the stage
@@ -93,12 +95,13 @@ struct Cfg {
     // TMEM accumulator buffers. The BF16 tile takes three, which leaves
     // TMEM room for two pending-partial slots (with two accumulators and four
     // TMEM slots it ran 5 % slower: the MMAs then run only one leaf ahead).
+    // The transposed tile takes three too, one per issuing warp.
     // The FP32 tile takes two: its 96-column slots are 48 KiB each, and with
     // three of them in TMEM a 448-leaf tree parks 12 instead of 24 values
     // per tile in shared memory and 3 instead of 7 in global memory, which
     // made that launch 4 % faster (with four accumulators it was a tenth
     // slower).
-    static constexpr int NACC = SWAP ? 4 : (F32 ? 2 : 3);
+    static constexpr int NACC = 3 - (F32 ? 1 : 0);
     static constexpr int STAGES = kStageWarps;          // shared-memory ring depth: one slot per stage warp
     static constexpr int A_STAGE = kBM * kBK * 2;       // bytes of one A stage
     // MN-major B tiles are copied in boxes of 64 columns (one 128-byte
@@ -715,7 +718,9 @@ struct Smem {
 // overlap the others' issue; on GB300 this ran faster than one issuing warp,
 // and faster on the large launches than issuing different leaves' MMAs
 // from several warps at once (which overlaps the issue waits but slowed the
-// epilogue, the tighter bound).
+// epilogue, the tighter bound). The transposed tile, whose epilogue has half
+// the work per leaf, issues that way (copy_role and issue_role below): QKV
+// at 17 rows 37.5 -> 35.5 us.
 //
 // MMAs are still issued in leaf order: warp j issues stage g's MMAs only
 // after warp j-1 has issued stage g-1's (the turn barriers). The barrier
@@ -874,6 +879,151 @@ __device__ __forceinline__ void stage_role(const Params &p, const Smem<F32, SWAP
     }
 }
 
+// Transposed tile: one copy warp and kSwapIssuers issuing warps. The copy
+// warp fills the shared-memory ring stage by stage; issuer i issues the
+// MMAs of the leaves G with G % kSwapIssuers == i into its own accumulator
+// i, so the issuers' waits for MMA acceptance overlap instead of following
+// a turn order. A stage's slot is released by both of its leaves' issuers
+// (the empty barrier counts two commits; a stage with a single leaf commits
+// twice). Only one thread waits on each accumulator-free barrier (its
+// issuer) and the copy warp alone waits on the empty barriers, so no waiter
+// can miss a phase.
+constexpr int kSwapIssuers = 3;
+
+template <int A_MAJOR, int B_MAJOR, bool F32, bool GROUPED, bool SWAP>
+__device__ __forceinline__ void copy_role(const Params &p, const Smem<F32, SWAP> &S)
+{
+    using C = Cfg<F32, SWAP>;
+    const bool leader = elect_one();
+    const int units = p.units;
+    const int L = p.num_leaves;
+    const int KS = (L + 1) / 2;
+    const int my_units = blockIdx.x < units ? (units - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+    const int total = my_units * KS;
+    uint32_t loaded = 0, parity = 0;
+    bool ok = true;
+    if (p.force_timeout)
+        ok = __all_sync(0xFFFFFFFFu, wait_bounded(S.never(), 0, S.abort_flag, p.status, p.timeout_ns, true));
+    for (int g = 0; ok && g < total; ++g) {
+        const int s = g % C::STAGES;
+        const uint32_t round = static_cast<uint32_t>(g / C::STAGES) & 1u;
+        const int tl = fdiv(g, p.div_stages);
+        const int ks = g - tl * KS;
+        const int u = blockIdx.x + tl * gridDim.x;
+        const Problem &pb = p.prob[GROUPED ? problem_of(p, u) : 0];
+        const int ul = u - pb.first_unit;
+        const int t = fdiv(ul, p.div_parts);
+        const int part = ul - t * p.parts;
+        int mt, nt;
+        tile_coords(t, pb, p.n_tiles, mt, nt);
+        if (!warp_wait(S.empty(s), round ^ 1u, S.abort_flag, p.status, p.timeout_ns)) { ok = false; break; }
+        const uint32_t full = S.full(s);
+        const uint32_t a_dst = S.sA + s * C::A_STAGE;
+        const uint32_t b_dst = S.sB + s * C::B_STAGE;
+        if (leader) {
+            mbar_arrive_expect_tx(full, static_cast<uint32_t>(pb.stage_tx));
+            const int k0 = part * L * kLeaf + ks * kBK, m0 = mt * kBM, n0 = nt * C::BN;
+            if constexpr (A_MAJOR == kKMajor) {
+                tma_load_2d(a_dst, &pb.tmap_a, full, k0, m0);
+            } else {
+                tma_load_2d(a_dst, &pb.tmap_a, full, m0, k0);
+                tma_load_2d(a_dst + 8192, &pb.tmap_a, full, m0 + 64, k0);
+            }
+            if constexpr (B_MAJOR == kKMajor) {
+                tma_load_2d(b_dst, &pb.tmap_b, full, k0, n0);
+            } else {
+#pragma unroll
+                for (int b = 0; b < C::B_COPY_COLS / 64; ++b)
+                    tma_load_2d(b_dst + 8192 * b, &pb.tmap_b, full, n0 + 64 * b, k0);
+            }
+            if constexpr (SWAP) {
+                const int gp = g + kPrefetchRounds * C::STAGES;
+                if (gp < total) {
+                    const int tlp = fdiv(gp, p.div_stages);
+                    const int ksp = gp - tlp * KS;
+                    const int up = blockIdx.x + tlp * gridDim.x;
+                    const Problem &pbp = p.prob[GROUPED ? problem_of(p, up) : 0];
+                    const int ulp = up - pbp.first_unit;
+                    const int tp = fdiv(ulp, p.div_parts);
+                    const int partp = ulp - tp * p.parts;
+                    int mtp, ntp;
+                    tile_coords(tp, pbp, p.n_tiles, mtp, ntp);
+                    const int kp = partp * L * kLeaf + ksp * kBK, mp = mtp * kBM;
+                    if constexpr (A_MAJOR == kKMajor) {
+                        tma_prefetch_2d(&pbp.tmap_a, kp, mp);
+                    } else {
+                        tma_prefetch_2d(&pbp.tmap_a, mp, kp);
+                        if (mp + 64 < pbp.rows) tma_prefetch_2d(&pbp.tmap_a, mp + 64, kp);
+                    }
+                }
+            }
+        }
+        __syncwarp();
+        loaded |= 1u << s;
+        parity = (parity & ~(1u << s)) | (round << s);
+    }
+    if (!ok) {
+        for (int s = 0; s < C::STAGES; ++s)
+            if (loaded & (1u << s))
+                wait_bounded(S.full(s), (parity >> s) & 1u, S.abort_flag, p.status, p.timeout_ns, false);
+    }
+}
+
+template <int A_MAJOR, int B_MAJOR, bool F32, bool GROUPED, bool SWAP>
+__device__ __forceinline__ void issue_role(const Params &p, const Smem<F32, SWAP> &S, int i)
+{
+    using C = Cfg<F32, SWAP>;
+    static_assert(C::NACC == kSwapIssuers, "one accumulator per issuer");
+    constexpr uint32_t IDESC = idesc_bf16(kBM, C::BN, A_MAJOR, B_MAJOR);
+    constexpr uint32_t A_KSTEP = ((A_MAJOR == kKMajor) ? 32u : 2048u) >> 4;
+    constexpr uint32_t B_KSTEP = ((B_MAJOR == kKMajor) ? 32u : 2048u) >> 4;
+    constexpr uint32_t A_LBO = (A_MAJOR == kKMajor) ? 16u : 8192u;
+    constexpr uint32_t B_LBO = (B_MAJOR == kKMajor) ? 16u : 8192u;
+    const bool leader = elect_one();
+    const uint64_t a_st0 = sdesc(S.sA, A_LBO, 1024u);
+    const uint64_t b_st0 = sdesc(S.sB, B_LBO, 1024u);
+    const uint32_t d = S.tmem + static_cast<uint32_t>(i * C::BN);
+    const uint32_t accf = S.accf(i), acce = S.acce(i);
+    const int units = p.units;
+    const int L = p.num_leaves;
+    const int KS = (L + 1) / 2;
+    const int my_units = blockIdx.x < units ? (units - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+    const int total = my_units * L;
+    uint32_t use = 0;
+    bool mma_issued = false, ok = true;
+    int tl = i / L, l = i - tl * L;       // position of leaf G = i; advanced by kSwapIssuers
+    for (int G = i; G < total; G += kSwapIssuers, ++use) {
+        const int g = tl * KS + (l >> 1);
+        const int half = l & 1;
+        const bool alone = (l + 1 == L) && half == 0;
+        const int s = g % C::STAGES;
+        if (!warp_wait(acce, (use & 1u) ^ 1u, S.abort_flag, p.status, p.timeout_ns) ||
+            !warp_wait(S.full(s), static_cast<uint32_t>(g / C::STAGES) & 1u, S.abort_flag, p.status, p.timeout_ns)) {
+            ok = false;
+            break;
+        }
+        tc_fence_after();
+        if (leader) {
+            const uint64_t a = a_st0 + static_cast<uint64_t>(s * (C::A_STAGE >> 4)) + (2 * half) * A_KSTEP;
+            const uint64_t b = b_st0 + static_cast<uint64_t>(s * (C::B_STAGE >> 4)) + (2 * half) * B_KSTEP;
+            mma_bf16(d, a, b, IDESC, 0u);
+            mma_bf16(d, a + A_KSTEP, b + B_KSTEP, IDESC, 1u);
+            mma_commit(accf);
+            mma_commit(S.empty(s));
+            if (alone) mma_commit(S.empty(s));
+        }
+        __syncwarp();
+        mma_issued = true;
+        l += kSwapIssuers;
+        while (l >= L) { l -= L; ++tl; }
+    }
+    if (!ok && mma_issued) {
+        if (leader) mma_commit(S.drain(i));
+        __syncwarp();
+        wait_bounded(S.drain(i), 0, S.abort_flag, p.status, p.timeout_ns, false);
+    }
+}
+
 // Epilogue warp: leaf rounding and the merge tree for one row and BN/2
 // columns of every tile.
 //
@@ -926,6 +1076,19 @@ __device__ __forceinline__ void epilogue_role(const Params &p, const Smem<F32, S
         }
         if constexpr (!F32) round_leaf(stg, dst);
     };
+    // Waits for the next leaf's accumulator and hands it straight back.
+    auto pass = [&]() {
+        if (!warp_wait(S.accf(acc), acc_phase, S.abort_flag, p.status, p.timeout_ns)) {
+            ok = false;
+            return;
+        }
+        __syncwarp();
+        mbar_arrive_if(S.acce(acc), lane == 0);
+        if (++acc == C::NACC) {
+            acc = 0;
+            acc_phase ^= 1u;
+        }
+    };
     // The same for a BF16 leaf that is the right child of dst (eight-leaf
     // blocks): each rounded pair is added to dst as it is formed.
     auto take_into = [&](ValW<W> &dst) {
@@ -966,6 +1129,17 @@ __device__ __forceinline__ void epilogue_role(const Params &p, const Smem<F32, S
         } else {
             c.out = static_cast<uint8_t *>(pb.out);
             c.ldo = pb.ldo;
+        }
+        if constexpr (SWAP) {
+            if (c.col >= p.cols) {
+                // The warp's 32 kernel columns are all past the output's
+                // rows (a launch of at most 32 rows): it has nothing to
+                // round, merge or store and only hands each accumulator
+                // back once the MMA has filled it.
+                for (int i = 0; ok && i < p.num_leaves; ++i) pass();
+                if (!ok) return;
+                continue;
+            }
         }
         for (int b = 0; b < NB; ++b) {
             const uint32_t e = p.blocks[b];
@@ -1068,7 +1242,7 @@ __global__ void __launch_bounds__(Cfg<F32, SWAP>::THREADS, 1) det_gemm_kernel(co
         *S.abort_flag = 0;
         for (int s = 0; s < C::STAGES; ++s) {
             mbar_init(S.full(s), 1);
-            mbar_init(S.empty(s), 1);
+            mbar_init(S.empty(s), SWAP ? 2 : 1);
         }
         for (int b = 0; b < C::NACC; ++b) {
             mbar_init(S.accf(b), 1);
@@ -1117,7 +1291,8 @@ __global__ void __launch_bounds__(Cfg<F32, SWAP>::THREADS, 1) det_gemm_kernel(co
     } else {
         // 384 threads: every warp has the registers it needs without a split.
         if (warp < C::EPI_WARPS) epilogue_role<F32, GROUPED, SWAP>(p, S, warp, lane);
-        else stage_role<A_MAJOR, B_MAJOR, F32, GROUPED, SWAP>(p, S, warp - C::FIRST_STAGE_WARP);
+        else if (warp == C::FIRST_STAGE_WARP) copy_role<A_MAJOR, B_MAJOR, F32, GROUPED, SWAP>(p, S);
+        else issue_role<A_MAJOR, B_MAJOR, F32, GROUPED, SWAP>(p, S, warp - C::FIRST_STAGE_WARP - 1);
     }
 
     // ---- teardown
