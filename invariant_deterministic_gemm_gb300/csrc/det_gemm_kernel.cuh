@@ -63,11 +63,14 @@
 // loads and MMAs are drained with bounded waits, TMEM is released and the
 // CTA exits. The epilogue's per-leaf wait keeps its retry loop inside one
 // inline PTX block and records a failure as data: the warp still loads and
-// hands back that leaf's accumulator (values of an aborted launch are never
-// used; the accesses stay inside the CTA's TMEM and barriers) and leaves at
-// the end of the block. Without a branch after every wait the compiler
-// schedules one leaf's arithmetic across the next leaf's wait (the MLP step
-// 627 -> 637 TFLOP/s, the FP32-output launch 437 -> 461).
+// hands back that leaf's accumulator and finishes the tile's blocks on
+// whatever the accumulators hold (the values of an aborted launch are never
+// used; the accesses stay inside the CTA's TMEM, shared memory and scratch,
+// and the FP32 tile's in-place root store inside the output), then leaves
+// at the tile's end. Without a branch after every wait, or after every
+// block, the compiler schedules one leaf's arithmetic across the next
+// leaf's wait (the MLP step 627 -> 645 TFLOP/s, the FP32-output launch
+// 437 -> 471).
 #pragma once
 
 #include "det_gemm_internal.h"
@@ -1198,7 +1201,6 @@ __device__ __forceinline__ void epilogue_role(const Params &p, const Smem<F32, S
                     take(Cc);
                     add(B, Cc);
                 }
-                if (!ok) return;
                 if (n >= 2) add(A, B);
             } else {
                 // n leaves = a left half of n/2 (rounded down) and a right
@@ -1227,7 +1229,6 @@ __device__ __forceinline__ void epilogue_role(const Params &p, const Smem<F32, S
                 }
                 if (nr >= 3) take_into(Cc);
                 if (nr >= 2) add(B, Cc);
-                if (!ok) return;
                 if (nl > 0) add(A, B);
                 else {
 #pragma unroll
@@ -1254,6 +1255,7 @@ __device__ __forceinline__ void epilogue_role(const Params &p, const Smem<F32, S
         // variants store it after the walk, which keeps that once-per-tile
         // code out of the block loop (2 % faster on their launches); the
         // FP32 variant measured 6 % slower that way and stores it in place.
+        if (!ok) return;   // a wait of this tile failed: the launch is aborting
         if constexpr (!F32) store_out<F32, SWAP>(A, p, c);
     }
 }
