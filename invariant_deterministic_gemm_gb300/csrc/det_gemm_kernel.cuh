@@ -24,7 +24,7 @@
 //              order (turn barriers). Warp 17 also allocates and frees TMEM.
 //
 // FP32-output tile (128 x 96): the same 640 threads and roles; each
-// epilogue thread owns 24 FP32 columns.
+// epilogue thread owns 32 FP32 columns (twelve epilogue warps, 512 threads).
 //
 // Transposed tile (launches with at most 64 output rows, BF16 out): the
 // MMA's A operand is the weight, so its 128 TMEM lanes are 128 output
@@ -93,12 +93,13 @@ constexpr int kPrefetchRounds = 2;  // transposed tile: L2 prefetch distance, in
 template <bool F32, bool SWAP = false>
 struct Cfg {
     // Epilogue warps and output columns per tile (rows when SWAP). The FP32
-    // tile is 96 columns wide with four epilogue warps per scheduler, 24
+    // tile is 96 columns wide with three epilogue warps per scheduler, 32
     // FP32 columns each: the thread that issues an MMA of 128 rows waits
     // about as long for any N up to 256, so a wider tile does more per MMA
     // issued, and 96 columns of FP32 values and pending partials still fit
-    // the registers, TMEM and shared memory.
-    static constexpr int EPI_WARPS = SWAP ? 8 : 16;
+    // the registers, TMEM and shared memory. (Four warps of 24 columns ran
+    // 1-3 % slower once the accumulator wait had no branch after it.)
+    static constexpr int EPI_WARPS = SWAP ? 8 : (F32 ? 12 : 16);
     static constexpr int GROUPS = EPI_WARPS / 4;        // epilogue warps per TMEM lane quadrant
     static constexpr int BN = SWAP ? 64 : (F32 ? 96 : 128);
     // TMEM accumulator buffers. The BF16 tile takes three, which leaves
@@ -119,7 +120,7 @@ struct Cfg {
     static constexpr int B_STAGE = B_COPY_COLS * kBK * 2;   // bytes of one B stage
     static constexpr int STAGE_TX = A_STAGE + B_STAGE;  // TMA bytes per stage with full boxes
     static constexpr int COLS = BN / GROUPS;            // accumulator columns per epilogue thread
-    static constexpr int WORDS = F32 ? COLS : COLS / 2; // 32-bit words per value per thread (16, or 24 for fp32)
+    static constexpr int WORDS = F32 ? COLS : COLS / 2; // 32-bit words per value per thread (16, or 32 for fp32)
     static constexpr int TMEM_COLS = 512;
     static constexpr int TMEM_SLOT_BASE = NACC * BN;    // after the accumulators
     static constexpr int TMEM_SLOT_STRIDE = WORDS * GROUPS;   // TMEM columns of one slot
@@ -170,7 +171,7 @@ struct Cfg {
     static_assert(SCRATCH_CTA_BYTES <= kMaxScratchCtaBytes, "scratch");
     static_assert(SMEM_BYTES <= 232448, "shared memory");
     static_assert(A_STAGE % 1024 == 0 && B_STAGE % 1024 == 0, "swizzle atoms");
-    static_assert(F32 ? WORDS == 24 : WORDS == 16, "epilogue values are 16 (BF16) or 24 (FP32) words per thread");
+    static_assert(F32 ? WORDS == 32 : WORDS == 16, "epilogue values are 16 (BF16) or 32 (FP32) words per thread");
     static_assert(EPI_WARPS % 4 == 0, "whole TMEM lane quadrants");
 };
 
@@ -432,41 +433,17 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
         : "memory");
 }
 
-// 24 columns as three loads of 8: every load starts on a multiple of its
-// own width (the FP32 tile's columns are 24 * group + 8 * i).
-__device__ __forceinline__ void tmem_ld24(uint32_t taddr, uint32_t (&r)[24])
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32])
 {
     asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%24];\n\t"
-        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%8, %9, %10, %11, %12, %13, %14, %15}, [%25];\n\t"
-        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%16, %17, %18, %19, %20, %21, %22, %23}, [%26];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
-          "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23])
-        : "r"(taddr), "r"(taddr + 8u), "r"(taddr + 16u));
-}
-
-__device__ __forceinline__ void tmem_st24(uint32_t taddr, const uint32_t (&r)[24])
-{
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%3, %4, %5, %6, %7, %8, %9, %10};\n\t"
-        "tcgen05.st.sync.aligned.32x32b.x8.b32 [%1], {%11, %12, %13, %14, %15, %16, %17, %18};\n\t"
-        "tcgen05.st.sync.aligned.32x32b.x8.b32 [%2], {%19, %20, %21, %22, %23, %24, %25, %26};"
-        ::"r"(taddr), "r"(taddr + 8u), "r"(taddr + 16u),
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17};\n\t"
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%1], {%18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33};"
+        ::"r"(taddr), "r"(taddr + 16u),
         "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
         "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
-        "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23])
+        "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
+        "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
         : "memory");
-}
-
-__device__ __forceinline__ void reg_fence24(uint32_t (&r)[24])
-{
-    asm volatile(""
-                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
-                   "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
-                   "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]),
-                   "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]));
 }
 
 __device__ __forceinline__ void reg_fence16(uint32_t (&r)[16])
@@ -554,7 +531,7 @@ __device__ __forceinline__ int problem_of(const Params &p, int u)
 // ------------------------------------------------------------- epilogue
 
 // Every epilogue value (a rounded leaf, a partial, the root) holds a
-// thread's columns (ValW<W>): 32 columns as 16 words of BF16 pairs, or 24
+// thread's columns (ValW<W>): 32 columns as 16 words of BF16 pairs, or 32
 // FP32 words.
 template <int W>
 using ValW = uint32_t[W];
@@ -564,25 +541,23 @@ using Val = ValW<16>;
 template <int W>
 __device__ __forceinline__ void tmem_ld_val(uint32_t taddr, ValW<W> &t)
 {
-    static_assert(W == 16 || W == 24 || W == 32, "TMEM load width");
+    static_assert(W == 16 || W == 32, "TMEM load width");
     if constexpr (W == 16) tmem_ld16(taddr, t);
-    else if constexpr (W == 24) tmem_ld24(taddr, t);
     else tmem_ld32(taddr, t);
 }
 
 template <int W>
 __device__ __forceinline__ void tmem_st_val(uint32_t taddr, const ValW<W> &v)
 {
-    static_assert(W == 16 || W == 24, "TMEM store width");
+    static_assert(W == 16 || W == 32, "TMEM store width");
     if constexpr (W == 16) tmem_st16(taddr, v);
-    else tmem_st24(taddr, v);
+    else tmem_st32(taddr, v);
 }
 
 template <int W>
 __device__ __forceinline__ void reg_fence_val(ValW<W> &t)
 {
     if constexpr (W == 16) reg_fence16(t);
-    else if constexpr (W == 24) reg_fence24(t);
     else reg_fence(t);
 }
 
@@ -598,21 +573,16 @@ struct EpiCtx {
     long long ldo;        // its leading dimension, elements
 };
 
-// 16-byte chunk k of a thread's shared-memory line of CHUNKS chunks (4, 6
-// or 8). Lines of consecutive lanes are 16*CHUNKS bytes apart; permuting the
+// 16-byte chunk k of a thread's shared-memory line of CHUNKS chunks (4 or
+// 8). Lines of consecutive lanes are 16*CHUNKS bytes apart; permuting the
 // chunks by lane puts the eight lanes of a quarter-warp access on eight
-// distinct bank groups. With 96-byte lines, lanes l and l+4 of a quarter
-// start on the same bank group and the four even ones on distinct ones;
-// rotating the upper four lanes' chunks by one puts them on the odd ones.
+// distinct bank groups.
 template <int CHUNKS>
 __device__ __forceinline__ uint32_t smem_chunk(uint32_t line, int lane, int k)
 {
-    static_assert(CHUNKS == 4 || CHUNKS == 6 || CHUNKS == 8, "lines of 64, 96 or 128 bytes");
+    static_assert(CHUNKS == 4 || CHUNKS == 8, "lines of 64 or 128 bytes");
     if constexpr (CHUNKS == 4) return line + static_cast<uint32_t>((k ^ ((lane >> 1) & 3)) * 16);
-    else if constexpr (CHUNKS == 6) {
-        const int r = (lane & 4) ? (k == 5 ? 0 : k + 1) : k;
-        return line + static_cast<uint32_t>(r * 16);
-    } else return line + static_cast<uint32_t>((k ^ (lane & 7)) * 16);
+    else return line + static_cast<uint32_t>((k ^ (lane & 7)) * 16);
 }
 
 // Writes this thread's value of the root to the output, clipped to the
@@ -724,7 +694,7 @@ __device__ __forceinline__ void store_slot(int s, const ValW<Cfg<F32, SWAP>::WOR
 
 // Loads this thread's N accumulator columns (FP32) into r and waits: the
 // staging registers of a BF16 leaf (32 columns), or the value itself of an
-// FP32 leaf (24 columns).
+// FP32 leaf (32 columns).
 template <int N>
 __device__ __forceinline__ void stage_load(uint32_t acc_taddr, ValW<N> &r)
 {
