@@ -786,17 +786,37 @@ __device__ __forceinline__ void stage_role(const Params &p, const Smem<F32, SWAP
         // Test hook: a wait that nothing will end.
         ok = __all_sync(0xFFFFFFFFu, wait_bounded(S.never(), 0, S.abort_flag, p.status, p.timeout_ns, true));
     }
+    // Grouped launch: the work unit's problem (a search over the problems),
+    // part and tile, kept from its first stage for the rest (this warp takes
+    // KS / kStageWarps stages of a unit). The plain launches recompute them
+    // per stage, which measured faster for them.
+    int cur_tl = -1, pi = 0, g_part = 0, g_mt = 0, g_nt = 0;
     for (int g = j; ok && g < total; g += kStageWarps) {
         const uint32_t round = static_cast<uint32_t>(g / kStageWarps) & 1u;
         const int tl = fdiv(g, p.div_stages);         // unit of this CTA
         const int ks = g - tl * KS;
-        const int u = blockIdx.x + tl * gridDim.x;
-        const Problem &pb = p.prob[GROUPED ? problem_of(p, u) : 0];
-        const int ul = u - pb.first_unit;
-        const int t = fdiv(ul, p.div_parts);
-        const int part = ul - t * p.parts;
-        int mt, nt;
-        tile_coords(t, pb, p.n_tiles, mt, nt);
+        int part, mt, nt;
+        if constexpr (GROUPED) {
+            if (tl != cur_tl) {
+                cur_tl = tl;
+                const int u = blockIdx.x + tl * gridDim.x;
+                pi = problem_of(p, u);
+                const int ul = u - p.prob[pi].first_unit;
+                const int t = fdiv(ul, p.div_parts);
+                g_part = ul - t * p.parts;
+                tile_coords(t, p.prob[pi], p.n_tiles, g_mt, g_nt);
+            }
+            part = g_part;
+            mt = g_mt;
+            nt = g_nt;
+        } else {
+            const int u = blockIdx.x + tl * gridDim.x;
+            const int ul = u - p.prob[0].first_unit;
+            const int t = fdiv(ul, p.div_parts);
+            part = ul - t * p.parts;
+            tile_coords(t, p.prob[0], p.n_tiles, mt, nt);
+        }
+        const Problem &pb = p.prob[pi];
         // ---- copy the stage into the slot once the MMAs of its last use are done
         if (!warp_wait(empty, round ^ 1u, S.abort_flag, p.status, p.timeout_ns)) {
             ok = false;
