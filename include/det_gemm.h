@@ -254,9 +254,9 @@ det_gemm_status det_rmsnorm(const det_gemm_bf16 *x, const det_gemm_bf16 *w, det_
  * describing det_gemm have no counterpart to this entry point.
  *
  * det_gemm_fwd allocates a scratch buffer with cudaMalloc on its first
- * launch on a stream. Callers that are capturing a CUDA graph, that run on a
- * memory arena they manage themselves, or that must never trigger an
- * allocation's device-wide synchronisation cannot accept that. This entry
+ * launch on a stream. Callers that run on a memory arena they manage
+ * themselves, or that must never trigger an allocation's device-wide
+ * synchronisation, cannot accept that. This entry
  * point computes exactly the same product, bit for bit, with the scratch in
  * a fixed 15 MiB array compiled into the library (every GPU that loads the
  * library holds it until the process exits), and allocates nothing: no
@@ -272,8 +272,7 @@ det_gemm_status det_rmsnorm(const det_gemm_bf16 *x, const det_gemm_bf16 *w, det_
  *     before anything is enqueued (det_gemm_last_error_detail says why).
  *   - Every call shares the array and nothing in it needs to start at zero
  *     (each pending partial is written before it is read). Calls that
- *     overlap on the GPU (different streams, or graphs replayed
- *     concurrently) race on it: serialise them.
+ *     overlap on the GPU (different streams) race on it: serialise them.
  *   - Arguments, layouts and errors are those of det_gemm_fwd.
  */
 det_gemm_status det_gemm_fwd_noalloc(const det_gemm_bf16 *A, const det_gemm_bf16 *B, det_gemm_bf16 *C,

@@ -194,7 +194,7 @@ def det_gemm_fwd(A: torch.Tensor, B: torch.Tensor, out: torch.Tensor | None = No
 
 def det_gemm_fwd_noalloc(A: torch.Tensor, B: torch.Tensor, out: torch.Tensor, stream=None):
     """det_gemm_fwd without any allocation, for callers that cannot allocate
-    device memory (graph capture, caller-managed arenas): the output must be
+    device memory (caller-managed arenas): the output must be
     given, and the library's scratch is a fixed array in its device image
     (see det_gemm.h for its limit and for why overlapping calls race)."""
     M, K = A.shape

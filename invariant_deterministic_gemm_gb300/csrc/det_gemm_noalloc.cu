@@ -3,13 +3,11 @@
 //
 // det_gemm_fwd keeps the tree's most rarely touched pending partials in a
 // scratch buffer that it allocates with cudaMalloc the first time it runs on
-// a stream. Some callers cannot let a library do that: code that is being
-// captured into a CUDA graph (cudaMalloc may not be called while a stream is
-// capturing, and a captured launch must not depend on an allocation made
-// behind the caller's back), serving and real-time paths that own every byte
-// of device memory through their own arena and must never trigger the
-// device-wide synchronisation an allocation can imply, and callers that run
-// with the device memory they were given and nothing more. This entry point
+// a stream. Some callers cannot let a library do that: serving and
+// real-time paths that own every byte of device memory through their own
+// arena and must never trigger the device-wide synchronisation an
+// allocation can imply, and callers that run with the device memory they
+// were given and nothing more. This entry point
 // runs the same kernel with its scratch in a fixed array that is part of the
 // library's device image instead.
 #include "det_gemm.h"

@@ -1,7 +1,6 @@
 """det_gemm_fwd_noalloc: the forward product for callers that cannot
-allocate device memory -- code being captured into a CUDA graph (cudaMalloc
-may not run while a stream captures), serving paths that hand every byte of
-device memory out of their own arena, and paths that must never trigger the
+allocate device memory -- serving paths that hand every byte of device
+memory out of their own arena, and paths that must never trigger the
 device-wide synchronisation an allocation can imply. It must give exactly
 what det_gemm_fwd gives (the same kernel and arithmetic, with its scratch in
 a fixed array of the library instead of a cudaMalloc'd buffer), call after
