@@ -110,7 +110,8 @@ struct Cfg {
     // three of them in TMEM a 448-leaf tree parks 12 instead of 24 values
     // per tile in shared memory and 3 instead of 7 in global memory, which
     // made that launch 4 % faster (with four accumulators it was a tenth
-    // slower).
+    // slower; with three, in the twelve-warp tile, the 448-leaf launch ran
+    // 2 % faster and the 128-leaf FP32 LM head 2 % slower).
     static constexpr int NACC = 3 - (F32 ? 1 : 0);
     static constexpr int STAGES = kStageWarps;          // shared-memory ring depth: one slot per stage warp
     static constexpr int A_STAGE = kBM * kBK * 2;       // bytes of one A stage
