@@ -592,6 +592,66 @@ det_gemm_status run_problems(Variant v, bool a_kmajor, bool b_kmajor, const Prob
 }
 
 // One plain GEMM (see run_problems).
+// The argument checks of run_problems for one plain product, without a launch.
+det_gemm_status validate_plain(const Mat &a, const Mat &b, const Mat &out, int64_t rows, int64_t cols, int64_t kc)
+{
+    if (rows < 0 || cols < 0 || kc < 0) return DET_GEMM_ERR_INVALID_ARG;
+    if (cols > (int64_t{1} << 31) - 256 || rows > (int64_t{1} << 31) - 256) return DET_GEMM_ERR_INVALID_ARG;
+    if (kc > kKcMax) return DET_GEMM_ERR_K_TOO_LARGE;
+    if (rows == 0 || cols == 0) return DET_GEMM_OK;
+    det_gemm_status s;
+    if ((s = check_mat(out)) != DET_GEMM_OK) return s;
+    if (kc > 0) {
+        if ((s = check_mat(a)) != DET_GEMM_OK) return s;
+        if ((s = check_mat(b)) != DET_GEMM_OK) return s;
+        if (overlaps(out, a) || overlaps(out, b)) return DET_GEMM_ERR_INVALID_ARG;
+    }
+    return DET_GEMM_OK;
+}
+
+// The busiest CTA's cost, in leaves, of a launch of `tiles` tiles over L
+// leaves with the contraction split that choose_parts picks (its model).
+int64_t launch_cost(int64_t tiles, int64_t L, int sms)
+{
+    const int parts = choose_parts(tiles, L, sms);
+    return (tiles * parts + sms - 1) / sms * (L / parts) + (parts > 1 ? int64_t{8} : int64_t{0});
+}
+
+// Tail split of a plain launch. When its tiles fill some rounds of one CTA
+// per SM and leave only a few tiles for the last round, the output's last
+// column panels run as a second launch of few tiles, which choose_parts
+// then splits at tree nodes over the otherwise idle SMs: QKV at 1024 rows
+// has 768 = 5 x 152 + 8 tiles of 128 leaves; 760 of them fill five rounds
+// and the other 8 run as 64 units of 16 leaves. Every element keeps its
+// leaves and tree (a split is tree-aligned), so the bits are those of one
+// launch. Returns the first column of the tail (a multiple of the tile
+// width), or 0 when one launch is as fast: the second launch and its merge
+// are counted as 24 leaves, and the split must save a twentieth.
+int64_t tail_split_column(Variant v, int64_t rows, int64_t cols, int64_t kc)
+{
+    if (v != kBf16KMN && v != kBf16KK && v != kBf16MNMN && v != kF32KMN && v != kF32KK) return 0;
+    if (rows <= 0 || cols <= 0 || kc <= 0) return 0;
+    DeviceState *st = nullptr;
+    if (device_state(&st) != DET_GEMM_OK) return 0;
+    const int sms = st->sm_count;
+    const int bn = variant_ops(v).bn;
+    const int64_t m_tiles = (rows + kBM - 1) / kBM, n_tiles = (cols + bn - 1) / bn;
+    const int64_t L = (kc + kLeaf - 1) / kLeaf;
+    const int64_t tiles = m_tiles * n_tiles;
+    if (tiles <= sms) return 0;
+    const int64_t whole = launch_cost(tiles, L, sms);
+    int64_t best = whole, best_c = 0;
+    for (int64_t c = 1; c < n_tiles && m_tiles * c <= sms; ++c) {
+        const int64_t cost = launch_cost(m_tiles * (n_tiles - c), L, sms) + launch_cost(m_tiles * c, L, sms) + 24;
+        if (cost < best) {
+            best = cost;
+            best_c = c;
+        }
+    }
+    if (best_c == 0 || best * 20 > whole * 19) return 0;
+    return (n_tiles - best_c) * bn;
+}
+
 det_gemm_status run(Variant v, Mat a, bool a_kmajor, Mat b, bool b_kmajor, Mat out, int64_t rows, int64_t cols,
                     int64_t kc, cudaStream_t stream, void *fixed_scratch = nullptr, size_t fixed_bytes = 0)
 {
@@ -606,6 +666,29 @@ det_gemm_status run(Variant v, Mat a, bool a_kmajor, Mat b, bool b_kmajor, Mat o
                             fixed_scratch, fixed_bytes);
     }
     const ProblemArgs pa{a, b, out, rows, nullptr, 0, nullptr};
+    int64_t c0 = 0;
+    if (!fixed_scratch && (c0 = tail_split_column(v, rows, cols, kc)) > 0) {
+        // Validate the whole product first: argument errors come back before
+        // anything is enqueued, as for an unsplit launch.
+        det_gemm_status s = validate_plain(a, b, out, rows, cols, kc);
+        if (s != DET_GEMM_OK) return s;
+        Mat b_tail = b, out_tail = out;
+        const Mat b_main = b_kmajor ? Mat{b.ptr, c0, b.cols, b.ld, b.esize} : Mat{b.ptr, b.rows, c0, b.ld, b.esize};
+        if (b_kmajor) {
+            b_tail.ptr = static_cast<const uint8_t *>(b.ptr) + c0 * b.ld * b.esize;
+            b_tail.rows = cols - c0;
+        } else {
+            b_tail.ptr = static_cast<const uint8_t *>(b.ptr) + c0 * b.esize;
+            b_tail.cols = cols - c0;
+        }
+        const Mat out_main{out.ptr, out.rows, c0, out.ld, out.esize};
+        out_tail.ptr = static_cast<const uint8_t *>(out.ptr) + c0 * out.esize;
+        out_tail.cols = cols - c0;
+        const ProblemArgs pm{a, b_main, out_main, rows, nullptr, 0, nullptr};
+        if ((s = run_problems(v, a_kmajor, b_kmajor, &pm, 1, c0, kc, stream)) != DET_GEMM_OK) return s;
+        const ProblemArgs pt{a, b_tail, out_tail, rows, nullptr, 0, nullptr};
+        return run_problems(v, a_kmajor, b_kmajor, &pt, 1, cols - c0, kc, stream);
+    }
     return run_problems(v, a_kmajor, b_kmajor, &pa, 1, cols, kc, stream, fixed_scratch, fixed_bytes);
 }
 

@@ -65,3 +65,34 @@ def test_split_weight_gradient_is_exact_on_integer_inputs():
         want = oracle.db(W.bits(A), W.bits(dC))
         assert exact_equal(W.bits(got), want), (kout, n)
         assert exact_equal(W.bits(got_t), np.ascontiguousarray(want.T)), (kout, n)
+
+
+def test_tail_split_equals_one_launch():
+    """A launch whose tiles fill whole rounds of one CTA per SM but a few
+    (the QKV projection at 1024 rows: 8 x 96 = 768 = 5 x 152 + 8 tiles)
+    runs its last column panel as a second launch whose tiles split their
+    contraction over the idle SMs. The result must be one launch's bits: a
+    one-group grouped launch never splits, and exact inputs must give the
+    oracle's bits."""
+    M, K, N = 1024, 4096, 12288
+    A = dev(W.randn_bf16((M, K), 1.0, 7600))
+    B = dev(W.randn_bf16((K, N), 0.02, 7601))
+    C = dg.det_gemm_fwd(A, B)
+    (G,) = dg.det_gemm_fwd_grouped([A], [B])
+    check()
+    assert bits_equal(C, G)
+    # the same through the other operand layouts that take the tail split
+    Wt = dev(W.randn_bf16((N, K), 0.02, 7602))
+    Ct = dg.det_gemm_fwd_rhs_transposed(A, Wt)
+    check()
+    Ai = W.randint_bf16((M, K), -3, 4, 7603)
+    Bi = W.randint_bf16((K, N), -3, 4, 7604)
+    Ci = dg.det_gemm_fwd(dev(Ai), dev(Bi))
+    check()
+    rows = np.array([0, 1, 511, 1023])
+    want = oracle.fwd(W.bits(Ai)[rows], W.bits(Bi))
+    assert exact_equal(W.bits(Ci.cpu())[rows], want)
+    # rhs-transposed against the forward with the weight transposed
+    Cf = dg.det_gemm_fwd(A, Wt.t().contiguous())
+    check()
+    assert bits_equal(Ct, Cf)
