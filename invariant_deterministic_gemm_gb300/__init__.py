@@ -20,6 +20,7 @@ column stride; row-slices of bigger tensors are accepted as they are.
 """
 from __future__ import annotations
 
+import array
 import ctypes
 import os
 import threading
@@ -130,26 +131,36 @@ def _stream_handle(stream) -> int:
 _ELEM_SIZE = {torch.bfloat16: 2, torch.float32: 4}
 
 
-def _mat(t: torch.Tensor, name: str, dtype=torch.bfloat16):
+def _name(name: str, index: int) -> str:
+    return name if index < 0 else "%s[%d]" % (name, index)
+
+
+def _mat(t: torch.Tensor, name: str, dtype=torch.bfloat16, index: int = -1):
+    """(data pointer, leading dimension) of a 2-D row-major CUDA tensor
+    (name, or name[index] for an element of a list, in error messages).
+    Each tensor property is read once and the name is formatted only for an
+    error: this marshalling is a small launch's whole host cost."""
     if not isinstance(t, torch.Tensor):
-        raise TypeError("%s must be a torch.Tensor" % name)
+        raise TypeError("%s must be a torch.Tensor" % _name(name, index))
     if t.dtype != dtype:
-        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
-    if t.dim() != 2:
-        raise ValueError("%s must be 2-D, got shape %s" % (name, tuple(t.shape)))
+        raise TypeError("%s must be %s, got %s" % (_name(name, index), dtype, t.dtype))
     if not t.is_cuda:
-        raise ValueError("%s must be a CUDA tensor" % name)
-    if t.shape[1] > 1 and t.stride(1) != 1:
-        raise ValueError("%s must be row-major with unit column stride" % name)
-    if t.shape[0] > 1:
-        ld = t.stride(0)
+        raise ValueError("%s must be a CUDA tensor" % _name(name, index))
+    shape = t.shape
+    if len(shape) != 2:
+        raise ValueError("%s must be 2-D, got shape %s" % (_name(name, index), tuple(shape)))
+    rows, cols = shape
+    s0, s1 = t.stride()
+    if cols > 1 and s1 != 1:
+        raise ValueError("%s must be row-major with unit column stride" % _name(name, index))
+    if rows > 1:
+        ld = s0
     else:
         # One row: the leading dimension is never used to address anything,
         # so any value that meets the library's 16-byte pitch rule will do.
-        ld = max(t.shape[1], t.stride(0))
         per16 = 16 // _ELEM_SIZE[dtype]
-        ld = (ld + per16 - 1) // per16 * per16
-    return t.data_ptr(), int(ld)
+        ld = (max(cols, s0) + per16 - 1) // per16 * per16
+    return t.data_ptr(), ld
 
 
 def _out(out, rows, cols, dtype, like: torch.Tensor):
@@ -299,7 +310,7 @@ def det_gemm_db_transposed(A: torch.Tensor, dC: torch.Tensor, out=None, stream=N
 def _merge(name, parts, out, dtype, stream):
     if not isinstance(parts, (list, tuple)) or len(parts) not in (2, 4, 8):
         raise ValueError("parts must be a list of 2, 4 or 8 tensors")
-    mats = [_mat(t, "parts[%d]" % i, dtype) for i, t in enumerate(parts)]
+    mats = [_mat(t, "parts", dtype, i) for i, t in enumerate(parts)]
     shape = tuple(parts[0].shape)
     if any(tuple(t.shape) != shape for t in parts):
         raise ValueError("parts must all have the same shape")
@@ -339,32 +350,50 @@ def det_gemm_fwd_grouped(As, Bs, outs=None, D=None, stream=None):
     if G == 0:
         return ([], []) if D is not None else []
     K, N = Bs[0].shape
-    mats_a = [_mat(a, "As[%d]" % g) for g, a in enumerate(As)]
-    mats_b = [_mat(b, "Bs[%d]" % g) for g, b in enumerate(Bs)]
+    bf16 = torch.bfloat16
+    a_ptr, a_ld, b_ptr, b_ld, c_ptr, c_ld, Ms, Cs = [], [], [], [], [], [], [], []
     for g in range(G):
-        if As[g].shape[1] != K or tuple(Bs[g].shape) != (K, N):
+        a, b = As[g], Bs[g]
+        p, ld = _mat(a, "As", bf16, g)
+        a_ptr.append(p)
+        a_ld.append(ld)
+        p, ld = _mat(b, "Bs", bf16, g)
+        b_ptr.append(p)
+        b_ld.append(ld)
+        m, k = a.shape
+        if k != K or b.shape != (K, N):
             raise ValueError("group %d: A must be [M, %d] and B [%d, %d]" % (g, K, K, N))
-    Cs = [_out(None if outs is None else outs[g], As[g].shape[0], N, torch.bfloat16, As[g]) for g in range(G)]
-    mats_c = [_mat(c, "outs[%d]" % g) for g, c in enumerate(Cs)]
-    ptrs = lambda xs: (ctypes.c_void_p * G)(*xs)
-    lds = lambda xs: (ctypes.c_int64 * G)(*xs)
-    Ms = lds([a.shape[0] for a in As])
+        c = _out(None if outs is None else outs[g], m, N, bf16, a)
+        p, ld = _mat(c, "outs", bf16, g)
+        c_ptr.append(p)
+        c_ld.append(ld)
+        Ms.append(m)
+        Cs.append(c)
     rowdots = None
-    d_arr = ld_arr = rd_arr = None
+    vals = a_ptr + b_ptr + c_ptr + Ms + a_ld + b_ld + c_ld
     if D is not None:
-        rowdots = [None if D[g] is None else torch.empty(As[g].shape[0], dtype=torch.float32, device=As[g].device)
+        rowdots = [None if D[g] is None else torch.empty(Ms[g], dtype=torch.float32, device=As[g].device)
                    for g in range(G)]
-        dm = [(0, N) if D[g] is None else _mat(D[g], "D[%d]" % g) for g in range(G)]
+        d_ptr, d_ld = [], []
         for g in range(G):
-            if D[g] is not None and tuple(D[g].shape) != (As[g].shape[0], N):
-                raise ValueError("D[%d] must be [M, N]" % g)
-        d_arr = ptrs([x for x, _ in dm])
-        ld_arr = lds([x for _, x in dm])
-        rd_arr = ptrs([0 if r is None else r.data_ptr() for r in rowdots])
-    st = lib().det_gemm_fwd_grouped(G, ptrs([x for x, _ in mats_a]), ptrs([x for x, _ in mats_b]),
-                                    ptrs([x for x, _ in mats_c]), Ms, N, K, lds([x for _, x in mats_a]),
-                                    lds([x for _, x in mats_b]), lds([x for _, x in mats_c]), d_arr, ld_arr, rd_arr,
-                                    _stream_handle(stream))
+            d = D[g]
+            if d is None:
+                p, ld = 0, N
+            else:
+                p, ld = _mat(d, "D", bf16, g)
+                if d.shape != (Ms[g], N):
+                    raise ValueError("D[%d] must be [M, N]" % g)
+            d_ptr.append(p)
+            d_ld.append(ld)
+        vals += d_ptr + d_ld + [0 if r is None else r.data_ptr() for r in rowdots]
+    # All per-group arrays in one host buffer (a ctypes array per list costs
+    # several times more); the call reads it before it returns.
+    buf = array.array("q", vals)
+    base = buf.buffer_info()[0]
+    at = [base + 8 * G * i for i in range(len(vals) // G)]
+    d_arr, ld_arr, rd_arr = (at[7], at[8], at[9]) if D is not None else (None, None, None)
+    st = lib().det_gemm_fwd_grouped(G, at[0], at[1], at[2], at[3], N, K, at[4], at[5], at[6], d_arr, ld_arr,
+                                    rd_arr, _stream_handle(stream))
     if st != 0:
         raise DetGemmError(st, "det_gemm_fwd_grouped")
     return (Cs, rowdots) if D is not None else Cs
