@@ -34,10 +34,13 @@
 // accumulators back); warp 8 copies every stage in with TMA and prefetches
 // the weight tiles of later stages into L2, and warps 9-11 issue the MMAs,
 // each into its own accumulator and without a turn order. The accumulators
-// and all seven pending slots fit in TMEM.
+// and all seven pending slots fit in TMEM. With at most 8 (16) output rows
+// the epilogue loads, rounds and merges only the 8 (16) columns of each
+// leaf that hold rows.
 //
 // Per tile: 64-wide K stages (two leaves) of the A and B operand tiles go
-// through a ring of four swizzled shared-memory slots. For leaf l the stage
+// through a ring of swizzled shared-memory slots (four; eight in the
+// transposed tile). For leaf l the stage
 // warp issues two K=16 MMAs into accumulator buffer l % NACC (the first one
 // overwrites, so each leaf starts from zero) and commits to that buffer's
 // "full" barrier. The epilogue loads the leaf, frees the buffer at once (so
@@ -78,7 +81,7 @@
 namespace detg {
 
 constexpr int kStatusTimeout = 6;   // DET_GEMM_ERR_TIMEOUT
-constexpr int kPrefetchRounds = 2;  // transposed tile: L2 prefetch distance, in rounds of the stage ring
+constexpr int kPrefetchRounds = 1;  // transposed tile: L2 prefetch distance, in rounds of the stage ring
 
 
 // ------------------------------------------------------------------ config
@@ -113,7 +116,11 @@ struct Cfg {
     // slower; with three, in the twelve-warp tile, the 448-leaf launch ran
     // 2 % faster and the 128-leaf FP32 LM head 2 % slower).
     static constexpr int NACC = 3 - (F32 ? 1 : 0);
-    static constexpr int STAGES = kStageWarps;          // shared-memory ring depth: one slot per stage warp
+    // Shared-memory ring depth: one slot per stage warp in the plain tiles;
+    // eight in the transposed tile, whose single copy warp keeps up to 16
+    // leaves of weight in flight (launches of 17 and 64 rows 2 us faster
+    // than with four; one row, bound by the epilogue, unchanged).
+    static constexpr int STAGES = SWAP ? 8 : kStageWarps;
     static constexpr int A_STAGE = kBM * kBK * 2;       // bytes of one A stage
     // MN-major B tiles are copied in boxes of 64 columns (one 128-byte
     // swizzle span), so a stage holds BN rounded up to 64 columns.
@@ -424,6 +431,34 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16])
         : "r"(taddr));
 }
 
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t (&r)[8])
+{
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_ld4(uint32_t taddr, uint32_t (&r)[4])
+{
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8])
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+                 "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_st4(uint32_t taddr, const uint32_t (&r)[4])
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(r[0]),
+                 "r"(r[1]), "r"(r[2]), "r"(r[3])
+                 : "memory");
+}
+
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16])
 {
     asm volatile(
@@ -453,6 +488,16 @@ __device__ __forceinline__ void reg_fence16(uint32_t (&r)[16])
                  : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
                    "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
                    "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]));
+}
+
+__device__ __forceinline__ void reg_fence8(uint32_t (&r)[8])
+{
+    asm volatile("" : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]));
+}
+
+__device__ __forceinline__ void reg_fence4(uint32_t (&r)[4])
+{
+    asm volatile("" : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]));
 }
 
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
@@ -538,27 +583,33 @@ template <int W>
 using ValW = uint32_t[W];
 using Val = ValW<16>;
 
-// TMEM <-> registers for W (16, 24 or 32) words.
+// TMEM <-> registers for W (4, 8, 16 or 32) words.
 template <int W>
 __device__ __forceinline__ void tmem_ld_val(uint32_t taddr, ValW<W> &t)
 {
-    static_assert(W == 16 || W == 32, "TMEM load width");
-    if constexpr (W == 16) tmem_ld16(taddr, t);
+    static_assert(W == 4 || W == 8 || W == 16 || W == 32, "TMEM load width");
+    if constexpr (W == 4) tmem_ld4(taddr, t);
+    else if constexpr (W == 8) tmem_ld8(taddr, t);
+    else if constexpr (W == 16) tmem_ld16(taddr, t);
     else tmem_ld32(taddr, t);
 }
 
 template <int W>
 __device__ __forceinline__ void tmem_st_val(uint32_t taddr, const ValW<W> &v)
 {
-    static_assert(W == 16 || W == 32, "TMEM store width");
-    if constexpr (W == 16) tmem_st16(taddr, v);
+    static_assert(W == 4 || W == 8 || W == 16 || W == 32, "TMEM store width");
+    if constexpr (W == 4) tmem_st4(taddr, v);
+    else if constexpr (W == 8) tmem_st8(taddr, v);
+    else if constexpr (W == 16) tmem_st16(taddr, v);
     else tmem_st32(taddr, v);
 }
 
 template <int W>
 __device__ __forceinline__ void reg_fence_val(ValW<W> &t)
 {
-    if constexpr (W == 16) reg_fence16(t);
+    if constexpr (W == 4) reg_fence4(t);
+    else if constexpr (W == 8) reg_fence8(t);
+    else if constexpr (W == 16) reg_fence16(t);
     else reg_fence(t);
 }
 
@@ -592,21 +643,20 @@ __device__ __forceinline__ uint32_t smem_chunk(uint32_t line, int lane, int k)
 // formed (every pending partial has been merged into it).
 //
 // Transposed tile (SWAP): the thread's TMEM lane is output column c.row and
-// its 32 values are output rows c.col .. c.col+31 of that column; each goes
+// its 2W values are output rows c.col .. c.col+2W-1 of that column; each goes
 // to out[(c.col + j) * ldo + c.row]. The 32 lanes of a warp hold 32
 // consecutive columns, so every store of the warp writes 64 contiguous bytes.
-template <bool F32, bool SWAP>
-__device__ __forceinline__ void store_out(const ValW<Cfg<F32, SWAP>::WORDS> &v, const Params &p, const EpiCtx &c)
+template <bool F32, bool SWAP, int W = Cfg<F32, SWAP>::WORDS>
+__device__ __forceinline__ void store_out(const ValW<W> &v, const Params &p, const EpiCtx &c)
 {
     using C = Cfg<F32, SWAP>;
-    constexpr int W = C::WORDS;
     constexpr int ES = F32 ? 4 : 2;
     if (c.row >= c.rows) return;
     if constexpr (SWAP) {
         const int nrows = p.cols - c.col;
         uint16_t *dst = reinterpret_cast<uint16_t *>(c.out) + static_cast<long long>(c.col) * c.ldo + c.row;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
+        for (int i = 0; i < W; ++i) {
             if (2 * i < nrows) dst[(2 * i) * c.ldo] = static_cast<uint16_t>(v[i] & 0xFFFFu);
             if (2 * i + 1 < nrows) dst[(2 * i + 1) * c.ldo] = static_cast<uint16_t>(v[i] >> 16);
         }
@@ -638,16 +688,19 @@ __device__ __forceinline__ void store_out(const ValW<Cfg<F32, SWAP>::WORDS> &v, 
     }
 }
 
-// Slot s >= 2 (TMEM, shared memory or global scratch) -> t.
-template <bool F32, bool SWAP>
-__device__ __forceinline__ void load_slot(int s, ValW<Cfg<F32, SWAP>::WORDS> &t, const EpiCtx &c)
+// Slot s >= 2 (TMEM, shared memory or global scratch) -> t. A narrow value
+// (W below the tile's words, transposed tile only) is the first W words of
+// the thread's slot columns.
+template <bool F32, bool SWAP, int W = Cfg<F32, SWAP>::WORDS>
+__device__ __forceinline__ void load_slot(int s, ValW<W> &t, const EpiCtx &c)
 {
     using C = Cfg<F32, SWAP>;
-    constexpr int W = C::WORDS;
-    if (s < C::SMEM_FIRST) {
+    static_assert(W == C::WORDS || C::SMEM_SLOTS + C::GLOBAL_SLOTS == 0, "narrow values live in TMEM only");
+    if (C::SMEM_SLOTS + C::GLOBAL_SLOTS == 0 || s < C::SMEM_FIRST) {
         tmem_ld_val<W>(c.tmem_slot + static_cast<uint32_t>((s - C::TMEM_FIRST) * C::TMEM_SLOT_STRIDE), t);
         tmem_wait_ld();
         reg_fence_val<W>(t);
+    } else if constexpr (W != C::WORDS) {
     } else if (s < C::GLOBAL_FIRST) {
         const uint32_t line = c.smem_slot + static_cast<uint32_t>((s - C::SMEM_FIRST) * C::SLOT_BYTES);
 #pragma unroll
@@ -668,14 +721,15 @@ __device__ __forceinline__ void load_slot(int s, ValW<Cfg<F32, SWAP>::WORDS> &t,
 }
 
 // v -> slot s >= 2 (TMEM, shared memory or global scratch).
-template <bool F32, bool SWAP>
-__device__ __forceinline__ void store_slot(int s, const ValW<Cfg<F32, SWAP>::WORDS> &v, const EpiCtx &c)
+template <bool F32, bool SWAP, int W = Cfg<F32, SWAP>::WORDS>
+__device__ __forceinline__ void store_slot(int s, const ValW<W> &v, const EpiCtx &c)
 {
     using C = Cfg<F32, SWAP>;
-    constexpr int W = C::WORDS;
-    if (s < C::SMEM_FIRST) {
+    static_assert(W == C::WORDS || C::SMEM_SLOTS + C::GLOBAL_SLOTS == 0, "narrow values live in TMEM only");
+    if (C::SMEM_SLOTS + C::GLOBAL_SLOTS == 0 || s < C::SMEM_FIRST) {
         tmem_st_val<W>(c.tmem_slot + static_cast<uint32_t>((s - C::TMEM_FIRST) * C::TMEM_SLOT_STRIDE), v);
         tmem_wait_st();
+    } else if constexpr (W != C::WORDS) {
     } else if (s < C::GLOBAL_FIRST) {
         const uint32_t line = c.smem_slot + static_cast<uint32_t>((s - C::SMEM_FIRST) * C::SLOT_BYTES);
 #pragma unroll
@@ -704,12 +758,13 @@ __device__ __forceinline__ void stage_load(uint32_t acc_taddr, ValW<N> &r)
     reg_fence_val<N>(r);
 }
 
-// A staged leaf's 32 FP32 columns -> F, rounded once to BF16 (RNE), two
+// A staged leaf's 2W FP32 columns -> F, rounded once to BF16 (RNE), two
 // columns per word.
-__device__ __forceinline__ void round_leaf(const uint32_t (&stg)[32], Val &F)
+template <int W>
+__device__ __forceinline__ void round_leaf(const uint32_t (&stg)[2 * W], ValW<W> &F)
 {
 #pragma unroll
-    for (int i = 0; i < 16; ++i) F[i] = cvt_bf16x2(stg[2 * i], stg[2 * i + 1]);
+    for (int i = 0; i < W; ++i) F[i] = cvt_bf16x2(stg[2 * i], stg[2 * i + 1]);
 }
 
 // ----------------------------------------------------------------- kernel
@@ -1076,11 +1131,17 @@ __device__ __forceinline__ void issue_role(const Params &p, const Smem<F32, SWAP
 // entry names and parked (one TMEM or scratch access) or written out as the
 // root. The code stays small so that the loop, rare branches included,
 // lives in the instruction cache.
-template <bool F32, bool GROUPED, bool SWAP>
+//
+// W is the number of words a thread loads, rounds, merges and stores per
+// value: the tile's WORDS, or, in the transposed tile of a launch with at
+// most 2W output rows, only the words that hold rows (8 or 16 columns of
+// each leaf instead of 32). The slots keep their layout; a narrow value is
+// the first W words of the thread's slot columns.
+template <bool F32, bool GROUPED, bool SWAP, int W = Cfg<F32, SWAP>::WORDS>
 __device__ __forceinline__ void epilogue_role(const Params &p, const Smem<F32, SWAP> &S, int warp, int lane)
 {
     using C = Cfg<F32, SWAP>;
-    constexpr int W = C::WORDS;
+    static_assert(W == C::WORDS || (SWAP && (W == 4 || W == 8)), "value width");
     const int q = warp & 3;               // TMEM lane quadrant (rows 32q .. 32q+31)
     const int cq = warp >> 2;             // column group of the tile (a quarter, or a half when SWAP)
     const uint32_t lane_bits = static_cast<uint32_t>(q * 32) << 16;
@@ -1095,7 +1156,8 @@ __device__ __forceinline__ void epilogue_role(const Params &p, const Smem<F32, S
     const int NB = p.num_blocks;
 
     ValW<W> A, B, Cc;
-    uint32_t stg[32];
+    constexpr int SW = F32 ? W : 2 * W;   // staging registers (the FP32 tile loads its leaves into the values)
+    uint32_t stg[SW];
     int acc = 0;                          // accumulator of the next leaf
     uint32_t acc_phase = 0;
     bool ok = true;
@@ -1107,7 +1169,7 @@ __device__ __forceinline__ void epilogue_role(const Params &p, const Smem<F32, S
         ok &= mbar_wait_inline(S.accf(acc), acc_phase, abort_s, p.status, p.timeout_ns) != 0;
         tc_fence_after();
         if constexpr (F32) stage_load<W>(acc0 + static_cast<uint32_t>(acc * C::BN), dst);
-        else stage_load<32>(acc0 + static_cast<uint32_t>(acc * C::BN), stg);
+        else stage_load<SW>(acc0 + static_cast<uint32_t>(acc * C::BN), stg);
         tc_fence_before();
         __syncwarp();
         mbar_arrive_if(S.acce(acc), lane == 0);
@@ -1115,7 +1177,7 @@ __device__ __forceinline__ void epilogue_role(const Params &p, const Smem<F32, S
             acc = 0;
             acc_phase ^= 1u;
         }
-        if constexpr (!F32) round_leaf(stg, dst);
+        if constexpr (!F32) round_leaf<W>(stg, dst);
     };
     // Waits for the next leaf's accumulator and hands it straight back.
     auto pass = [&]() {
@@ -1132,7 +1194,7 @@ __device__ __forceinline__ void epilogue_role(const Params &p, const Smem<F32, S
     auto take_into = [&](ValW<W> &dst) {
         ok &= mbar_wait_inline(S.accf(acc), acc_phase, abort_s, p.status, p.timeout_ns) != 0;
         tc_fence_after();
-        stage_load<32>(acc0 + static_cast<uint32_t>(acc * C::BN), stg);
+        stage_load<SW>(acc0 + static_cast<uint32_t>(acc * C::BN), stg);
         tc_fence_before();
         __syncwarp();
         mbar_arrive_if(S.acce(acc), lane == 0);
@@ -1141,7 +1203,7 @@ __device__ __forceinline__ void epilogue_role(const Params &p, const Smem<F32, S
             acc_phase ^= 1u;
         }
 #pragma unroll
-        for (int i = 0; i < 16; ++i) dst[i] = merge<false>(dst[i], cvt_bf16x2(stg[2 * i], stg[2 * i + 1]));
+        for (int i = 0; i < SW / 2; ++i) dst[i] = merge<false>(dst[i], cvt_bf16x2(stg[2 * i], stg[2 * i + 1]));
     };
     auto add = [](ValW<W> &left, const ValW<W> &right) {
 #pragma unroll
@@ -1230,16 +1292,16 @@ __device__ __forceinline__ void epilogue_role(const Params &p, const Smem<F32, S
 #pragma unroll 1
             for (uint32_t m = (e & 0x3FFu) >> C::TMEM_FIRST; m != 0; m &= m - 1) {
                 const int s = C::TMEM_FIRST + __ffs(static_cast<int>(m)) - 1;   // lowest pending slot left
-                load_slot<F32, SWAP>(s, B, c);   // B is free once the block is merged
+                load_slot<F32, SWAP, W>(s, B, c);   // B is free once the block is merged
 #pragma unroll
                 for (int i = 0; i < W; ++i) A[i] = merge<F32>(B[i], A[i]);
             }
             const int st = static_cast<int>(e >> 12);
             if constexpr (F32) {
-                if (st == kSlotRoot) store_out<F32, SWAP>(A, p, c);
-                else store_slot<F32, SWAP>(st, A, c);
+                if (st == kSlotRoot) store_out<F32, SWAP, W>(A, p, c);
+                else store_slot<F32, SWAP, W>(st, A, c);
             } else {
-                if (st != kSlotRoot) store_slot<F32, SWAP>(st, A, c);
+                if (st != kSlotRoot) store_slot<F32, SWAP, W>(st, A, c);
             }
         }
         // The schedule's last block, and only it, forms the root. The BF16
@@ -1247,7 +1309,7 @@ __device__ __forceinline__ void epilogue_role(const Params &p, const Smem<F32, S
         // code out of the block loop (2 % faster on their launches); the
         // FP32 variant measured 6 % slower that way and stores it in place.
         if (!ok) return;   // a wait of this tile failed: the launch is aborting
-        if constexpr (!F32) store_out<F32, SWAP>(A, p, c);
+        if constexpr (!F32) store_out<F32, SWAP, W>(A, p, c);
     }
 }
 
@@ -1324,8 +1386,13 @@ __global__ void __launch_bounds__(Cfg<F32, SWAP>::THREADS, 1) det_gemm_kernel(co
         }
     } else {
         // 384 threads: every warp has the registers it needs without a split.
-        if (warp < C::EPI_WARPS) epilogue_role<F32, GROUPED, SWAP>(p, S, warp, lane);
-        else if (warp == C::FIRST_STAGE_WARP) copy_role<A_MAJOR, B_MAJOR, F32, GROUPED, SWAP>(p, S);
+        // The epilogue handles only the columns of each leaf that hold rows
+        // when the launch has at most 8 or 16 of them.
+        if (warp < C::EPI_WARPS) {
+            if (p.cols <= 8) epilogue_role<F32, GROUPED, SWAP, 4>(p, S, warp, lane);
+            else if (p.cols <= 16) epilogue_role<F32, GROUPED, SWAP, 8>(p, S, warp, lane);
+            else epilogue_role<F32, GROUPED, SWAP>(p, S, warp, lane);
+        } else if (warp == C::FIRST_STAGE_WARP) copy_role<A_MAJOR, B_MAJOR, F32, GROUPED, SWAP>(p, S);
         else issue_role<A_MAJOR, B_MAJOR, F32, GROUPED, SWAP>(p, S, warp - C::FIRST_STAGE_WARP - 1);
     }
 

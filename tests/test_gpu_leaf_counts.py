@@ -40,7 +40,7 @@ def test_both_tiles_match_the_oracle_for_every_block_shape(L):
     check()
     assert exact_equal(W.bits(plain.cpu()), want), ("plain", L)
     assert exact_equal(W.bits(plain_t.cpu()), want_t), ("plain rhs_transposed", L)
-    for M in (1, 17, 64):                                 # the transposed tile
+    for M in (1, 8, 16, 17, 64):                          # the transposed tile (narrow up to 8 and 16 rows)
         got = dg.det_gemm_fwd(Ad[:M], Bd)
         got_t = dg.det_gemm_fwd_rhs_transposed(Ad[:M], Wd)
         check()

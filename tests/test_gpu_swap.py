@@ -30,7 +30,7 @@ from gpu_util import assert_bf16_close, check, dev, exact_equal
 
 pytestmark = pytest.mark.gpu
 
-ROWS = (1, 2, 7, 16, 17, 33, 63, 64)
+ROWS = (1, 2, 7, 8, 9, 16, 17, 33, 63, 64)
 
 
 def bits_equal(x, y):
@@ -136,9 +136,10 @@ def _adversarial(kind, shape, seed):
 @pytest.mark.parametrize("kind", ["normal", "wide", "ties"])
 @pytest.mark.parametrize("Kc", ADV_KC)
 def test_transposed_tile_equals_the_plain_tile_on_stress_inputs(kind, Kc):
-    """Five seeds per case. Rows 1, 17, 64 take the transposed tile (both of
-    its instances: B stored [K, N] for the forward, and K-major operands for
-    the rhs-transposed forward and dA); rows 65 and 128 take the plain tile;
+    """Five seeds per case. Rows 1, 8, 9, 16, 17, 64 take the transposed tile
+    (both of its instances: B stored [K, N] for the forward, and K-major
+    operands for the rhs-transposed forward and dA; at most 8 and at most 16
+    rows with its narrow epilogues); rows 65 and 128 take the plain tile;
     all are compared with the same rows of a 256-row launch."""
     N = 192                                            # two column tiles, the second ragged
     for seed in range(5):
@@ -151,7 +152,7 @@ def test_transposed_tile_equals_the_plain_tile_on_stress_inputs(kind, Kc):
         full = dg.det_gemm_fwd(A, B)
         full_t = dg.det_gemm_fwd_rhs_transposed(A, Wt)
         full_da = dg.det_gemm_da(dC, Bd)
-        for M in (1, 17, 64, 65, 128):
+        for M in (1, 8, 9, 16, 17, 64, 65, 128):
             assert bits_equal(dg.det_gemm_fwd(A[:M], B), full[:M]), (kind, Kc, seed, M, "fwd")
             assert bits_equal(dg.det_gemm_fwd_rhs_transposed(A[:M], Wt), full_t[:M]), (kind, Kc, seed, M, "rhs_t")
             assert bits_equal(dg.det_gemm_da(dC[:M], Bd), full_da[:M]), (kind, Kc, seed, M, "da")
