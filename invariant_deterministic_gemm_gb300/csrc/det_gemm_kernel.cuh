@@ -988,6 +988,31 @@ __device__ __forceinline__ void stage_role(const Params &p, const Smem<F32, SWAP
 // can miss a phase.
 constexpr int kSwapIssuers = 3;
 
+// Where the K-stages of one work unit come from: its problem, the first
+// contraction element of its part, and its tile's first row and column.
+struct UnitAt {
+    const Problem *pb;
+    int k0, m0, n0;
+};
+
+template <bool F32, bool GROUPED, bool SWAP>
+__device__ __forceinline__ UnitAt unit_at(const Params &p, int tl, int L)
+{
+    using C = Cfg<F32, SWAP>;
+    const int u = blockIdx.x + tl * gridDim.x;
+    const Problem &pb = p.prob[GROUPED ? problem_of(p, u) : 0];
+    const int ul = u - pb.first_unit;
+    const int t = fdiv(ul, p.div_parts);
+    const int part = ul - t * p.parts;
+    int mt, nt;
+    tile_coords(t, pb, p.n_tiles, mt, nt);
+    return UnitAt{&pb, part * L * kLeaf, mt * kBM, nt * C::BN};
+}
+
+// The copy warp keeps two cursors, the stage it copies and the stage it
+// prefetches into L2, and finds a unit's coordinates once per unit: a
+// per-stage recomputation (a chain of multiply-shift divisions) made this
+// warp the launch's bottleneck, at about 850 cycles per stage.
 template <int A_MAJOR, int B_MAJOR, bool F32, bool GROUPED, bool SWAP>
 __device__ __forceinline__ void copy_role(const Params &p, const Smem<F32, SWAP> &S)
 {
@@ -1002,56 +1027,48 @@ __device__ __forceinline__ void copy_role(const Params &p, const Smem<F32, SWAP>
     bool ok = true;
     if (p.force_timeout)
         ok = __all_sync(0xFFFFFFFFu, wait_bounded(S.never(), 0, S.abort_flag, p.status, p.timeout_ns, true));
+    constexpr int PF = kPrefetchRounds * C::STAGES;   // prefetch distance, stages
+    int tl = 0, ks = 0;                                // copy cursor: unit and K-stage
+    UnitAt at{};
+    if (total > 0) at = unit_at<F32, GROUPED, SWAP>(p, 0, L);
+    int tlp = 0, ksp = 0;                              // prefetch cursor, PF stages ahead
+    UnitAt atp{};
+    if (PF < total) {
+        tlp = fdiv(PF, p.div_stages);
+        ksp = PF - tlp * KS;
+        atp = unit_at<F32, GROUPED, SWAP>(p, tlp, L);
+    }
     for (int g = 0; ok && g < total; ++g) {
         const int s = g % C::STAGES;
         const uint32_t round = static_cast<uint32_t>(g / C::STAGES) & 1u;
-        const int tl = fdiv(g, p.div_stages);
-        const int ks = g - tl * KS;
-        const int u = blockIdx.x + tl * gridDim.x;
-        const Problem &pb = p.prob[GROUPED ? problem_of(p, u) : 0];
-        const int ul = u - pb.first_unit;
-        const int t = fdiv(ul, p.div_parts);
-        const int part = ul - t * p.parts;
-        int mt, nt;
-        tile_coords(t, pb, p.n_tiles, mt, nt);
         if (!warp_wait(S.empty(s), round ^ 1u, S.abort_flag, p.status, p.timeout_ns)) { ok = false; break; }
         const uint32_t full = S.full(s);
         const uint32_t a_dst = S.sA + s * C::A_STAGE;
         const uint32_t b_dst = S.sB + s * C::B_STAGE;
         if (leader) {
-            mbar_arrive_expect_tx(full, static_cast<uint32_t>(pb.stage_tx));
-            const int k0 = part * L * kLeaf + ks * kBK, m0 = mt * kBM, n0 = nt * C::BN;
+            mbar_arrive_expect_tx(full, static_cast<uint32_t>(at.pb->stage_tx));
+            const int k0 = at.k0 + ks * kBK;
             if constexpr (A_MAJOR == kKMajor) {
-                tma_load_2d(a_dst, &pb.tmap_a, full, k0, m0);
+                tma_load_2d(a_dst, &at.pb->tmap_a, full, k0, at.m0);
             } else {
-                tma_load_2d(a_dst, &pb.tmap_a, full, m0, k0);
-                tma_load_2d(a_dst + 8192, &pb.tmap_a, full, m0 + 64, k0);
+                tma_load_2d(a_dst, &at.pb->tmap_a, full, at.m0, k0);
+                tma_load_2d(a_dst + 8192, &at.pb->tmap_a, full, at.m0 + 64, k0);
             }
             if constexpr (B_MAJOR == kKMajor) {
-                tma_load_2d(b_dst, &pb.tmap_b, full, k0, n0);
+                tma_load_2d(b_dst, &at.pb->tmap_b, full, k0, at.n0);
             } else {
 #pragma unroll
                 for (int b = 0; b < C::B_COPY_COLS / 64; ++b)
-                    tma_load_2d(b_dst + 8192 * b, &pb.tmap_b, full, n0 + 64 * b, k0);
+                    tma_load_2d(b_dst + 8192 * b, &at.pb->tmap_b, full, at.n0 + 64 * b, k0);
             }
             if constexpr (SWAP) {
-                const int gp = g + kPrefetchRounds * C::STAGES;
-                if (gp < total) {
-                    const int tlp = fdiv(gp, p.div_stages);
-                    const int ksp = gp - tlp * KS;
-                    const int up = blockIdx.x + tlp * gridDim.x;
-                    const Problem &pbp = p.prob[GROUPED ? problem_of(p, up) : 0];
-                    const int ulp = up - pbp.first_unit;
-                    const int tp = fdiv(ulp, p.div_parts);
-                    const int partp = ulp - tp * p.parts;
-                    int mtp, ntp;
-                    tile_coords(tp, pbp, p.n_tiles, mtp, ntp);
-                    const int kp = partp * L * kLeaf + ksp * kBK, mp = mtp * kBM;
+                if (g + PF < total) {
+                    const int kp = atp.k0 + ksp * kBK;
                     if constexpr (A_MAJOR == kKMajor) {
-                        tma_prefetch_2d(&pbp.tmap_a, kp, mp);
+                        tma_prefetch_2d(&atp.pb->tmap_a, kp, atp.m0);
                     } else {
-                        tma_prefetch_2d(&pbp.tmap_a, mp, kp);
-                        if (mp + 64 < pbp.rows) tma_prefetch_2d(&pbp.tmap_a, mp + 64, kp);
+                        tma_prefetch_2d(&atp.pb->tmap_a, atp.m0, kp);
+                        if (atp.m0 + 64 < atp.pb->rows) tma_prefetch_2d(&atp.pb->tmap_a, atp.m0 + 64, kp);
                     }
                 }
             }
@@ -1059,6 +1076,14 @@ __device__ __forceinline__ void copy_role(const Params &p, const Smem<F32, SWAP>
         __syncwarp();
         loaded |= 1u << s;
         parity = (parity & ~(1u << s)) | (round << s);
+        if (++ks == KS) {
+            ks = 0;
+            if (++tl < my_units) at = unit_at<F32, GROUPED, SWAP>(p, tl, L);
+        }
+        if (++ksp == KS) {
+            ksp = 0;
+            if (++tlp < my_units) atp = unit_at<F32, GROUPED, SWAP>(p, tlp, L);
+        }
     }
     if (!ok) {
         for (int s = 0; s < C::STAGES; ++s)

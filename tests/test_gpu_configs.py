@@ -88,6 +88,11 @@ def test_lm_head_bf16_and_fp32_against_oracle_samples():
     part = dg.det_gemm_fwd_rhs_transposed(Ag[100:612], Wg)
     check()
     assert bits_equal(part, C[100:612])
+    # decode-sized slices take the transposed tile, about eight 128-column
+    # tiles per CTA
+    for lo, hi in ((100, 101), (100, 112), (100, 164)):
+        assert bits_equal(dg.det_gemm_fwd_rhs_transposed(Ag[lo:hi], Wg), C[lo:hi]), (lo, hi)
+    check()
     rows = [0, 1000, 2047]
     cols = np.sort(np.random.default_rng(0).choice(V, 3000, replace=False))
     Ab, Wb = W.bits(A), W.bits(Wt)

@@ -119,6 +119,25 @@ def test_normal_inputs_within_tolerance_of_oracle():
     assert_bf16_close(got_t, want_t, nodemax_t, K // 32, "rhs_transposed, 3 rows")
 
 
+def test_transposed_tile_with_several_units_per_cta():
+    """More output columns than 152 tiles of 128 hold: each CTA of a
+    transposed launch walks two or three tiles, with its copy warp's stage
+    and prefetch cursors crossing from one tile to the next (and a ragged
+    last tile). Rows 1, 9 and 64 (all three epilogue widths) must equal the
+    same rows of a 256-row plain-tile launch, through both transposed
+    instances."""
+    K, N = 256, 2 * 152 * 128 + 200
+    A = dev(W.randn_bf16((256, K), 1.0, 30101))
+    B = dev(W.randn_bf16((K, N), 0.05, 30102))
+    Wt = dev(W.randn_bf16((N, K), 0.05, 30103))
+    full = dg.det_gemm_fwd(A, B)
+    full_t = dg.det_gemm_fwd_rhs_transposed(A, Wt)
+    for M in (1, 9, 64):
+        assert bits_equal(dg.det_gemm_fwd(A[:M], B), full[:M]), (M, "fwd")
+        assert bits_equal(dg.det_gemm_fwd_rhs_transposed(A[:M], Wt), full_t[:M]), (M, "rhs_t")
+    check()
+
+
 ADV_KC = [32, 96, 4096, 14336, 32768]
 
 
