@@ -31,8 +31,9 @@
 // columns, and its N side (64) holds the rows. 384 threads: warps 0-7
 // epilogue, two per scheduler, each owning one output column per lane and
 // 32 rows (a warp whose 32 rows are all past the output's only hands the
-// accumulators back); warp 8 copies every stage in with TMA and prefetches
-// the weight tiles of later stages into L2, and warps 9-11 issue the MMAs,
+// accumulators back); warp 8 copies every stage in with TMA (and, for a
+// weight stored [K, N], prefetches the weight tiles of later stages into
+// L2), and warps 9-11 issue the MMAs,
 // each into its own accumulator and without a turn order. The accumulators
 // and all seven pending slots fit in TMEM. With at most 8 (16) output rows
 // the epilogue loads, rounds and merges only the 8 (16) columns of each
@@ -81,7 +82,7 @@
 namespace detg {
 
 constexpr int kStatusTimeout = 6;   // DET_GEMM_ERR_TIMEOUT
-constexpr int kPrefetchRounds = 1;  // transposed tile: L2 prefetch distance, in rounds of the stage ring
+constexpr int kPrefetchRounds = 1;  // transposed tile, weight MN-major: L2 prefetch distance, in rounds of the stage ring
 
 
 // ------------------------------------------------------------------ config
@@ -894,32 +895,6 @@ __device__ __forceinline__ void stage_role(const Params &p, const Smem<F32, SWAP
                 for (int b = 0; b < C::B_COPY_COLS / 64; ++b)
                     tma_load_2d(b_dst + 8192 * b, &pb.tmap_b, full, n0 + 64 * b, k0);
             }
-            if constexpr (SWAP) {
-                // Transposed tile (few output rows): the launch streams the
-                // A operand from DRAM with little arithmetic per byte, so
-                // four slots in flight leave each SM waiting on DRAM
-                // latency. The A tile this warp will copy kPrefetchRounds
-                // rounds from now is fetched into L2 already.
-                const int gp = g + kPrefetchRounds * kStageWarps;
-                if (gp < total) {
-                    const int tlp = fdiv(gp, p.div_stages);
-                    const int ksp = gp - tlp * KS;
-                    const int up = blockIdx.x + tlp * gridDim.x;
-                    const Problem &pbp = p.prob[GROUPED ? problem_of(p, up) : 0];
-                    const int ulp = up - pbp.first_unit;
-                    const int tp = fdiv(ulp, p.div_parts);
-                    const int partp = ulp - tp * p.parts;
-                    int mtp, ntp;
-                    tile_coords(tp, pbp, p.n_tiles, mtp, ntp);
-                    const int kp = partp * L * kLeaf + ksp * kBK, mp = mtp * kBM;
-                    if constexpr (A_MAJOR == kKMajor) {
-                        tma_prefetch_2d(&pbp.tmap_a, kp, mp);
-                    } else {
-                        tma_prefetch_2d(&pbp.tmap_a, mp, kp);
-                        if (mp + 64 < pbp.rows) tma_prefetch_2d(&pbp.tmap_a, mp + 64, kp);
-                    }
-                }
-            }
         }
         __syncwarp();
         tma_pending = true;
@@ -1061,7 +1036,11 @@ __device__ __forceinline__ void copy_role(const Params &p, const Smem<F32, SWAP>
                 for (int b = 0; b < C::B_COPY_COLS / 64; ++b)
                     tma_load_2d(b_dst + 8192 * b, &at.pb->tmap_b, full, at.n0 + 64 * b, k0);
             }
-            if constexpr (SWAP) {
+            // L2 prefetch of the weight PF stages ahead: for a weight stored
+            // [K, N] only (QKV at one row 31.4 -> 29.3 us); with the weight
+            // stored [N, K] the launches ran faster without it (64 rows
+            // 35.5 -> 33.6 us), and sixteen stages ahead slower still.
+            if constexpr (SWAP && A_MAJOR != kKMajor) {
                 if (g + PF < total) {
                     const int kp = atp.k0 + ksp * kBK;
                     if constexpr (A_MAJOR == kKMajor) {
