@@ -1036,19 +1036,15 @@ __device__ __forceinline__ void copy_role(const Params &p, const Smem<F32, SWAP>
                 for (int b = 0; b < C::B_COPY_COLS / 64; ++b)
                     tma_load_2d(b_dst + 8192 * b, &at.pb->tmap_b, full, at.n0 + 64 * b, k0);
             }
-            // L2 prefetch of the weight PF stages ahead: for a weight stored
-            // [K, N] only (QKV at one row 31.4 -> 29.3 us); with the weight
-            // stored [N, K] the launches ran faster without it (64 rows
-            // 35.5 -> 33.6 us), and sixteen stages ahead slower still.
+            // L2 prefetch of the weight PF stages ahead, for a weight stored
+            // [K, N] (MN-major A) only: with the weight stored [N, K] the
+            // launches ran faster without it (64 rows 35.5 -> 33.6 us), and
+            // with it sixteen stages ahead slower still.
             if constexpr (SWAP && A_MAJOR != kKMajor) {
                 if (g + PF < total) {
                     const int kp = atp.k0 + ksp * kBK;
-                    if constexpr (A_MAJOR == kKMajor) {
-                        tma_prefetch_2d(&atp.pb->tmap_a, kp, atp.m0);
-                    } else {
-                        tma_prefetch_2d(&atp.pb->tmap_a, atp.m0, kp);
-                        if (atp.m0 + 64 < atp.pb->rows) tma_prefetch_2d(&atp.pb->tmap_a, atp.m0 + 64, kp);
-                    }
+                    tma_prefetch_2d(&atp.pb->tmap_a, atp.m0, kp);
+                    if (atp.m0 + 64 < atp.pb->rows) tma_prefetch_2d(&atp.pb->tmap_a, atp.m0 + 64, kp);
                 }
             }
         }
