@@ -12,10 +12,12 @@
  *       T(lo, hi) = leaf[lo]                         if hi - lo == 1
  *                 = bf16(T(lo, mid) + T(mid, hi))    otherwise, mid = (lo + hi) / 2
  *   (integer division; for an odd range the left child holds the smaller
- *   half). No split-K and no TF32: the bits of an output element depend only
- *   on its own row of the left operand and its own column of the right one,
- *   never on M, on how rows are chunked or padded, or on which CTA computed
- *   it. When L is even, a contiguous half-K product is one child of the root,
+ *   half). No TF32, and no split-K that combines partial sums in a
+ *   launch-dependent order (a launch with few output tiles may split its
+ *   contraction, but only at nodes of this tree, which gives the same bits):
+ *   the bits of an output element depend only on its own row of the left
+ *   operand and its own column of the right one, never on M, on how rows are
+ *   chunked or padded, or on which CTA computed it. When L is even, a contiguous half-K product is one child of the root,
  *   so bf16(first_half + second_half) equals the full product bit for bit.
  *
  *   How an output is tiled is an implementation choice that never shows in
@@ -48,12 +50,16 @@
  *   - Outputs must not overlap inputs (DET_GEMM_ERR_INVALID_ARG otherwise).
  *   - A device-side failure (a bounded wait that expired) is reported by
  *     det_gemm_check(), not by the launching call.
- *   - The library allocates no device memory per call. It keeps one small
- *     device scratch buffer per (device, stream) it has launched on (one CTA
- *     per SM x 144 KiB: the tree's most rarely touched pending partials), created
- *     on the first launch on that stream and reused by every later one, so
- *     launches on different streams never share it. det_gemm_shutdown()
- *     releases them.
+ *   - The library keeps one device scratch buffer per (device, stream) it has
+ *     launched on: one CTA per SM x 144 KiB for the tree's most rarely
+ *     touched pending partials, followed, when a launch needs them, by the
+ *     part products of a launch that splits its contraction (parts x the
+ *     output's size) and the grouped row reduction's per-tile slots. It is
+ *     created on the first launch on that stream and reused by every later
+ *     one; a launch that needs more replaces it with a larger one
+ *     (cudaFree, which waits for the device, then cudaMalloc). Launches on
+ *     different streams never share it. det_gemm_shutdown() releases them;
+ *     det_gemm_fwd_noalloc allocates nothing.
  */
 #ifndef DET_GEMM_H
 #define DET_GEMM_H
